@@ -1,0 +1,612 @@
+// Host side of the C ABI declared in include/dobb.h: argument checks, the
+// state layout inside the caller's device buffer, the grouped work lists
+// (one list per phase, cost-sorted, consumed by persistent CTAs) and the
+// per-phase launches.
+//
+// "Dobb: Shard-Local Preconditioning in Block-Diagonal Eigenbases": the
+// per-matrix state is the block second moments (Table 3 caption: n^2/B
+// entries), the block bases (Table 18: fp32 accumulation and basis storage,
+// 8 n^2/B bytes with both), and the momentum; the refresh runs inside the
+// optimizer call every T steps (Table 5 caption, Table 21 footnote a).
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "dobb_internal.cuh"
+
+using namespace dobb;
+
+namespace {
+
+thread_local std::string g_err;
+
+dobb_status fail(dobb_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return st;
+}
+
+#define CUDA_TRY(expr)                                                                   \
+  do {                                                                                   \
+    cudaError_t e_ = (expr);                                                             \
+    if (e_ != cudaSuccess) return fail(DOBB_ERR_CUDA, "%s: %s", #expr, cudaGetErrorString(e_)); \
+  } while (0)
+
+constexpr size_t kAlign = 256;
+size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+struct Layout {
+  size_t a_floats = 0, lam_floats = 0, m_floats = 0;
+  int64_t nblocks = 0;
+  size_t off_A = 0, off_Q = 0, off_lam = 0, off_M = 0, off_flags = 0, off_stats = 0,
+         off_check = 0, off_info = 0, off_tiles = 0, off_scratch = 0, total = 0;
+  size_t n_tiles = 0;
+};
+
+struct Chunk {
+  int mat_base = 0, mat_end = 0;
+  int step_off = 0, step_n = 0;
+  int syrk_off = 0, syrk_n = 0;
+  int eig_off = 0, eig_n = 0;
+  int max_k = 1;
+};
+
+// Work lists of all phases, in the order they are stored on the device.
+struct WorkLists {
+  std::vector<Tile> tiles;
+  std::vector<Chunk> chunks;
+  int blocks_off = 0, blocks_n = 0;  // every (matrix, block) once, by matrix
+};
+
+bool validate_shapes(int num, const int64_t* m, const int64_t* n, int B) {
+  if (num <= 0 || !m || !n) {
+    fail(DOBB_ERR_INVALID_ARG, "num_matrices must be > 0 and shape arrays non-NULL");
+    return false;
+  }
+  if (B <= 0) {
+    fail(DOBB_ERR_INVALID_ARG, "B must be > 0 (got %d)", B);
+    return false;
+  }
+  for (int i = 0; i < num; ++i) {
+    if (m[i] <= 0 || n[i] <= 0) {
+      fail(DOBB_ERR_INVALID_ARG, "matrix %d has shape %lld x %lld", i, (long long)m[i], (long long)n[i]);
+      return false;
+    }
+    if (n[i] % B != 0) {
+      fail(DOBB_ERR_INVALID_ARG, "matrix %d: n=%lld is not divisible by B=%d", i, (long long)n[i], B);
+      return false;
+    }
+    const int64_t k = n[i] / B;
+    if (k > kMaxK) {
+      fail(DOBB_ERR_UNSUPPORTED, "matrix %d: block width k=%lld exceeds %d", i, (long long)k, kMaxK);
+      return false;
+    }
+    if (m[i] > (int64_t)1 << 31) {
+      fail(DOBB_ERR_UNSUPPORTED, "matrix %d: m=%lld too large", i, (long long)m[i]);
+      return false;
+    }
+  }
+  return true;
+}
+
+WorkLists build_work(int num, const int64_t* m, const int64_t* n, int B) {
+  WorkLists wl;
+  const int TM = step_rows_per_tile();
+  const int ST = syrk_tile();
+  for (int c0 = 0; c0 < num; c0 += kMaxMatPerLaunch) {
+    Chunk ch;
+    ch.mat_base = c0;
+    ch.mat_end = std::min(num, c0 + kMaxMatPerLaunch);
+    std::vector<std::pair<int64_t, Tile>> v;
+    // step tiles: (matrix, block, row0); cost ~ rows * k
+    for (int i = ch.mat_base; i < ch.mat_end; ++i) {
+      const int k = (int)(n[i] / B);
+      ch.max_k = std::max(ch.max_k, k);
+      for (int b = 0; b < B; ++b)
+        for (int64_t r = 0; r < m[i]; r += TM) v.push_back({(int64_t)k, Tile{i, b, (int)r, 0}});
+    }
+    std::stable_sort(v.begin(), v.end(), [](auto& x, auto& y) { return x.first > y.first; });
+    ch.step_off = (int)wl.tiles.size();
+    ch.step_n = (int)v.size();
+    for (auto& e : v) wl.tiles.push_back(e.second);
+    // syrk tiles: upper triangle of ceil(k / ST)^2 output tiles per block
+    v.clear();
+    for (int i = ch.mat_base; i < ch.mat_end; ++i) {
+      const int k = (int)(n[i] / B);
+      const int nt = (k + ST - 1) / ST;
+      for (int b = 0; b < B; ++b)
+        for (int ti = 0; ti < nt; ++ti)
+          for (int tj = ti; tj < nt; ++tj) v.push_back({(int64_t)k, Tile{i, b, ti, tj}});
+    }
+    std::stable_sort(v.begin(), v.end(), [](auto& x, auto& y) { return x.first > y.first; });
+    ch.syrk_off = (int)wl.tiles.size();
+    ch.syrk_n = (int)v.size();
+    for (auto& e : v) wl.tiles.push_back(e.second);
+    // eigen items: one per block, largest k first (cost ~ k^3)
+    v.clear();
+    for (int i = ch.mat_base; i < ch.mat_end; ++i) {
+      const int k = (int)(n[i] / B);
+      for (int b = 0; b < B; ++b) v.push_back({(int64_t)k, Tile{i, b, 0, 0}});
+    }
+    std::stable_sort(v.begin(), v.end(), [](auto& x, auto& y) { return x.first > y.first; });
+    ch.eig_off = (int)wl.tiles.size();
+    ch.eig_n = (int)v.size();
+    for (auto& e : v) wl.tiles.push_back(e.second);
+    wl.chunks.push_back(ch);
+  }
+  wl.blocks_off = (int)wl.tiles.size();
+  for (int i = 0; i < num; ++i)
+    for (int b = 0; b < B; ++b) wl.tiles.push_back(Tile{i, b, 0, 0});
+  wl.blocks_n = (int)wl.tiles.size() - wl.blocks_off;
+  return wl;
+}
+
+Layout compute_layout(int num, const int64_t* m, const int64_t* n, int B, size_t n_tiles) {
+  Layout L;
+  for (int i = 0; i < num; ++i) {
+    const int64_t k = n[i] / B;
+    L.a_floats += (size_t)B * k * k;
+    L.lam_floats += (size_t)B * k;
+    L.m_floats += (size_t)m[i] * n[i];
+    L.nblocks += B;
+  }
+  size_t off = 0;
+  L.off_A = off;      off = align_up(off + 4 * L.a_floats);
+  L.off_Q = off;      off = align_up(off + 4 * L.a_floats);
+  L.off_lam = off;    off = align_up(off + 4 * L.lam_floats);
+  L.off_M = off;      off = align_up(off + 4 * L.m_floats);
+  L.off_flags = off;  off = align_up(off + 4 * (size_t)L.nblocks);
+  L.off_stats = off;  off = align_up(off + 16 * (size_t)L.nblocks);
+  L.off_check = off;  off = align_up(off + 12 * (size_t)L.nblocks);
+  L.off_info = off;   off = align_up(off + sizeof(MatInfo) * (size_t)num);
+  L.off_tiles = off;  off = align_up(off + sizeof(Tile) * n_tiles);
+  L.off_scratch = off; off = align_up(off + 8 * L.a_floats);
+  L.total = off;
+  L.n_tiles = n_tiles;
+  return L;
+}
+
+}  // namespace
+
+struct dobb_ctx {
+  int device = 0;
+  int num = 0, B = 1, T = 0;
+  float beta1 = 0.95f, beta2 = 0.99f, scale_s = 1.f;
+  dobb_dtype pdt = DOBB_F32, adt = DOBB_F32;
+  std::vector<int64_t> m, n;
+  std::vector<MatInfo> info;
+  WorkLists wl;
+  Layout L;
+  char* base = nullptr;
+  size_t bytes = 0;
+  int64_t t = 0;
+  int max_sweeps = 40;
+  float tol = 0.f;
+  int sm_count = 1;
+  size_t smem_limit = 0;
+  size_t smem_per_sm = 0;
+  int64_t launches = 0;
+  std::vector<float> check_host;
+
+  float* A() const { return reinterpret_cast<float*>(base + L.off_A); }
+  float* Q() const { return reinterpret_cast<float*>(base + L.off_Q); }
+  float* lam() const { return reinterpret_cast<float*>(base + L.off_lam); }
+  float* M() const { return reinterpret_cast<float*>(base + L.off_M); }
+  uint32_t* flags() const { return reinterpret_cast<uint32_t*>(base + L.off_flags); }
+  float* stats() const { return reinterpret_cast<float*>(base + L.off_stats); }
+  float* check() const { return reinterpret_cast<float*>(base + L.off_check); }
+  MatInfo* dinfo() const { return reinterpret_cast<MatInfo*>(base + L.off_info); }
+  Tile* dtiles() const { return reinterpret_cast<Tile*>(base + L.off_tiles); }
+  float* scratch() const { return reinterpret_cast<float*>(base + L.off_scratch); }
+};
+
+namespace {
+
+dobb_status check_handle(dobb_handle h) {
+  if (!h) return fail(DOBB_ERR_STATE, "NULL handle");
+  int dev = -1;
+  CUDA_TRY(cudaGetDevice(&dev));
+  if (dev != h->device)
+    return fail(DOBB_ERR_STATE, "current device %d differs from the handle's device %d", dev, h->device);
+  return DOBB_OK;
+}
+
+dobb_status do_refresh(dobb_handle h, cudaStream_t s) {
+  for (const Chunk& ch : h->wl.chunks) {
+    if (ch.eig_n == 0) continue;
+    // blocks whose U and V fit in shared memory keep them there; larger
+    // blocks use the global scratch area and only sort in shared memory
+    size_t smem = 0;
+    for (int i = ch.mat_base; i < ch.mat_end; ++i) {
+      const int k = (int)(h->n[i] / h->B);
+      const size_t full = jacobi_smem_for(k);
+      smem = std::max(smem, full <= h->smem_limit ? full : jacobi_sort_smem_for(k));
+    }
+    EigArgs a{};
+    a.info = h->dinfo();
+    a.tiles = h->dtiles() + ch.eig_off;
+    a.num_tiles = ch.eig_n;
+    a.max_sweeps = h->max_sweeps;
+    a.A = h->A();
+    a.Q = h->Q();
+    a.lam = h->lam();
+    a.scratch = h->scratch();
+    a.flags = h->flags();
+    a.stats = h->stats();
+    a.tol = h->tol;
+    const int by_smem = std::max(1, (int)(h->smem_per_sm / (smem + 1024)));
+    const int g = std::max(1, std::min(ch.eig_n, h->sm_count * std::min(jacobi_ctas_per_sm(), by_smem)));
+    cudaError_t e = launch_jacobi(a, g, smem, s);
+    if (e != cudaSuccess) return fail(DOBB_ERR_CUDA, "eigen launch: %s", cudaGetErrorString(e));
+    ++h->launches;
+  }
+  return DOBB_OK;
+}
+
+dobb_status do_step(dobb_handle h, void* const* W, const void* const* G, float lr,
+                    int8_t* const* S_out, cudaStream_t s) {
+  if (!W || !G) return fail(DOBB_ERR_INVALID_ARG, "W and G arrays must be non-NULL");
+  for (int i = 0; i < h->num; ++i)
+    if (!W[i] || !G[i]) return fail(DOBB_ERR_INVALID_ARG, "W[%d] or G[%d] is NULL", i, i);
+  if (!(lr == lr)) return fail(DOBB_ERR_INVALID_ARG, "lr is NaN");
+  if (h->T > 0 && h->t % h->T == 0) {
+    dobb_status st = do_refresh(h, s);
+    if (st != DOBB_OK) return st;
+  }
+  // zero the per-step sums (slots 0 and 1 of each block's 4 stats)
+  CUDA_TRY(cudaMemset2DAsync(h->stats(), 16, 0, 8, (size_t)h->L.nblocks, s));
+  for (const Chunk& ch : h->wl.chunks) {
+    if (ch.step_n == 0) continue;
+    StepArgs a{};
+    a.info = h->dinfo();
+    a.tiles = h->dtiles() + ch.step_off;
+    a.num_tiles = ch.step_n;
+    a.mat_base = ch.mat_base;
+    a.Q = h->Q();
+    a.M = h->M();
+    a.flags = h->flags();
+    a.stats = h->stats();
+    a.beta1 = h->beta1;
+    a.lr_s = lr * h->scale_s;
+    for (int i = ch.mat_base; i < ch.mat_end; ++i) {
+      a.W[i - ch.mat_base] = W[i];
+      a.G[i - ch.mat_base] = G[i];
+      a.S[i - ch.mat_base] = S_out ? S_out[i] : nullptr;
+    }
+    const size_t smem = step_smem_for(ch.max_k);
+    if (smem > h->smem_limit)
+      return fail(DOBB_ERR_UNSUPPORTED, "block width %d needs %zu bytes of shared memory", ch.max_k, smem);
+    const int by_smem = std::max(1, (int)(h->smem_per_sm / (smem + 1024)));
+    const int g = std::max(1, std::min(ch.step_n, h->sm_count * std::min(4, by_smem)));
+    cudaError_t e = launch_step_ffma(a, h->pdt, g, smem, s);
+    if (e != cudaSuccess) return fail(DOBB_ERR_CUDA, "step launch: %s", cudaGetErrorString(e));
+    ++h->launches;
+  }
+  h->t += 1;
+  return DOBB_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* dobb_last_error(void) { return g_err.c_str(); }
+
+size_t dobb_state_bytes(int num_matrices, const int64_t* m, const int64_t* n, int B) {
+  if (!validate_shapes(num_matrices, m, n, B)) return 0;
+  WorkLists wl = build_work(num_matrices, m, n, B);
+  return compute_layout(num_matrices, m, n, B, wl.tiles.size()).total;
+}
+
+dobb_status dobb_create(dobb_handle* out, int num_matrices, const int64_t* m, const int64_t* n,
+                        int B, float beta1, float beta2, int refresh_period, float scale_s,
+                        dobb_dtype param_dtype, dobb_dtype act_dtype, void* state_mem,
+                        size_t state_bytes, void* stream) {
+  g_err.clear();
+  if (!out) return fail(DOBB_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  if (!validate_shapes(num_matrices, m, n, B)) return DOBB_ERR_INVALID_ARG;
+  if (!(beta1 >= 0.f && beta1 < 1.f) || !(beta2 >= 0.f && beta2 < 1.f))
+    return fail(DOBB_ERR_INVALID_ARG, "beta1=%g beta2=%g must lie in [0, 1)", beta1, beta2);
+  if (refresh_period < 0) return fail(DOBB_ERR_INVALID_ARG, "refresh_period must be >= 0");
+  if (!(scale_s == scale_s)) return fail(DOBB_ERR_INVALID_ARG, "scale_s is NaN");
+  if ((param_dtype != DOBB_F32 && param_dtype != DOBB_BF16) ||
+      (act_dtype != DOBB_F32 && act_dtype != DOBB_BF16))
+    return fail(DOBB_ERR_INVALID_ARG, "unknown dtype");
+  if (!state_mem) return fail(DOBB_ERR_INVALID_ARG, "state_mem is NULL");
+  if (reinterpret_cast<uintptr_t>(state_mem) % kAlign != 0)
+    return fail(DOBB_ERR_INVALID_ARG, "state_mem must be %zu-byte aligned", kAlign);
+
+  dobb_ctx* h = new dobb_ctx();
+  h->num = num_matrices;
+  h->B = B;
+  h->beta1 = beta1;
+  h->beta2 = beta2;
+  h->T = refresh_period;
+  h->scale_s = scale_s;
+  h->pdt = param_dtype;
+  h->adt = act_dtype;
+  h->m.assign(m, m + num_matrices);
+  h->n.assign(n, n + num_matrices);
+  h->wl = build_work(num_matrices, m, n, B);
+  h->L = compute_layout(num_matrices, m, n, B, h->wl.tiles.size());
+  if (state_bytes < h->L.total) {
+    size_t need = h->L.total;
+    delete h;
+    return fail(DOBB_ERR_STATE, "state buffer of %zu bytes is smaller than the %zu required",
+                state_bytes, need);
+  }
+  h->base = static_cast<char*>(state_mem);
+  h->bytes = state_bytes;
+
+  cudaError_t e = cudaGetDevice(&h->device);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&h->sm_count, cudaDevAttrMultiProcessorCount, h->device);
+  int optin = 0, per_sm = 0;
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, h->device);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, h->device);
+  h->smem_per_sm = (size_t)per_sm;
+  if (e != cudaSuccess) {
+    delete h;
+    return fail(DOBB_ERR_CUDA, "device query: %s", cudaGetErrorString(e));
+  }
+  h->smem_limit = (size_t)optin - 2048;  // room for static shared memory
+  if ((e = configure_jacobi(h->smem_limit)) != cudaSuccess ||
+      (e = configure_step(h->smem_limit)) != cudaSuccess) {
+    delete h;
+    return fail(DOBB_ERR_CUDA, "kernel configuration: %s", cudaGetErrorString(e));
+  }
+
+  // per-matrix metadata
+  int64_t aoff = 0, loff = 0, moff = 0;
+  int32_t blk = 0;
+  for (int i = 0; i < num_matrices; ++i) {
+    MatInfo mi{};
+    mi.m = m[i];
+    mi.n = n[i];
+    mi.k = (int32_t)(n[i] / B);
+    mi.B = B;
+    mi.blk0 = blk;
+    mi.a_off = aoff;
+    mi.lam_off = loff;
+    mi.m_off = moff;
+    h->info.push_back(mi);
+    aoff += (int64_t)B * mi.k * mi.k;
+    loff += (int64_t)B * mi.k;
+    moff += m[i] * n[i];
+    blk += B;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const Layout& L = h->L;
+  e = cudaMemcpyAsync(h->dinfo(), h->info.data(), sizeof(MatInfo) * h->info.size(),
+                      cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(h->dtiles(), h->wl.tiles.data(), sizeof(Tile) * h->wl.tiles.size(),
+                        cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(h->base + L.off_A, 0, 4 * L.a_floats, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(h->base + L.off_M, 0, 4 * L.m_floats, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(h->base + L.off_flags, 0, L.off_info - L.off_flags, s);
+  if (e == cudaSuccess) {
+    const int g = std::max(1, std::min(h->wl.blocks_n, h->sm_count * 4));
+    e = launch_init_bases(h->Q(), h->lam(), h->dinfo(), h->dtiles() + h->wl.blocks_off,
+                          h->wl.blocks_n, g, s);
+    ++h->launches;
+  }
+  // the host arrays above must outlive the asynchronous copies: they belong
+  // to the handle; make the copies complete before returning anyway so the
+  // caller may reuse its shape arrays and the first call sees a ready state.
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) {
+    delete h;
+    return fail(DOBB_ERR_CUDA, "state initialisation: %s", cudaGetErrorString(e));
+  }
+  *out = h;
+  return DOBB_OK;
+}
+
+dobb_status dobb_destroy(dobb_handle h) {
+  if (!h) return fail(DOBB_ERR_STATE, "NULL handle");
+  delete h;
+  return DOBB_OK;
+}
+
+dobb_status dobb_accumulate_moments(dobb_handle h, const void* const* X, const int64_t* N,
+                                    void* stream) {
+  dobb_status st = check_handle(h);
+  if (st != DOBB_OK) return st;
+  if (!X || !N) return fail(DOBB_ERR_INVALID_ARG, "X and N arrays must be non-NULL");
+  for (int i = 0; i < h->num; ++i)
+    if (N[i] < 0) return fail(DOBB_ERR_INVALID_ARG, "N[%d] < 0", i);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  for (const Chunk& ch : h->wl.chunks) {
+    if (ch.syrk_n == 0) continue;
+    AccArgs a{};
+    a.info = h->dinfo();
+    a.tiles = h->dtiles() + ch.syrk_off;
+    a.num_tiles = ch.syrk_n;
+    a.mat_base = ch.mat_base;
+    a.A = h->A();
+    a.flags = h->flags();
+    a.beta2 = h->beta2;
+    for (int i = ch.mat_base; i < ch.mat_end; ++i) {
+      a.X[i - ch.mat_base] = X[i];
+      a.N[i - ch.mat_base] = X[i] ? N[i] : 0;
+    }
+    const int g = std::max(1, std::min(ch.syrk_n, h->sm_count * 4));
+    cudaError_t e = launch_syrk_ema(a, h->adt, g, s);
+    if (e != cudaSuccess) return fail(DOBB_ERR_CUDA, "accumulate launch: %s", cudaGetErrorString(e));
+    ++h->launches;
+  }
+  return DOBB_OK;
+}
+
+dobb_status dobb_refresh_bases(dobb_handle h, void* stream) {
+  dobb_status st = check_handle(h);
+  if (st != DOBB_OK) return st;
+  return do_refresh(h, static_cast<cudaStream_t>(stream));
+}
+
+dobb_status dobb_step(dobb_handle h, void* const* W, const void* const* G, float lr, void* stream) {
+  dobb_status st = check_handle(h);
+  if (st != DOBB_OK) return st;
+  return do_step(h, W, G, lr, nullptr, static_cast<cudaStream_t>(stream));
+}
+
+dobb_status dobb_step_with_signs(dobb_handle h, void* const* W, const void* const* G, float lr,
+                                 int8_t* const* S_out, void* stream) {
+  dobb_status st = check_handle(h);
+  if (st != DOBB_OK) return st;
+  if (!S_out) return fail(DOBB_ERR_INVALID_ARG, "S_out is NULL");
+  return do_step(h, W, G, lr, S_out, static_cast<cudaStream_t>(stream));
+}
+
+dobb_status dobb_get_step(dobb_handle h, int64_t* t) {
+  if (!h || !t) return fail(DOBB_ERR_INVALID_ARG, "NULL argument");
+  *t = h->t;
+  return DOBB_OK;
+}
+
+dobb_status dobb_set_step(dobb_handle h, int64_t t) {
+  if (!h || t < 0) return fail(DOBB_ERR_INVALID_ARG, "bad handle or negative step");
+  h->t = t;
+  return DOBB_OK;
+}
+
+dobb_status dobb_set_jacobi(dobb_handle h, int max_sweeps, float tol) {
+  if (!h || max_sweeps < 1 || !(tol >= 0.f)) return fail(DOBB_ERR_INVALID_ARG, "bad eigensolver settings");
+  h->max_sweeps = max_sweeps;
+  h->tol = tol;
+  return DOBB_OK;
+}
+
+dobb_status dobb_state_tensor(dobb_handle h, dobb_tensor which, int matrix, void** dev_ptr,
+                              size_t* bytes) {
+  if (!h || !dev_ptr || !bytes) return fail(DOBB_ERR_INVALID_ARG, "NULL argument");
+  if (matrix < -1 || matrix >= h->num) return fail(DOBB_ERR_INVALID_ARG, "matrix %d out of range", matrix);
+  const MatInfo* mi = matrix >= 0 ? &h->info[matrix] : nullptr;
+  switch (which) {
+    case DOBB_T_MOMENTS:
+    case DOBB_T_BASES: {
+      float* base = which == DOBB_T_MOMENTS ? h->A() : h->Q();
+      if (mi) {
+        *dev_ptr = base + mi->a_off;
+        *bytes = 4 * (size_t)mi->B * mi->k * mi->k;
+      } else {
+        *dev_ptr = base;
+        *bytes = 4 * h->L.a_floats;
+      }
+      return DOBB_OK;
+    }
+    case DOBB_T_EIGVALS:
+      *dev_ptr = mi ? h->lam() + mi->lam_off : h->lam();
+      *bytes = mi ? 4 * (size_t)mi->B * mi->k : 4 * h->L.lam_floats;
+      return DOBB_OK;
+    case DOBB_T_MOMENTUM:
+      *dev_ptr = mi ? h->M() + mi->m_off : h->M();
+      *bytes = mi ? 4 * (size_t)(mi->m * mi->n) : 4 * h->L.m_floats;
+      return DOBB_OK;
+    case DOBB_T_FLAGS:
+      *dev_ptr = mi ? h->flags() + mi->blk0 : h->flags();
+      *bytes = 4 * (mi ? (size_t)mi->B : (size_t)h->L.nblocks);
+      return DOBB_OK;
+    case DOBB_T_STATS:
+      *dev_ptr = mi ? h->stats() + 4 * (size_t)mi->blk0 : h->stats();
+      *bytes = 16 * (mi ? (size_t)mi->B : (size_t)h->L.nblocks);
+      return DOBB_OK;
+  }
+  return fail(DOBB_ERR_INVALID_ARG, "unknown tensor %d", (int)which);
+}
+
+int64_t dobb_num_blocks(dobb_handle h) { return h ? h->L.nblocks : -1; }
+
+int64_t dobb_block_offset(dobb_handle h, int matrix) {
+  if (!h || matrix < 0 || matrix >= h->num) return -1;
+  return h->info[matrix].blk0;
+}
+
+dobb_status dobb_get_block_flags(dobb_handle h, uint32_t* host_out, void* stream) {
+  dobb_status st = check_handle(h);
+  if (st != DOBB_OK) return st;
+  if (!host_out) return fail(DOBB_ERR_INVALID_ARG, "host_out is NULL");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  CUDA_TRY(cudaMemcpyAsync(host_out, h->flags(), 4 * (size_t)h->L.nblocks, cudaMemcpyDeviceToHost, s));
+  CUDA_TRY(cudaStreamSynchronize(s));
+  return DOBB_OK;
+}
+
+dobb_status dobb_clear_block_flags(dobb_handle h, void* stream) {
+  dobb_status st = check_handle(h);
+  if (st != DOBB_OK) return st;
+  CUDA_TRY(cudaMemsetAsync(h->flags(), 0, 4 * (size_t)h->L.nblocks, static_cast<cudaStream_t>(stream)));
+  return DOBB_OK;
+}
+
+dobb_status dobb_get_block_stats(dobb_handle h, float* host_out, void* stream) {
+  dobb_status st = check_handle(h);
+  if (st != DOBB_OK) return st;
+  if (!host_out) return fail(DOBB_ERR_INVALID_ARG, "host_out is NULL");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  CUDA_TRY(cudaMemcpyAsync(host_out, h->stats(), 16 * (size_t)h->L.nblocks, cudaMemcpyDeviceToHost, s));
+  CUDA_TRY(cudaStreamSynchronize(s));
+  return DOBB_OK;
+}
+
+dobb_status dobb_check_bases(dobb_handle h, float* host_out, void* stream) {
+  dobb_status st = check_handle(h);
+  if (st != DOBB_OK) return st;
+  if (!host_out) return fail(DOBB_ERR_INVALID_ARG, "host_out is NULL");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  CheckArgs a{};
+  a.info = h->dinfo();
+  a.tiles = h->dtiles() + h->wl.blocks_off;
+  a.num_tiles = h->wl.blocks_n;
+  a.A = h->A();
+  a.Q = h->Q();
+  a.lam = h->lam();
+  a.out = h->check();
+  const int g = std::max(1, std::min(a.num_tiles, h->sm_count * 8));
+  cudaError_t e = launch_check(a, g, s);
+  if (e != cudaSuccess) return fail(DOBB_ERR_CUDA, "check launch: %s", cudaGetErrorString(e));
+  ++h->launches;
+  CUDA_TRY(cudaMemcpyAsync(host_out, h->check(), 12 * (size_t)h->L.nblocks, cudaMemcpyDeviceToHost, s));
+  CUDA_TRY(cudaStreamSynchronize(s));
+  return DOBB_OK;
+}
+
+size_t dobb_checkpoint_bytes(dobb_handle h) { return h ? h->L.off_stats - h->L.off_A : 0; }
+
+dobb_status dobb_get_state(dobb_handle h, void* dst_dev, size_t dst_bytes, int64_t* t_out,
+                           void* stream) {
+  dobb_status st = check_handle(h);
+  if (st != DOBB_OK) return st;
+  const size_t need = dobb_checkpoint_bytes(h);
+  if (!dst_dev || dst_bytes < need)
+    return fail(DOBB_ERR_INVALID_ARG, "checkpoint buffer needs %zu bytes", need);
+  CUDA_TRY(cudaMemcpyAsync(dst_dev, h->base + h->L.off_A, need, cudaMemcpyDeviceToDevice,
+                           static_cast<cudaStream_t>(stream)));
+  if (t_out) *t_out = h->t;
+  return DOBB_OK;
+}
+
+dobb_status dobb_set_state(dobb_handle h, const void* src_dev, size_t src_bytes, int64_t t,
+                           void* stream) {
+  dobb_status st = check_handle(h);
+  if (st != DOBB_OK) return st;
+  const size_t need = dobb_checkpoint_bytes(h);
+  if (!src_dev || src_bytes < need || t < 0)
+    return fail(DOBB_ERR_INVALID_ARG, "checkpoint needs %zu bytes and t >= 0", need);
+  CUDA_TRY(cudaMemcpyAsync(h->base + h->L.off_A, src_dev, need, cudaMemcpyDeviceToDevice,
+                           static_cast<cudaStream_t>(stream)));
+  h->t = t;
+  return DOBB_OK;
+}
+
+int64_t dobb_launch_count(dobb_handle h) { return h ? h->launches : -1; }
+
+}  // extern "C"

@@ -1,0 +1,112 @@
+// Internal declarations shared by the host API and the kernels of the Dobb
+// optimizer step ("Dobb: Shard-Local Preconditioning in Block-Diagonal
+// Eigenbases", arXiv 2610.39412).  Not part of the public ABI.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+#include "dobb.h"
+
+namespace dobb {
+
+// Matrices addressed by one grouped launch; larger sets are split into
+// several launches of at most this many matrices (pointer tables travel in
+// the kernel parameter block).
+constexpr int kMaxMatPerLaunch = 512;
+
+// Largest block width k the library accepts.
+constexpr int kMaxK = 8192;
+
+// Per-matrix metadata, resident in device memory (built at dobb_create).
+struct MatInfo {
+  int64_t m, n;      // W is m x n
+  int32_t k, B;      // block width, blocks per matrix
+  int32_t blk0;      // global index of this matrix's block 0
+  int32_t pad0;
+  int64_t a_off;     // float offset of block 0 in the A (and Q) regions
+  int64_t lam_off;   // float offset of block 0 in the Lambda region
+  int64_t m_off;     // float offset of the matrix in the M region
+};
+
+// One unit of grouped work: matrix, block and two phase-specific indices.
+struct Tile {
+  int32_t mat, blk, a, b;
+};
+
+enum DType : int { kF32 = 0, kBF16 = 1 };
+
+struct AccArgs {
+  const MatInfo* info;
+  const Tile* tiles;
+  int32_t num_tiles;
+  int32_t mat_base;       // matrix index of pointer-table slot 0
+  float* A;
+  uint32_t* flags;
+  float beta2;
+  const void* X[kMaxMatPerLaunch];
+  int64_t N[kMaxMatPerLaunch];
+};
+
+struct EigArgs {
+  const MatInfo* info;
+  const Tile* tiles;
+  int32_t num_tiles;
+  int32_t max_sweeps;
+  const float* A;
+  float* Q;
+  float* lam;
+  float* scratch;         // 2 * (floats of the A region): U and V of each block
+  uint32_t* flags;
+  float* stats;
+  float tol;              // relative orthogonality threshold (0 = default)
+};
+
+struct StepArgs {
+  const MatInfo* info;
+  const Tile* tiles;
+  int32_t num_tiles;
+  int32_t mat_base;
+  const float* Q;
+  float* M;
+  uint32_t* flags;
+  float* stats;
+  float beta1;
+  float lr_s;             // lr * s
+  void* W[kMaxMatPerLaunch];
+  const void* G[kMaxMatPerLaunch];
+  int8_t* S[kMaxMatPerLaunch];
+};
+
+struct CheckArgs {
+  const MatInfo* info;
+  const Tile* tiles;
+  int32_t num_tiles;
+  const float* A;
+  const float* Q;
+  const float* lam;
+  float* out;             // 3 floats per block
+};
+
+// Launchers (return cudaGetLastError() of the launch).
+cudaError_t launch_syrk_ema(const AccArgs& a, int act_dtype, int grid, cudaStream_t s);
+cudaError_t launch_jacobi(const EigArgs& a, int grid, size_t smem_limit, cudaStream_t s);
+cudaError_t launch_step_ffma(const StepArgs& a, int param_dtype, int grid, size_t smem,
+                             cudaStream_t s);
+cudaError_t launch_check(const CheckArgs& a, int grid, cudaStream_t s);
+
+// Kernel resource queries used by the scheduler at create time.
+int step_rows_per_tile();
+int syrk_tile();
+int jacobi_smem_max_k(size_t smem_limit);
+size_t jacobi_smem_for(int k);
+size_t jacobi_sort_smem_for(int k);
+int jacobi_ctas_per_sm();
+size_t step_smem_for(int k);
+cudaError_t configure_jacobi(size_t smem_limit);
+cudaError_t configure_step(size_t smem_limit);
+cudaError_t launch_init_bases(float* Q, float* lam, const MatInfo* info, const Tile* items,
+                              int num_items, int grid, cudaStream_t s);
+
+}  // namespace dobb

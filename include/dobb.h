@@ -1,0 +1,175 @@
+/*
+ * dobb.h -- C ABI of the Dobb optimizer step on one GPU (sm_103a).
+ *
+ * Dobb ("Dobb: Shard-Local Preconditioning in Block-Diagonal Eigenbases",
+ * arXiv 2610.39412, Abstract) keeps, for every weight matrix W (m x n, y = W x,
+ * Table 6 notation), the input-activation second moment as B diagonal k x k
+ * blocks (k = n / B, Table 3 caption: n^2/B entries per matrix), a complete
+ * orthonormal eigenbasis of every block, and a momentum buffer.  One
+ * optimizer step projects the momentum into the block bases, takes the sign
+ * of the coefficients (the l_inf normalisation of Table 13), reconstructs the
+ * update and applies it:
+ *
+ *     A_b <- beta2 A_b + (1 - beta2) X_b^T X_b / N     dobb_accumulate_moments
+ *     Q_b, Lambda_b : A_b = Q_b Lambda_b Q_b^T          dobb_refresh_bases
+ *     M <- beta1 M + G ; C_b = M_b Q_b ; S_b = sign(C_b) ;
+ *     U_b = S_b Q_b^T ; W <- W - lr * s * U              dobb_step
+ *
+ * The refresh is the exact eigendecomposition of Table 15; it runs inside the
+ * step call every `refresh_period` steps (Table 21 footnote a: the moment
+ * reduction runs behind the backward pass, the refresh inside the optimizer
+ * call).
+ *
+ * Conventions shared by every call
+ *  - All pointers named *_dev or documented as device pointers are CUDA
+ *    device memory of the device that was current at dobb_create; pointer
+ *    arrays themselves (const void* const* ...) are host arrays.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Every call is asynchronous on that stream unless stated.
+ *  - Matrices are row-major.  X for matrix i is N_i x n_i (one row per token).
+ *    W and G are m_i x n_i in the parameter dtype; M is fp32 library state.
+ *  - The library never allocates device memory after dobb_create: the state
+ *    lives in a caller-provided device buffer of dobb_state_bytes() bytes,
+ *    which the caller owns and must keep alive until dobb_destroy.
+ *  - Errors: every call returns a dobb_status; on failure dobb_last_error()
+ *    (thread-local, valid until the next call on the same thread) gives a
+ *    message.  Device-side conditions (non-finite input, non-convergence)
+ *    never trap: they set per-block flag bits read by dobb_get_block_flags.
+ */
+#ifndef DOBB_H
+#define DOBB_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct dobb_ctx* dobb_handle;
+
+typedef enum {
+  DOBB_OK = 0,
+  DOBB_ERR_INVALID_ARG = 1,   /* bad shape, pointer, size or value          */
+  DOBB_ERR_CUDA = 2,          /* a CUDA runtime call failed                  */
+  DOBB_ERR_NONFINITE = 3,     /* reserved for callers mapping flag bits      */
+  DOBB_ERR_NOT_CONVERGED = 4, /* reserved for callers mapping flag bits      */
+  DOBB_ERR_STATE = 5,         /* wrong device, buffer too small, bad handle  */
+  DOBB_ERR_UNSUPPORTED = 6    /* shape outside what the kernels support      */
+} dobb_status;
+
+typedef enum { DOBB_F32 = 0, DOBB_BF16 = 1 } dobb_dtype;
+
+/* Per-block flag bits, OR-ed on the device, cleared by dobb_clear_block_flags. */
+#define DOBB_FLAG_NONFINITE_X 1u     /* accumulate saw a non-finite activation      */
+#define DOBB_FLAG_NONFINITE_G 2u     /* step saw a non-finite gradient / momentum   */
+#define DOBB_FLAG_NONFINITE_A 4u     /* refresh skipped (A non-finite); basis kept  */
+#define DOBB_FLAG_NOT_CONVERGED 8u   /* eigensolver hit its sweep cap; basis written */
+
+/* Which state tensor dobb_state_tensor() returns. */
+typedef enum {
+  DOBB_T_MOMENTS = 0,  /* A: per matrix B blocks of k x k fp32, row-major, full symmetric */
+  DOBB_T_BASES = 1,    /* Q: per matrix B blocks of k x k fp32, row-major; column j is the
+                          eigenvector of the j-th largest eigenvalue                         */
+  DOBB_T_EIGVALS = 2,  /* Lambda: per matrix B x k fp32, descending within a block         */
+  DOBB_T_MOMENTUM = 3, /* M: per matrix m x n fp32, row-major                              */
+  DOBB_T_FLAGS = 4,    /* per block uint32 flag bits (all blocks of all matrices)          */
+  DOBB_T_STATS = 5     /* per block 4 fp32: ||U_b||_F^2, ||C_b||_F^2 of the last step,
+                          Jacobi sweeps and final relative off-norm of the last refresh     */
+} dobb_tensor;
+
+/* Bytes of device state for the given matrix set (m[i] x n[i], n[i] % B == 0).
+ * Returns 0 if the arguments are invalid (see dobb_last_error). */
+size_t dobb_state_bytes(int num_matrices, const int64_t* m, const int64_t* n, int B);
+
+/* Create an optimizer over `num_matrices` matrices.
+ *   m, n            host arrays of the matrix shapes; n[i] % B == 0, k = n/B in [1, 8192]
+ *   B               blocks per matrix (same for all matrices)
+ *   beta1, beta2    momentum and second-moment EMA coefficients, in [0, 1)
+ *   refresh_period  T: dobb_step refreshes the bases when t % T == 0; 0 = never
+ *   scale_s         update scale s (Table 9), W <- W - lr * s * U
+ *   param_dtype     dtype of W and G; act_dtype dtype of X
+ *   state_mem       caller-owned device buffer of at least dobb_state_bytes()
+ *                   bytes, 256-byte aligned
+ * Initialises A = 0, Q = I, Lambda = 0, M = 0, flags = 0, t = 0 on `stream`.
+ * The handle is bound to the current CUDA device. */
+dobb_status dobb_create(dobb_handle* out, int num_matrices, const int64_t* m,
+                        const int64_t* n, int B, float beta1, float beta2,
+                        int refresh_period, float scale_s, dobb_dtype param_dtype,
+                        dobb_dtype act_dtype, void* state_mem, size_t state_bytes,
+                        void* stream);
+
+dobb_status dobb_destroy(dobb_handle h);
+
+/* Thread-local message of the last failed call on this thread ("" if none). */
+const char* dobb_last_error(void);
+
+/* Accumulate block second moments (one grouped launch over all matrices):
+ * A_b <- beta2 A_b + (1 - beta2) X_b^T X_b / N_i for every block of matrix i.
+ *   X   host array of num_matrices device pointers (X[i] may be NULL to skip i)
+ *   N   host array of token counts (N[i] == 0 skips matrix i) */
+dobb_status dobb_accumulate_moments(dobb_handle h, const void* const* X,
+                                    const int64_t* N, void* stream);
+
+/* Recompute Q_b, Lambda_b of every block from the current A_b now (one
+ * grouped launch).  Blocks whose A is non-finite keep their basis and get
+ * DOBB_FLAG_NONFINITE_A. */
+dobb_status dobb_refresh_bases(dobb_handle h, void* stream);
+
+/* One optimizer step over all matrices (one grouped launch, plus the refresh
+ * first when refresh_period > 0 and t % refresh_period == 0); then t += 1.
+ *   W   host array of device pointers, updated in place (param_dtype)
+ *   G   host array of device pointers (param_dtype) */
+dobb_status dobb_step(dobb_handle h, void* const* W, const void* const* G,
+                      float lr, void* stream);
+
+/* dobb_step that also writes S = sign(C) as int8 (m_i x n_i, row-major) to
+ * S_out[i] (device pointers; an entry may be NULL).  Test hook. */
+dobb_status dobb_step_with_signs(dobb_handle h, void* const* W, const void* const* G,
+                                 float lr, int8_t* const* S_out, void* stream);
+
+/* Host-side step counter. */
+dobb_status dobb_get_step(dobb_handle h, int64_t* t);
+dobb_status dobb_set_step(dobb_handle h, int64_t t);
+
+/* Eigensolver controls: sweep cap (default 40) and relative column
+ * orthogonality threshold (0 = default, a few fp32 ulps times sqrt(k)). */
+dobb_status dobb_set_jacobi(dobb_handle h, int max_sweeps, float tol);
+
+/* Device pointer and byte size of a state tensor of one matrix
+ * (matrix >= 0) or of the whole region over all matrices (matrix == -1). */
+dobb_status dobb_state_tensor(dobb_handle h, dobb_tensor which, int matrix,
+                              void** dev_ptr, size_t* bytes);
+
+/* Number of blocks over all matrices and the index of matrix i's first block
+ * (blocks are numbered matrix by matrix). */
+int64_t dobb_num_blocks(dobb_handle h);
+int64_t dobb_block_offset(dobb_handle h, int matrix);
+
+/* Copy the per-block flags / stats to host memory (num_blocks entries of
+ * uint32, or 4 * num_blocks floats).  Synchronises `stream`. */
+dobb_status dobb_get_block_flags(dobb_handle h, uint32_t* host_out, void* stream);
+dobb_status dobb_clear_block_flags(dobb_handle h, void* stream);
+dobb_status dobb_get_block_stats(dobb_handle h, float* host_out, void* stream);
+
+/* Invariant check of the current bases (one grouped launch, fp64 sums):
+ * per block 3 floats ||A Q - Q Lambda||_F / ||A||_F, ||Q^T Q - I||_F,
+ * ||Q Lambda Q^T - A||_F / ||A||_F written to host_out (3 * num_blocks).
+ * Synchronises `stream`. */
+dobb_status dobb_check_bases(dobb_handle h, float* host_out, void* stream);
+
+/* Checkpoint: bytes of the persistent state (A, Q, Lambda, M, flags), copy
+ * it to / from a caller device buffer, together with the step counter. */
+size_t dobb_checkpoint_bytes(dobb_handle h);
+dobb_status dobb_get_state(dobb_handle h, void* dst_dev, size_t dst_bytes,
+                           int64_t* t_out, void* stream);
+dobb_status dobb_set_state(dobb_handle h, const void* src_dev, size_t src_bytes,
+                           int64_t t, void* stream);
+
+/* Number of kernel launches issued by this handle since creation (host count). */
+int64_t dobb_launch_count(dobb_handle h);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DOBB_H */

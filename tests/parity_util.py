@@ -1,0 +1,116 @@
+"""Shared helpers of the GPU parity tests: build seeded inputs, run the CUDA
+path through the C ABI and the fp64 oracle on the same inputs, and score the
+results with the oracle's parity rules.
+
+Tolerances (the bar every GPU test applies):
+  * block moments A: relative Frobenius error <= 1e-5 per block;
+  * eigen-blocks: ||Q Lambda Q^T - A||_F / ||A||_F <= 1e-5 and
+    ||A Q - Q Lambda||_F / ||A||_F <= 1e-5 (fp64 evaluation against the
+    oracle's A), ||Q^T Q - I||_F <= 1e-5 * sqrt(k) (k columns, each
+    normalised to fp32 rounding), eigenvalues within 1e-5 ||A||_F of the
+    oracle's (Weyl's bound for a 1e-5 backward error);
+  * signs: disagreements with sign(C_ref) only where |C_ref| < 1e-5 RMS(C_b)
+    and in fewer than 1e-4 of the entries, C_ref computed in fp64 with the
+    GPU's own basis (the basis of an ill-conditioned block is determined
+    only to fp32 accuracy, so the sign check must not depend on it);
+  * parameters: fp32 W within 1e-5 max relative error; bf16 W bitwise equal
+    to the rounded fp64 result except where that result lies within
+    1e-5 max|W| of a rounding midpoint (oracle.metrics.bf16_parity), both
+    computed from the GPU's signs at the tolerated entries.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from block_eigenbasis_preconditioning_gb300 import inputs as I
+from oracle import dobb as O
+from oracle import metrics as MX
+
+TOL_A = 1e-5
+TOL_EIG = 1e-5
+TOL_SIGN_BAND = 1e-5
+TOL_SIGN_FRAC = 1e-4
+TOL_W = 1e-5
+
+TORCH = {"f32": torch.float32, "bf16": torch.bfloat16}
+
+
+def to_dev(x: np.ndarray, dtype: str) -> torch.Tensor:
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32))
+    return t.to(device="cuda", dtype=TORCH[dtype]).contiguous()
+
+
+def to_np(t: torch.Tensor) -> np.ndarray:
+    return t.detach().to(torch.float64).cpu().numpy()
+
+
+def make_problem(shapes, N, eff, seed, param_dtype="f32", act_dtype="f32"):
+    """Seeded inputs for a list of (m, n): X (N x n), G = D X / N, W."""
+    rng = np.random.default_rng(seed)
+    Xs, Gs, Ws = [], [], []
+    for (m, n) in shapes:
+        X = I.activations(N, n, eff, rng, dtype=act_dtype)
+        Xs.append(X)
+        Gs.append(I.gradients(m, X, rng, dtype=param_dtype))
+        Ws.append(I.weights(m, n, rng, dtype=param_dtype))
+    return Xs, Gs, Ws
+
+
+def check_moments(opt, orc, matrices=None):
+    worst = 0.0
+    for i in (matrices if matrices is not None else range(len(orc.shapes))):
+        Ag = to_np(opt.tensor("moments", i))
+        Ar = orc.A[i]
+        for b in range(Ar.shape[0]):
+            fro = np.linalg.norm(Ar[b])
+            err = np.linalg.norm(Ag[b] - Ar[b]) / (fro if fro > 0 else 1.0)
+            worst = max(worst, err)
+            assert np.array_equal(Ag[b], Ag[b].T), "A must stay exactly symmetric"
+    assert worst <= TOL_A, f"block moments relative error {worst:.3e}"
+    return worst
+
+
+def check_bases(opt, A_ref_list, matrices=None):
+    """Eigen residuals of the GPU bases against fp64 reference moments."""
+    worst = {"residual": 0.0, "orth": 0.0, "recon": 0.0, "lam": 0.0}
+    for i in (matrices if matrices is not None else range(len(A_ref_list))):
+        Q = to_np(opt.tensor("bases", i))
+        lam = to_np(opt.tensor("eigvals", i))
+        Ar = A_ref_list[i]
+        for b in range(Ar.shape[0]):
+            k = Ar.shape[1]
+            r = MX.eig_residuals(Ar[b], Q[b], lam[b])
+            assert r["residual"] <= TOL_EIG, f"matrix {i} block {b}: residual {r['residual']:.3e}"
+            assert r["recon"] <= TOL_EIG, f"matrix {i} block {b}: reconstruction {r['recon']:.3e}"
+            assert r["orth"] <= TOL_EIG * max(1.0, np.sqrt(k)), f"orthogonality {r['orth']:.3e}"
+            lam_ref = np.sort(np.linalg.eigvalsh(0.5 * (Ar[b] + Ar[b].T)))[::-1]
+            fro = np.linalg.norm(Ar[b])
+            dl = np.abs(lam[b] - lam_ref).max() / (fro if fro > 0 else 1.0)
+            assert dl <= TOL_EIG, f"eigenvalues off by {dl:.3e} ||A||"
+            assert np.all(np.diff(lam[b]) <= 0), "eigenvalues must be sorted descending"
+            for key in ("residual", "orth", "recon"):
+                worst[key] = max(worst[key], r[key])
+            worst["lam"] = max(worst["lam"], dl)
+    return worst
+
+
+def check_update(W_prev, M_prev, G, Q_gpu, S_gpu, W_gpu, M_gpu, beta1, lr, s, param_dtype, k):
+    """Score one matrix's update against the oracle run with the GPU basis."""
+    ref = O.update_from_bases(W_prev, M_prev, G, Q_gpu, beta1, lr, s, param_dtype)
+    # momentum
+    dm = np.abs(M_gpu - ref["M"]).max() / max(np.abs(ref["M"]).max(), 1e-30)
+    assert dm <= 1e-6, f"momentum relative error {dm:.3e}"
+    # signs
+    sa = MX.sign_agreement(ref["C"], S_gpu, k, TOL_SIGN_BAND)
+    assert sa["outside_band"] == 0, f"{sa['outside_band']} sign flips outside the band"
+    assert sa["fraction"] < TOL_SIGN_FRAC, f"sign disagreement fraction {sa['fraction']:.2e}"
+    # parameters, scored with the GPU's signs at the tolerated entries
+    ref2 = O.update_from_bases(W_prev, M_prev, G, Q_gpu, beta1, lr, s, "f32", S_override=S_gpu)
+    if param_dtype == "f32":
+        e = MX.w_rel_error(W_gpu, ref2["W"])
+        assert e <= TOL_W, f"W max relative error {e:.3e}"
+        return {"sign": sa, "w_err": e, "m_err": dm}
+    res = MX.bf16_parity(W_gpu, ref2["W"], TOL_W)
+    assert res["violations"] == 0, f"bf16 W: {res}"
+    return {"sign": sa, "bf16": res, "m_err": dm}

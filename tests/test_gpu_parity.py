@@ -1,0 +1,244 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 oracle on the
+same seeded inputs, phase by phase and over whole multi-step runs."""
+import numpy as np
+import pytest
+import torch
+
+from block_eigenbasis_preconditioning_gb300 import inputs as I
+from oracle import dobb as O
+from oracle import metrics as MX
+
+from parity_util import (TOL_A, check_bases, check_moments, check_update, make_problem,
+                         to_dev, to_np)
+
+pytestmark = pytest.mark.gpu
+
+
+def _dobb(*a, **k):
+    from block_eigenbasis_preconditioning_gb300 import Dobb
+    return Dobb(*a, **k)
+
+
+# --------------------------------------------------------------------------
+# (a1) block moments
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("act", ["f32", "bf16"])
+@pytest.mark.parametrize("shapes,B,N", [
+    ([(24, 96), (33, 64)], 2, 100),      # k = 48 / 32, ragged token tail
+    ([(8, 130)], 2, 37),                 # k = 65: crosses one 64 tile
+    ([(5, 7)], 7, 3),                    # k = 1
+    ([(40, 400)], 1, 70),                # k = 400: 7 x 7 tiles
+])
+def test_moments_match_oracle(act, shapes, B, N):
+    Xs, _, _ = make_problem(shapes, N, 0.3, seed=1, act_dtype=act)
+    opt = _dobb(shapes, B, beta2=0.9, refresh_period=0, act_dtype=act)
+    orc = O.DobbOracle(shapes, B, beta2=0.9, refresh_period=0)
+    for rep in range(3):
+        Xd = [to_dev(x, act) for x in Xs]
+        opt.accumulate(Xd)
+        orc.accumulate(Xs)
+        torch.cuda.synchronize()
+        check_moments(opt, orc)
+        Xs = [x[::-1].copy() for x in Xs]
+
+
+def test_moments_skip_null_and_flag_nonfinite():
+    shapes = [(8, 32), (8, 32)]
+    Xs, _, _ = make_problem(shapes, 16, 0.5, seed=2)
+    opt = _dobb(shapes, 2, refresh_period=0)
+    orc = O.DobbOracle(shapes, 2, refresh_period=0)
+    opt.accumulate([to_dev(Xs[0], "f32"), None])
+    orc.accumulate([Xs[0], None])
+    check_moments(opt, orc)
+    assert np.all(opt.block_flags() == 0)
+    bad = Xs[1].copy()
+    bad[3, 20] = np.nan
+    opt.accumulate([None, to_dev(bad, "f32")])
+    flags = opt.block_flags()
+    assert flags[opt.block_offset(1) + 1] & 1 and flags[opt.block_offset(1)] == 0
+    # refresh keeps the previous basis (identity) for the non-finite block
+    opt.refresh()
+    f2 = opt.block_flags()
+    assert f2[opt.block_offset(1) + 1] & 4
+    Q = to_np(opt.tensor("bases", 1))
+    assert np.array_equal(Q[1], np.eye(16))
+
+
+# --------------------------------------------------------------------------
+# (a2) eigen refresh
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("k", [1, 2, 3, 5, 16, 48, 100, 128, 168, 169, 192, 400])
+def test_refresh_on_spd_blocks_with_gaps(k):
+    rng = np.random.default_rng(k)
+    B = 2
+    shapes = [(4, B * k)]
+    opt = _dobb(shapes, B, refresh_period=0)
+    A = np.stack([I.spd_with_gap(k, rng, cond=1e6)[0] if k > 1 else np.array([[0.7]])
+                  for _ in range(B)])
+    opt.tensor("moments", 0).copy_(torch.from_numpy(A.astype(np.float32)).reshape(-1))
+    A32 = A.astype(np.float32).astype(np.float64)
+    opt.refresh()
+    torch.cuda.synchronize()
+    check_bases(opt, [A32])
+    assert np.all(opt.block_flags() == 0)
+    chk = opt.check_bases()
+    assert chk[:, 0].max() <= 1e-5 and chk[:, 2].max() <= 1e-5
+
+
+@pytest.mark.parametrize("k,eff", [(192, 0.15), (100, 0.10), (64, 0.40)])
+def test_refresh_on_accumulated_moments(k, eff):
+    """Blocks of a low-effective-rank activation moment (ill-conditioned)."""
+    B = 2
+    shapes = [(16, B * k)]
+    Xs, _, _ = make_problem(shapes, 1024, eff, seed=3)
+    opt = _dobb(shapes, B, beta2=0.0, refresh_period=0)
+    opt.accumulate([to_dev(Xs[0], "f32")])
+    opt.refresh()
+    torch.cuda.synchronize()
+    A_gpu = to_np(opt.tensor("moments", 0))
+    check_bases(opt, [A_gpu])
+    orc = O.DobbOracle(shapes, B, beta2=0.0, refresh_period=0)
+    orc.accumulate(Xs)
+    check_moments(opt, orc)
+
+
+# --------------------------------------------------------------------------
+# (a3 - a7) the update, with the GPU's own basis
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("pdt", ["f32", "bf16"])
+@pytest.mark.parametrize("shapes,B", [
+    ([(37, 96)], 2),            # k = 48, ragged rows
+    ([(1, 24), (17, 24)], 3),   # m = 1, k = 8
+    ([(130, 200)], 2),          # k = 100
+    ([(20, 400)], 1),           # k = 400
+    ([(9, 15)], 5),             # k = 3 (odd)
+])
+def test_update_matches_oracle_with_gpu_basis(pdt, shapes, B):
+    Xs, Gs, Ws = make_problem(shapes, 256, 0.2, seed=4, param_dtype=pdt)
+    opt = _dobb(shapes, B, beta1=0.9, beta2=0.95, refresh_period=1, scale_s=1.5, param_dtype=pdt)
+    Wd = [to_dev(w, pdt) for w in Ws]
+    Gd = [to_dev(g, pdt) for g in Gs]
+    Sd = [torch.zeros(w.shape, dtype=torch.int8, device="cuda") for w in Ws]
+    M_prev = [np.zeros(s) for s in shapes]
+    W_prev = [to_np(w) for w in Wd]
+    opt.accumulate([to_dev(x, "f32") for x in Xs])
+    opt.step(Wd, Gd, 0.02, signs=Sd)
+    torch.cuda.synchronize()
+    for i, (m, n) in enumerate(shapes):
+        Q = to_np(opt.tensor("bases", i))
+        check_update(W_prev[i], M_prev[i], to_np(Gd[i]), Q, to_np(Sd[i]), to_np(Wd[i]),
+                     to_np(opt.tensor("momentum", i)), 0.9, 0.02, 1.5, pdt, n // B)
+    # ||U_b||_F^2 equals the number of nonzero signs (orthonormal Q_b)
+    st = opt.block_stats()
+    for i, (m, n) in enumerate(shapes):
+        k = n // B
+        S = to_np(Sd[i])
+        for b in range(B):
+            nnz = np.count_nonzero(S[:, b * k:(b + 1) * k])
+            assert abs(st[opt.block_offset(i) + b, 0] - nnz) <= 1e-4 * max(nnz, 1)
+
+
+def test_identity_basis_gives_sign_of_momentum():
+    shapes = [(33, 40)]
+    _, Gs, Ws = make_problem(shapes, 8, 0.5, seed=5)
+    opt = _dobb(shapes, 4, beta1=0.5, refresh_period=0, scale_s=2.0)
+    Wd, Gd = [to_dev(Ws[0], "f32")], [to_dev(Gs[0], "f32")]
+    W0 = to_np(Wd[0])
+    opt.step(Wd, Gd, 0.01)
+    torch.cuda.synchronize()
+    expect = W0 - 0.01 * 2.0 * np.sign(Gs[0].astype(np.float64))
+    assert MX.w_rel_error(to_np(Wd[0]), expect) <= 1e-6
+
+
+def test_nonfinite_gradient_is_flagged():
+    shapes = [(16, 32)]
+    _, Gs, Ws = make_problem(shapes, 8, 0.5, seed=6)
+    G = Gs[0].copy()
+    G[2, 30] = np.inf
+    opt = _dobb(shapes, 2, refresh_period=0)
+    opt.step([to_dev(Ws[0], "f32")], [to_dev(G, "f32")], 0.01)
+    f = opt.block_flags()
+    assert f[1] & 2 and not f[0] & 2
+
+
+# --------------------------------------------------------------------------
+# whole runs: single fp32 768 x 768 matrix, B = 4 (k = 192), 10 steps,
+# refresh every 5, beta1 0.95, beta2 0.99, lr 0.02, s 1, seed 0
+# --------------------------------------------------------------------------
+
+def _run(shapes, B, N, eff, steps, T, pdt, adt, seed, beta1=0.95, beta2=0.99, lr=0.02, s=1.0):
+    rng = np.random.default_rng(seed)
+    opt = _dobb(shapes, B, beta1=beta1, beta2=beta2, refresh_period=T, scale_s=s,
+                param_dtype=pdt, act_dtype=adt)
+    orc = O.DobbOracle(shapes, B, beta1=beta1, beta2=beta2, refresh_period=0, scale_s=s,
+                       param_dtype=pdt)
+    Ws = [I.weights(m, n, rng, dtype=pdt) for (m, n) in shapes]
+    Wd = [to_dev(w, pdt) for w in Ws]
+    for t in range(steps):
+        Xs = [I.activations(N, n, eff, rng, dtype=adt) for (m, n) in shapes]
+        Gs = [I.gradients(m, X, rng, dtype=pdt) for (m, n), X in zip(shapes, Xs)]
+        Gd = [to_dev(g, pdt) for g in Gs]
+        Sd = [torch.zeros(w.shape, dtype=torch.int8, device="cuda") for w in Wd]
+        W_prev = [to_np(w) for w in Wd]
+        M_prev = [m.copy() for m in orc.M]
+        opt.accumulate([to_dev(x, adt) for x in Xs])
+        orc.accumulate(Xs)
+        opt.step(Wd, Gd, lr, signs=Sd)
+        torch.cuda.synchronize()
+        check_moments(opt, orc)
+        if T > 0 and t % T == 0:
+            check_bases(opt, [a.astype(np.float64) for a in orc.A])
+        for i, (m, n) in enumerate(shapes):
+            Q = to_np(opt.tensor("bases", i))
+            check_update(W_prev[i], M_prev[i], to_np(Gd[i]), Q, to_np(Sd[i]), to_np(Wd[i]),
+                         to_np(opt.tensor("momentum", i)), beta1, lr, s, pdt, n // B)
+            orc.M[i] = O.momentum(M_prev[i], to_np(Gd[i]), beta1)
+    return opt
+
+
+def test_single_matrix_ten_steps():
+    _run([(768, 768)], 4, 1024, 0.15, steps=10, T=5, pdt="f32", adt="f32", seed=0)
+
+
+def test_small_model_bf16_mixed_shapes():
+    shapes = [(96, 64), (256, 64), (64, 256)]
+    _run(shapes, 4, 512, 0.2, steps=4, T=2, pdt="bf16", adt="bf16", seed=7)
+
+
+# --------------------------------------------------------------------------
+# checkpoint / resume is bitwise
+# --------------------------------------------------------------------------
+
+def test_checkpoint_resume_bitwise():
+    shapes = [(64, 96), (32, 48)]
+    rng = np.random.default_rng(8)
+    seq = []
+    for t in range(8):
+        Xs = [I.activations(64, n, 0.3, rng) for (m, n) in shapes]
+        Gs = [I.gradients(m, X, rng) for (m, n), X in zip(shapes, Xs)]
+        seq.append((Xs, Gs))
+    W0 = [I.weights(m, n, rng) for (m, n) in shapes]
+
+    def run(opt, W, ts):
+        for t in ts:
+            Xs, Gs = seq[t]
+            opt.accumulate([to_dev(x, "f32") for x in Xs])
+            opt.step(W, [to_dev(g, "f32") for g in Gs], 0.02)
+
+    a = _dobb(shapes, 2, refresh_period=3)
+    Wa = [to_dev(w, "f32") for w in W0]
+    run(a, Wa, range(5))
+    buf, t = a.get_state()
+    W_mid = [w.clone() for w in Wa]
+    run(a, Wa, range(5, 8))
+    b = _dobb(shapes, 2, refresh_period=3)
+    b.set_state(buf, t)
+    run(b, W_mid, range(5, 8))
+    torch.cuda.synchronize()
+    for x, y in zip(Wa, W_mid):
+        assert torch.equal(x, y)
+    assert torch.equal(a.tensor("momentum"), b.tensor("momentum"))
+    assert torch.equal(a.tensor("bases"), b.tensor("bases"))
