@@ -269,9 +269,13 @@ def run_gpu(args):
         dist.init_process_group("nccl")
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
-    ms = I.gpt2_xl_shapes()
+    ms = I.gpt2_xl_shapes(include_embedding=args.layers is None)
     shapes, layers = ms.shapes, ms.layer
-    params = ms.num_params
+    if args.layers is not None:
+        keep = [i for i, li in enumerate(layers) if li < args.layers]
+        shapes = [shapes[i] for i in keep]
+        layers = [layers[i] for i in keep]
+    params = sum(m * n for m, n in shapes)
     Xsets, Gs, Ws = make_inputs(torch, shapes, layers, device, seed=1234 + rank)
     opt = Dobb(shapes, B_BLOCKS, BETA1, BETA2, refresh_period=REFRESH, scale_s=SCALE,
                param_dtype="bf16", act_dtype="bf16", device=device)
@@ -386,8 +390,11 @@ def run_gpu(args):
                 "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": ms_step,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
                 "data": "synthetic",
-                "config": {"workload": "gpt2-xl B=16: 289 matrices, 1.555e9 params, bf16 W/G, "
-                                       "fp32 M, X 8192 bf16 tokens/matrix, refresh every 10",
+                "config": {"workload": ("gpt2-xl B=16: 289 matrices, 1.555e9 params, bf16 W/G, "
+                                        "fp32 M, X 8192 bf16 tokens/matrix, refresh every 10")
+                           if args.layers is None else
+                           f"gpt2-xl shapes, first {args.layers} layers ({len(shapes)} matrices, "
+                           f"{params} params), B=16",
                            "B": B_BLOCKS, "refresh_period": REFRESH, "tokens": N_TOKENS,
                            "refresh_steps_timed": sum(is_refresh),
                            "l2": "inputs larger than L2 (22 GB streamed per step)",
@@ -443,6 +450,9 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="smaller model of the same layer shapes (first L layers, no "
+                         "embedding), for profiler captures")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -20,7 +20,8 @@ STATUS_NAMES = {0: "DOBB_OK", 1: "DOBB_ERR_INVALID_ARG", 2: "DOBB_ERR_CUDA",
                 3: "DOBB_ERR_NONFINITE", 4: "DOBB_ERR_NOT_CONVERGED", 5: "DOBB_ERR_STATE",
                 6: "DOBB_ERR_UNSUPPORTED"}
 DTYPES = {"f32": 0, "bf16": 1}
-TENSORS = {"moments": 0, "bases": 1, "eigvals": 2, "momentum": 3, "flags": 4, "stats": 5}
+TENSORS = {"moments": 0, "bases": 1, "eigvals": 2, "momentum": 3, "flags": 4, "stats": 5,
+           "error": 6}
 FLAG_NONFINITE_X = 1
 FLAG_NONFINITE_G = 2
 FLAG_NONFINITE_A = 4
@@ -57,6 +58,8 @@ SIGNATURES = [
     ("dobb_get_state", _c.c_int, [_VP, _VP, _c.c_size_t, _I64P, _VP]),
     ("dobb_set_state", _c.c_int, [_VP, _VP, _c.c_size_t, _c.c_int64, _VP]),
     ("dobb_launch_count", _c.c_int64, [_VP]),
+    ("dobb_set_step_path", _c.c_int, [_VP, _c.c_int]),
+    ("dobb_sync_bases", _c.c_int, [_VP, _VP]),
 ]
 
 

@@ -15,6 +15,9 @@
 #include <string>
 #include <vector>
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "dobb_internal.cuh"
 
 using namespace dobb;
@@ -43,25 +46,39 @@ constexpr size_t kAlign = 256;
 size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
 struct Layout {
-  size_t a_floats = 0, lam_floats = 0, m_floats = 0;
+  size_t a_floats = 0, lam_floats = 0, m_floats = 0, pack_bytes = 0;
   int64_t nblocks = 0;
   size_t off_A = 0, off_Q = 0, off_lam = 0, off_M = 0, off_flags = 0, off_stats = 0,
-         off_check = 0, off_info = 0, off_tiles = 0, off_scratch = 0, total = 0;
+         off_check = 0, off_err = 0, off_info = 0, off_maps = 0, off_tiles = 0, off_pack = 0,
+         off_scratch = 0, total = 0;
   size_t n_tiles = 0;
 };
 
+constexpr int kTcRows = 128;
+
+int64_t pad16f(int64_t v) { return (v + 15) / 16 * 16; }
+
 struct Chunk {
   int mat_base = 0, mat_end = 0;
-  int step_off = 0, step_n = 0;
+  int step_off = 0, step_n = 0;     // FFMA tiles of every matrix
+  int tc_off = 0, tc_n = 0;         // tensor-core tiles (eligible matrices)
+  int rest_off = 0, rest_n = 0;     // FFMA tiles of the other matrices
+  int max_k_tc = 0, max_k_rest = 1;
   int syrk_off = 0, syrk_n = 0;
   int eig_off = 0, eig_n = 0;
   int max_k = 1;
+};
+
+struct SyrkChunk {
+  int mat_base = 0, mat_end = 0, off = 0, n = 0, max_k = 8;
 };
 
 // Work lists of all phases, in the order they are stored on the device.
 struct WorkLists {
   std::vector<Tile> tiles;
   std::vector<Chunk> chunks;
+  std::vector<SyrkChunk> syrk_tc;
+  int syrk_rest_off = 0, syrk_rest_n = 0;
   int blocks_off = 0, blocks_n = 0;  // every (matrix, block) once, by matrix
 };
 
@@ -116,6 +133,29 @@ WorkLists build_work(int num, const int64_t* m, const int64_t* n, int B) {
     ch.step_off = (int)wl.tiles.size();
     ch.step_n = (int)v.size();
     for (auto& e : v) wl.tiles.push_back(e.second);
+    // tensor-core tiles of 128 rows, and FFMA tiles of the ineligible rest
+    v.clear();
+    std::vector<std::pair<int64_t, Tile>> rest;
+    for (int i = ch.mat_base; i < ch.mat_end; ++i) {
+      const int k = (int)(n[i] / B);
+      if (tc_eligible(m[i], n[i], k)) {
+        ch.max_k_tc = std::max(ch.max_k_tc, k);
+        for (int b = 0; b < B; ++b)
+          for (int64_t r = 0; r < m[i]; r += kTcRows) v.push_back({(int64_t)k, Tile{i, b, (int)r, 0}});
+      } else {
+        ch.max_k_rest = std::max(ch.max_k_rest, k);
+        for (int b = 0; b < B; ++b)
+          for (int64_t r = 0; r < m[i]; r += TM) rest.push_back({(int64_t)k, Tile{i, b, (int)r, 0}});
+      }
+    }
+    std::stable_sort(v.begin(), v.end(), [](auto& x, auto& y) { return x.first > y.first; });
+    std::stable_sort(rest.begin(), rest.end(), [](auto& x, auto& y) { return x.first > y.first; });
+    ch.tc_off = (int)wl.tiles.size();
+    ch.tc_n = (int)v.size();
+    for (auto& e : v) wl.tiles.push_back(e.second);
+    ch.rest_off = (int)wl.tiles.size();
+    ch.rest_n = (int)rest.size();
+    for (auto& e : rest) wl.tiles.push_back(e.second);
     // syrk tiles: upper triangle of ceil(k / ST)^2 output tiles per block
     v.clear();
     for (int i = ch.mat_base; i < ch.mat_end; ++i) {
@@ -141,6 +181,50 @@ WorkLists build_work(int num, const int64_t* m, const int64_t* n, int B) {
     for (auto& e : v) wl.tiles.push_back(e.second);
     wl.chunks.push_back(ch);
   }
+  // tensor-core accumulate: chunks of eligible matrices, tiles of 128 rows
+  // (the slice count depends on each block's misalignment to 8 columns)
+  {
+    std::vector<int> elig;
+    for (int i = 0; i < num; ++i)
+      if (syrk_tc_eligible(n[i], (int)(n[i] / B))) elig.push_back(i);
+    for (size_t c0 = 0; c0 < elig.size();) {
+      SyrkChunk sc;
+      sc.mat_base = elig[c0];
+      std::vector<std::pair<int64_t, Tile>> v;
+      size_t c1 = c0;
+      while (c1 < elig.size() && elig[c1] - sc.mat_base < kMaxSyrkTcMat) {
+        const int i = elig[c1];
+        const int k = (int)(n[i] / B);
+        sc.max_k = std::max(sc.max_k, k);
+        for (int b = 0; b < B; ++b) {
+          const int d = (int)(((int64_t)b * k) & 7);
+          for (int t = 0; 128 * t < k + d; ++t) v.push_back({(int64_t)k, Tile{i, b, t, 0}});
+        }
+        ++c1;
+      }
+      sc.mat_end = elig[c1 - 1] + 1;
+      std::stable_sort(v.begin(), v.end(), [](auto& x, auto& y) { return x.first > y.first; });
+      sc.off = (int)wl.tiles.size();
+      sc.n = (int)v.size();
+      for (auto& e : v) wl.tiles.push_back(e.second);
+      wl.syrk_tc.push_back(sc);
+      c0 = c1;
+    }
+    // FFMA accumulate tiles of the matrices the tensor-core kernel skips
+    std::vector<std::pair<int64_t, Tile>> v;
+    for (int i = 0; i < num; ++i) {
+      const int k = (int)(n[i] / B);
+      if (syrk_tc_eligible(n[i], k)) continue;
+      const int nt = (k + ST - 1) / ST;
+      for (int b = 0; b < B; ++b)
+        for (int ti = 0; ti < nt; ++ti)
+          for (int tj = ti; tj < nt; ++tj) v.push_back({(int64_t)k, Tile{i, b, ti, tj}});
+    }
+    std::stable_sort(v.begin(), v.end(), [](auto& x, auto& y) { return x.first > y.first; });
+    wl.syrk_rest_off = (int)wl.tiles.size();
+    wl.syrk_rest_n = (int)v.size();
+    for (auto& e : v) wl.tiles.push_back(e.second);
+  }
   wl.blocks_off = (int)wl.tiles.size();
   for (int i = 0; i < num; ++i)
     for (int b = 0; b < B; ++b) wl.tiles.push_back(Tile{i, b, 0, 0});
@@ -154,8 +238,9 @@ Layout compute_layout(int num, const int64_t* m, const int64_t* n, int B, size_t
     const int64_t k = n[i] / B;
     L.a_floats += (size_t)B * k * k;
     L.lam_floats += (size_t)B * k;
-    L.m_floats += (size_t)m[i] * n[i];
+    L.m_floats += (size_t)pad16f(m[i] * n[i]);
     L.nblocks += B;
+    if (tc_eligible(m[i], n[i], (int)k)) L.pack_bytes += (size_t)B * tc_block_image_bytes((int)k);
   }
   size_t off = 0;
   L.off_A = off;      off = align_up(off + 4 * L.a_floats);
@@ -165,8 +250,11 @@ Layout compute_layout(int num, const int64_t* m, const int64_t* n, int B, size_t
   L.off_flags = off;  off = align_up(off + 4 * (size_t)L.nblocks);
   L.off_stats = off;  off = align_up(off + 16 * (size_t)L.nblocks);
   L.off_check = off;  off = align_up(off + 12 * (size_t)L.nblocks);
+  L.off_err = off;    off = align_up(off + 4);
   L.off_info = off;   off = align_up(off + sizeof(MatInfo) * (size_t)num);
+  L.off_maps = off;   off = align_up(off + sizeof(CUtensorMap) * (size_t)num);
   L.off_tiles = off;  off = align_up(off + sizeof(Tile) * n_tiles);
+  L.off_pack = off;   off = align_up(off + L.pack_bytes);
   L.off_scratch = off; off = align_up(off + 8 * L.a_floats);
   L.total = off;
   L.n_tiles = n_tiles;
@@ -193,7 +281,15 @@ struct dobb_ctx {
   size_t smem_limit = 0;
   size_t smem_per_sm = 0;
   int64_t launches = 0;
+  int path = 0;            // 0: tensor-core kernel where eligible, 1: FFMA only
+  // cached X tensor maps (pointer and token count they were encoded for)
+  std::vector<CUtensorMap> xmaps;
+  std::vector<const void*> xmap_ptr;
+  std::vector<int64_t> xmap_N;
+  PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  bool any_tc = false;
   std::vector<float> check_host;
+  std::vector<CUtensorMap> maps;
 
   float* A() const { return reinterpret_cast<float*>(base + L.off_A); }
   float* Q() const { return reinterpret_cast<float*>(base + L.off_Q); }
@@ -205,6 +301,9 @@ struct dobb_ctx {
   MatInfo* dinfo() const { return reinterpret_cast<MatInfo*>(base + L.off_info); }
   Tile* dtiles() const { return reinterpret_cast<Tile*>(base + L.off_tiles); }
   float* scratch() const { return reinterpret_cast<float*>(base + L.off_scratch); }
+  uint32_t* err() const { return reinterpret_cast<uint32_t*>(base + L.off_err); }
+  void* dmaps() const { return base + L.off_maps; }
+  unsigned char* pack() const { return reinterpret_cast<unsigned char*>(base + L.off_pack); }
 };
 
 namespace {
@@ -215,6 +314,16 @@ dobb_status check_handle(dobb_handle h) {
   CUDA_TRY(cudaGetDevice(&dev));
   if (dev != h->device)
     return fail(DOBB_ERR_STATE, "current device %d differs from the handle's device %d", dev, h->device);
+  return DOBB_OK;
+}
+
+dobb_status do_pack(dobb_handle h, cudaStream_t s) {
+  if (!h->any_tc) return DOBB_OK;
+  const int g = std::max(1, std::min(h->wl.blocks_n, h->sm_count * 8));
+  cudaError_t e = launch_pack_bases(h->Q(), h->pack(), h->dinfo(), h->dtiles() + h->wl.blocks_off,
+                                    h->wl.blocks_n, g, s);
+  if (e != cudaSuccess) return fail(DOBB_ERR_CUDA, "pack launch: %s", cudaGetErrorString(e));
+  ++h->launches;
   return DOBB_OK;
 }
 
@@ -247,7 +356,7 @@ dobb_status do_refresh(dobb_handle h, cudaStream_t s) {
     if (e != cudaSuccess) return fail(DOBB_ERR_CUDA, "eigen launch: %s", cudaGetErrorString(e));
     ++h->launches;
   }
-  return DOBB_OK;
+  return do_pack(h, s);
 }
 
 dobb_status do_step(dobb_handle h, void* const* W, const void* const* G, float lr,
@@ -262,6 +371,10 @@ dobb_status do_step(dobb_handle h, void* const* W, const void* const* G, float l
   }
   // zero the per-step sums (slots 0 and 1 of each block's 4 stats)
   CUDA_TRY(cudaMemset2DAsync(h->stats(), 16, 0, 8, (size_t)h->L.nblocks, s));
+  bool aligned = true;
+  for (int i = 0; i < h->num; ++i)
+    if ((reinterpret_cast<uintptr_t>(W[i]) | reinterpret_cast<uintptr_t>(G[i])) % 16 != 0) aligned = false;
+  const bool use_tc = h->path == 0 && aligned;
   for (const Chunk& ch : h->wl.chunks) {
     if (ch.step_n == 0) continue;
     StepArgs a{};
@@ -280,11 +393,32 @@ dobb_status do_step(dobb_handle h, void* const* W, const void* const* G, float l
       a.G[i - ch.mat_base] = G[i];
       a.S[i - ch.mat_base] = S_out ? S_out[i] : nullptr;
     }
-    const size_t smem = step_smem_for(ch.max_k);
+    if (use_tc && ch.tc_n > 0) {
+      StepArgs at = a;
+      at.tiles = h->dtiles() + ch.tc_off;
+      at.num_tiles = ch.tc_n;
+      TcArgs t{};
+      t.maps = h->dmaps();
+      t.qpack = h->pack();
+      t.err = h->err();
+      t.bstage = (int32_t)step_tc_bstage(ch.max_k_tc);
+      const size_t smem = step_tc_smem(ch.max_k_tc);
+      const int g = std::max(1, std::min(ch.tc_n, h->sm_count));
+      cudaError_t e = launch_step_tc(at, t, h->pdt, g, smem, s);
+      if (e != cudaSuccess) return fail(DOBB_ERR_CUDA, "tensor-core step launch: %s", cudaGetErrorString(e));
+      ++h->launches;
+    }
+    const bool rest_only = use_tc && ch.tc_n > 0;
+    const int n_ffma = rest_only ? ch.rest_n : ch.step_n;
+    if (n_ffma == 0) continue;
+    a.tiles = h->dtiles() + (rest_only ? ch.rest_off : ch.step_off);
+    a.num_tiles = n_ffma;
+    const int kmax = rest_only ? ch.max_k_rest : ch.max_k;
+    const size_t smem = step_smem_for(kmax);
     if (smem > h->smem_limit)
-      return fail(DOBB_ERR_UNSUPPORTED, "block width %d needs %zu bytes of shared memory", ch.max_k, smem);
+      return fail(DOBB_ERR_UNSUPPORTED, "block width %d needs %zu bytes of shared memory", kmax, smem);
     const int by_smem = std::max(1, (int)(h->smem_per_sm / (smem + 1024)));
-    const int g = std::max(1, std::min(ch.step_n, h->sm_count * std::min(4, by_smem)));
+    const int g = std::max(1, std::min(n_ffma, h->sm_count * std::min(4, by_smem)));
     cudaError_t e = launch_step_ffma(a, h->pdt, g, smem, s);
     if (e != cudaSuccess) return fail(DOBB_ERR_CUDA, "step launch: %s", cudaGetErrorString(e));
     ++h->launches;
@@ -358,13 +492,15 @@ dobb_status dobb_create(dobb_handle* out, int num_matrices, const int64_t* m, co
   }
   h->smem_limit = (size_t)optin - 2048;  // room for static shared memory
   if ((e = configure_jacobi(h->smem_limit)) != cudaSuccess ||
-      (e = configure_step(h->smem_limit)) != cudaSuccess) {
+      (e = configure_step(h->smem_limit)) != cudaSuccess ||
+      (e = configure_step_tc(h->smem_limit)) != cudaSuccess ||
+      (e = configure_syrk_tc(h->smem_limit)) != cudaSuccess) {
     delete h;
     return fail(DOBB_ERR_CUDA, "kernel configuration: %s", cudaGetErrorString(e));
   }
 
   // per-matrix metadata
-  int64_t aoff = 0, loff = 0, moff = 0;
+  int64_t aoff = 0, loff = 0, moff = 0, poff = 0;
   int32_t blk = 0;
   for (int i = 0; i < num_matrices; ++i) {
     MatInfo mi{};
@@ -376,11 +512,48 @@ dobb_status dobb_create(dobb_handle* out, int num_matrices, const int64_t* m, co
     mi.a_off = aoff;
     mi.lam_off = loff;
     mi.m_off = moff;
+    mi.tc = tc_eligible(m[i], n[i], mi.k) ? 1 : 0;
+    mi.qblk_bytes = mi.tc ? tc_block_image_bytes(mi.k) : 0;
+    mi.qp_off = poff;
     h->info.push_back(mi);
     aoff += (int64_t)B * mi.k * mi.k;
     loff += (int64_t)B * mi.k;
-    moff += m[i] * n[i];
+    moff += pad16f(m[i] * n[i]);
+    poff += (int64_t)B * mi.qblk_bytes;
     blk += B;
+    h->any_tc = h->any_tc || mi.tc;
+  }
+  // one TMA descriptor per matrix for its momentum (fp32, box 32 x 128, 128B swizzle)
+  h->maps.assign(num_matrices, CUtensorMap{});
+  h->xmaps.assign(num_matrices, CUtensorMap{});
+  h->xmap_ptr.assign(num_matrices, nullptr);
+  h->xmap_N.assign(num_matrices, -1);
+  if (h->any_tc || (act_dtype == DOBB_BF16 && !h->wl.syrk_tc.empty())) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess || fn == nullptr || q != cudaDriverEntryPointSuccess) {
+      delete h;
+      return fail(DOBB_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+    }
+    auto encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    h->encode = encode;
+    for (int i = 0; i < num_matrices; ++i) {
+      const MatInfo& mi = h->info[i];
+      if (!mi.tc) continue;
+      cuuint64_t dims[2] = {(cuuint64_t)mi.n, (cuuint64_t)mi.m};
+      cuuint64_t strides[1] = {(cuuint64_t)mi.n * 4};
+      cuuint32_t box[2] = {32, 128};
+      cuuint32_t estr[2] = {1, 1};
+      CUresult r = encode(&h->maps[i], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, h->M() + mi.m_off, dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+      if (r != CUDA_SUCCESS) {
+        delete h;
+        return fail(DOBB_ERR_CUDA, "tensor map encode failed for matrix %d (code %d)", i, (int)r);
+      }
+    }
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const Layout& L = h->L;
@@ -391,6 +564,9 @@ dobb_status dobb_create(dobb_handle* out, int num_matrices, const int64_t* m, co
                         cudaMemcpyHostToDevice, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(h->base + L.off_A, 0, 4 * L.a_floats, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(h->base + L.off_M, 0, 4 * L.m_floats, s);
+  if (e == cudaSuccess && h->any_tc)
+    e = cudaMemcpyAsync(h->dmaps(), h->maps.data(), sizeof(CUtensorMap) * h->maps.size(),
+                        cudaMemcpyHostToDevice, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(h->base + L.off_flags, 0, L.off_info - L.off_flags, s);
   if (e == cudaSuccess) {
     const int g = std::max(1, std::min(h->wl.blocks_n, h->sm_count * 4));
@@ -398,6 +574,7 @@ dobb_status dobb_create(dobb_handle* out, int num_matrices, const int64_t* m, co
                           h->wl.blocks_n, g, s);
     ++h->launches;
   }
+  if (e == cudaSuccess && do_pack(h, s) != DOBB_OK) e = cudaErrorUnknown;
   // the host arrays above must outlive the asynchronous copies: they belong
   // to the handle; make the copies complete before returning anyway so the
   // caller may reuse its shape arrays and the first call sees a ready state.
@@ -424,6 +601,80 @@ dobb_status dobb_accumulate_moments(dobb_handle h, const void* const* X, const i
   for (int i = 0; i < h->num; ++i)
     if (N[i] < 0) return fail(DOBB_ERR_INVALID_ARG, "N[%d] < 0", i);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  bool x_aligned = true;
+  for (int i = 0; i < h->num; ++i)
+    if (X[i] && reinterpret_cast<uintptr_t>(X[i]) % 16 != 0) x_aligned = false;
+  const bool use_tc = h->path == 0 && h->adt == DOBB_BF16 && h->encode && x_aligned &&
+                      !h->wl.syrk_tc.empty() &&
+                      (h->wl.syrk_rest_n == 0 || h->num <= kMaxMatPerLaunch);
+  if (use_tc) {
+    SyrkTcArgs* a = new SyrkTcArgs();
+    for (const SyrkChunk& sc : h->wl.syrk_tc) {
+      std::memset(a, 0, sizeof(SyrkTcArgs));
+      a->info = h->dinfo();
+      a->tiles = h->dtiles() + sc.off;
+      a->num_tiles = sc.n;
+      a->mat_base = sc.mat_base;
+      a->A = h->A();
+      a->flags = h->flags();
+      a->err = h->err();
+      a->beta2 = h->beta2;
+      for (int i = sc.mat_base; i < sc.mat_end; ++i) {
+        const int slot = i - sc.mat_base;
+        a->X[slot] = X[i];
+        a->N[slot] = X[i] ? N[i] : 0;
+        if (!X[i] || N[i] <= 0 || !syrk_tc_eligible(h->n[i], (int)(h->n[i] / h->B))) continue;
+        if (h->xmap_ptr[i] != X[i] || h->xmap_N[i] != N[i]) {
+          cuuint64_t dims[2] = {(cuuint64_t)h->n[i], (cuuint64_t)N[i]};
+          cuuint64_t strides[1] = {(cuuint64_t)h->n[i] * 2};
+          cuuint32_t box[2] = {64, 64};
+          cuuint32_t estr[2] = {1, 1};
+          CUresult r = h->encode(&h->xmaps[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                                 const_cast<void*>(X[i]), dims, strides, box, estr,
+                                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+          if (r != CUDA_SUCCESS) {
+            delete a;
+            return fail(DOBB_ERR_CUDA, "X tensor map encode failed for matrix %d (code %d)", i, (int)r);
+          }
+          h->xmap_ptr[i] = X[i];
+          h->xmap_N[i] = N[i];
+        }
+        a->maps[slot] = h->xmaps[i];
+      }
+      a->stages = syrk_tc_stages(sc.max_k, h->smem_limit - 1024);
+      a->stage_bytes = (int32_t)syrk_tc_stage_bytes(sc.max_k);
+      const size_t smem = syrk_tc_smem(sc.max_k, a->stages);
+      const int g = std::max(1, std::min(sc.n, h->sm_count));
+      cudaError_t e = launch_syrk_tc(*a, g, smem, s);
+      if (e != cudaSuccess) {
+        delete a;
+        return fail(DOBB_ERR_CUDA, "tensor-core accumulate launch: %s", cudaGetErrorString(e));
+      }
+      ++h->launches;
+    }
+    delete a;
+    if (h->wl.syrk_rest_n == 0) return DOBB_OK;
+    // the matrices the tensor-core kernel does not cover (one FFMA launch;
+    // use_tc guarantees that all of them fit one pointer table)
+    AccArgs r{};
+    r.info = h->dinfo();
+    r.tiles = h->dtiles() + h->wl.syrk_rest_off;
+    r.num_tiles = h->wl.syrk_rest_n;
+    r.mat_base = 0;
+    r.A = h->A();
+    r.flags = h->flags();
+    r.beta2 = h->beta2;
+    for (int i = 0; i < h->num; ++i) {
+      r.X[i] = X[i];
+      r.N[i] = X[i] ? N[i] : 0;
+    }
+    const int g = std::max(1, std::min(r.num_tiles, h->sm_count * 4));
+    cudaError_t e = launch_syrk_ema(r, h->adt, g, s);
+    if (e != cudaSuccess) return fail(DOBB_ERR_CUDA, "accumulate launch: %s", cudaGetErrorString(e));
+    ++h->launches;
+    return DOBB_OK;
+  }
   for (const Chunk& ch : h->wl.chunks) {
     if (ch.syrk_n == 0) continue;
     AccArgs a{};
@@ -519,6 +770,10 @@ dobb_status dobb_state_tensor(dobb_handle h, dobb_tensor which, int matrix, void
       *dev_ptr = mi ? h->stats() + 4 * (size_t)mi->blk0 : h->stats();
       *bytes = 16 * (mi ? (size_t)mi->B : (size_t)h->L.nblocks);
       return DOBB_OK;
+    case DOBB_T_ERROR:
+      *dev_ptr = h->err();
+      *bytes = 4;
+      return DOBB_OK;
   }
   return fail(DOBB_ERR_INVALID_ARG, "unknown tensor %d", (int)which);
 }
@@ -604,9 +859,21 @@ dobb_status dobb_set_state(dobb_handle h, const void* src_dev, size_t src_bytes,
   CUDA_TRY(cudaMemcpyAsync(h->base + h->L.off_A, src_dev, need, cudaMemcpyDeviceToDevice,
                            static_cast<cudaStream_t>(stream)));
   h->t = t;
-  return DOBB_OK;
+  return do_pack(h, static_cast<cudaStream_t>(stream));
 }
 
 int64_t dobb_launch_count(dobb_handle h) { return h ? h->launches : -1; }
+
+dobb_status dobb_set_step_path(dobb_handle h, int path) {
+  if (!h || path < 0 || path > 1) return fail(DOBB_ERR_INVALID_ARG, "path must be 0 or 1");
+  h->path = path;
+  return DOBB_OK;
+}
+
+dobb_status dobb_sync_bases(dobb_handle h, void* stream) {
+  dobb_status st = check_handle(h);
+  if (st != DOBB_OK) return st;
+  return do_pack(h, static_cast<cudaStream_t>(stream));
+}
 
 }  // extern "C"

@@ -4,6 +4,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 
@@ -18,6 +19,8 @@ constexpr int kMaxMatPerLaunch = 512;
 
 // Largest block width k the library accepts.
 constexpr int kMaxK = 8192;
+// Largest block width of the tensor-core update kernel (TMEM holds C).
+constexpr int kMaxTcK = 448;
 
 // Per-matrix metadata, resident in device memory (built at dobb_create).
 struct MatInfo {
@@ -27,7 +30,19 @@ struct MatInfo {
   int32_t pad0;
   int64_t a_off;     // float offset of block 0 in the A (and Q) regions
   int64_t lam_off;   // float offset of block 0 in the Lambda region
-  int64_t m_off;     // float offset of the matrix in the M region
+  int64_t m_off;     // float offset of the matrix in the M region (16-float aligned)
+  int64_t qp_off;    // byte offset of block 0's packed operand images
+  int64_t qblk_bytes;  // bytes of one block's packed images
+  int32_t tc;        // 1 if the tensor-core update kernel handles this matrix
+  int32_t pad1;
+};
+
+// Extra arguments of the tensor-core update kernel.
+struct TcArgs {
+  const void* maps;        // one CUtensorMap (128 B) per matrix, for M
+  const unsigned char* qpack;
+  uint32_t* err;           // device error word (timeouts)
+  int32_t bstage;          // bytes of one B stage
 };
 
 // One unit of grouped work: matrix, block and two phase-specific indices.
@@ -47,6 +62,26 @@ struct AccArgs {
   float beta2;
   const void* X[kMaxMatPerLaunch];
   int64_t N[kMaxMatPerLaunch];
+};
+
+// Matrices per tensor-core accumulate launch (their X tensor maps travel in
+// the kernel parameter block).
+constexpr int kMaxSyrkTcMat = 200;
+
+struct SyrkTcArgs {
+  const MatInfo* info;
+  const Tile* tiles;      // (matrix, block, 128-row slice, 0)
+  int32_t num_tiles;
+  int32_t mat_base;       // slot i of X / N / maps is matrix mat_base + i
+  float* A;
+  uint32_t* flags;
+  uint32_t* err;
+  float beta2;
+  int32_t stages;
+  int32_t stage_bytes;
+  const void* X[kMaxSyrkTcMat];
+  int64_t N[kMaxSyrkTcMat];
+  CUtensorMap maps[kMaxSyrkTcMat];
 };
 
 struct EigArgs {
@@ -106,6 +141,21 @@ int jacobi_ctas_per_sm();
 size_t step_smem_for(int k);
 cudaError_t configure_jacobi(size_t smem_limit);
 cudaError_t configure_step(size_t smem_limit);
+size_t step_tc_smem(int max_k);
+size_t step_tc_bstage(int max_k);
+int64_t tc_block_image_bytes(int k);
+bool tc_eligible(int64_t m, int64_t n, int k);
+cudaError_t configure_step_tc(size_t smem_limit);
+cudaError_t launch_step_tc(const StepArgs& a, const TcArgs& t, int param_dtype, int grid,
+                           size_t smem, cudaStream_t s);
+cudaError_t launch_pack_bases(const float* Q, unsigned char* qpack, const MatInfo* info,
+                              const Tile* items, int num_items, int grid, cudaStream_t s);
+size_t syrk_tc_stage_bytes(int max_k);
+int syrk_tc_stages(int max_k, size_t smem_limit);
+size_t syrk_tc_smem(int max_k, int stages);
+bool syrk_tc_eligible(int64_t n, int k);
+cudaError_t configure_syrk_tc(size_t smem_limit);
+cudaError_t launch_syrk_tc(const SyrkTcArgs& a, int grid, size_t smem, cudaStream_t s);
 cudaError_t launch_init_bases(float* Q, float* lam, const MatInfo* info, const Tile* items,
                               int num_items, int grid, cudaStream_t s);
 

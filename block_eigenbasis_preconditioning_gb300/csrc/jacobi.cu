@@ -2,7 +2,8 @@
 // ("Dobb", Abstract: a complete basis within each block; Table 15: exact
 // eigendecomposition refresh).
 //
-// One-sided (Hestenes) Jacobi with V accumulated: U starts as A, V as I; each
+// One-sided (Hestenes) Jacobi with V accumulated: V starts as the current
+// basis Q (the identity before the first refresh) and U as A V; each
 // rotation of a column pair (p, q) makes u_p and u_q orthogonal and applies
 // the same rotation to v_p, v_q, so A V = U is kept.  Pairs are visited in
 // round-robin (circle) order: each round holds k/2 disjoint pairs that the
@@ -81,21 +82,33 @@ jacobi_kernel(const __grid_constant__ EigArgs a, int smem_floats) {
     }
     int* perm = reinterpret_cast<int*>(lamv + kp2);
 
-    // U = A (column p of U is row p of the symmetric A), V = I, ||A||_F^2
+    // Warm start from the current basis: V = Q (column j of V is column j of
+    // the row-major Q), U = A V.  With Q = I (no refresh yet) this is the
+    // plain start U = A, V = I.  ||A||_F^2 and a finiteness check on the way.
     float ss = 0.f;
     int bad = 0;
+    const float* Qold = a.Q + boff;
     for (int64_t e = tid; e < kk2; e += blockDim.x) {
       const float v = Ab[e];
       bad |= !isfinite(v);
       ss = fmaf(v, v, ss);
-      U[e] = v;
-      V[e] = ((e / k) == (e % k)) ? 1.f : 0.f;
+      const int j = (int)(e / k), l = (int)(e % k);
+      V[e] = Qold[(int64_t)l * k + j];
     }
     if (__syncthreads_or(bad)) {
       if (tid == 0) atomicOr(flag, (uint32_t)DOBB_FLAG_NONFINITE_A);
       continue;  // keep the previous basis
     }
     const float fro2 = block_sum(ss, red);
+    for (int p = warp; p < k; p += nw) {
+      const float* vp = V + (int64_t)p * k;
+      for (int i = lane; i < k; i += 32) {
+        float acc = 0.f;
+        for (int l = 0; l < k; ++l) acc = fmaf(Ab[(int64_t)l * k + i], vp[l], acc);  // A symmetric
+        U[(int64_t)p * k + i] = acc;
+      }
+    }
+    __syncthreads();
     const float tol = a.tol > 0.f ? a.tol : 4.f * sqrtf((float)k) * kEps;
     const float tau = 0.25f * kEps * sqrtf(fro2);
     const int kk = k + (k & 1);

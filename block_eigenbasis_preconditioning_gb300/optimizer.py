@@ -85,7 +85,7 @@ class Dobb:
                                          ctypes.byref(ptr), ctypes.byref(nbytes)))
         off = int(ptr.value) - self.state.data_ptr()
         raw = self.state[off:off + int(nbytes.value)]
-        if which == "flags":
+        if which in ("flags", "error"):
             return raw.view(torch.int32)
         t = raw.view(torch.float32)
         if matrix < 0:
@@ -111,6 +111,16 @@ class Dobb:
     @t.setter
     def t(self, value: int) -> None:
         check(self.lib.dobb_set_step(self.handle, int(value)))
+
+    def set_step_path(self, path: str = "auto") -> None:
+        """"auto": tensor-core kernel where eligible; "ffma": FP32 FFMA kernel only."""
+        check(self.lib.dobb_set_step_path(self.handle, {"auto": 0, "ffma": 1}[path]))
+
+    def sync_bases(self, stream=None) -> None:
+        check(self.lib.dobb_sync_bases(self.handle, _stream_ptr(stream)))
+
+    def device_error(self) -> int:
+        return int(self.tensor("error").item())
 
     def set_jacobi(self, max_sweeps: int = 40, tol: float = 0.0) -> None:
         check(self.lib.dobb_set_jacobi(self.handle, int(max_sweeps), float(tol)))

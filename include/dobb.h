@@ -74,8 +74,10 @@ typedef enum {
   DOBB_T_EIGVALS = 2,  /* Lambda: per matrix B x k fp32, descending within a block         */
   DOBB_T_MOMENTUM = 3, /* M: per matrix m x n fp32, row-major                              */
   DOBB_T_FLAGS = 4,    /* per block uint32 flag bits (all blocks of all matrices)          */
-  DOBB_T_STATS = 5     /* per block 4 fp32: ||U_b||_F^2, ||C_b||_F^2 of the last step,
-                          Jacobi sweeps and final relative off-norm of the last refresh     */
+  DOBB_T_STATS = 5,    /* per block 4 fp32: ||U_b||_F^2, ||C_b||_F^2 of the last step,
+                          Jacobi sweeps and rotations of the last sweep of the last refresh */
+  DOBB_T_ERROR = 6     /* one uint32: nonzero if a device-side wait timed out (the step
+                          that set it must be treated as failed); cleared by the caller    */
 } dobb_tensor;
 
 /* Bytes of device state for the given matrix set (m[i] x n[i], n[i] % B == 0).
@@ -168,6 +170,17 @@ dobb_status dobb_set_state(dobb_handle h, const void* src_dev, size_t src_bytes,
 
 /* Number of kernel launches issued by this handle since creation (host count). */
 int64_t dobb_launch_count(dobb_handle h);
+
+/* Update-kernel selection: 0 (default) runs the tcgen05 tensor-core kernel for
+ * every matrix with k % 4 == 0 and k <= 448 (and 16-byte aligned W, G) and the
+ * FP32 FFMA kernel for the rest; 1 runs the FFMA kernel for all matrices.
+ * Both compute the same update within the documented tolerance. */
+dobb_status dobb_set_step_path(dobb_handle h, int path);
+
+/* Re-derive the tensor-core operand images of the bases after the caller
+ * wrote Q directly through dobb_state_tensor(DOBB_T_BASES).  Refresh, create
+ * and dobb_set_state do this themselves. */
+dobb_status dobb_sync_bases(dobb_handle h, void* stream);
 
 #ifdef __cplusplus
 }

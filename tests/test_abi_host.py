@@ -64,9 +64,10 @@ def test_state_bytes_scale_with_model():
     assert ms_.num_params == 1_554_971_200
     ms, ns = _shape_args(ms_.shapes)
     nb = lib.dobb_state_bytes(len(ms_.shapes), ms, ns, 16)
-    # momentum alone is 4 bytes per parameter
+    # momentum alone is 4 bytes per parameter; moments, bases, packed tensor-core
+    # operand images and eigensolver scratch add about 3 more at B = 16
     assert nb > 4 * ms_.num_params
-    assert nb < 6 * ms_.num_params
+    assert nb < 8 * ms_.num_params
 
 
 def test_create_rejects_bad_arguments_without_device():

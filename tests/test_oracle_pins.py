@@ -451,6 +451,16 @@ def test_parity_rules_detect_planted_errors():
     Wbad = Wb.copy()
     Wbad[0, 0] = O.round_to_bf16(np.array([Wb[0, 0] * (1 + 2 ** -6)]))[0]
     assert MX.bf16_parity(Wbad, W)["violations"] == 1
+    # a value whose exact result sits on a rounding midpoint may round either way
+    x = np.array([1.0 + 2.0 ** -8, 0.5])
+    assert MX.bf16_parity(np.array([1.0 + 2.0 ** -7, 0.5]), x)["violations"] == 0
+    assert MX.bf16_parity(np.array([1.0, 0.5]), x)["violations"] == 0
+    # tiny entries: any value reachable from within the normwise band is accepted
+    y = np.array([1e-6, 0.08])
+    ok = O.round_to_bf16(np.array([1e-6 + 5e-7, 0.08]))
+    assert MX.bf16_parity(ok, y)["violations"] == 0
+    bad = O.round_to_bf16(np.array([1e-6 + 2e-6, 0.08]))
+    assert MX.bf16_parity(bad, y)["violations"] == 1
     assert MX.w_rel_error(W, W) == 0.0
 
 
