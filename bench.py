@@ -143,8 +143,10 @@ def make_inputs(torch, shapes, layers, device, seed, n_xsets=2):
     from block_eigenbasis_preconditioning_gb300 import inputs as I
     g = torch.Generator(device=device)
     g.manual_seed(seed)
+    import numpy as np
     nl = max(layers) if layers else 1
     lam_cache = {}
+    haar_cache = {}
     Xsets = [[] for _ in range(n_xsets)]
     Gs, Ws = [], []
     for (m, n), li in zip(shapes, layers):
@@ -155,9 +157,13 @@ def make_inputs(torch, shapes, layers, device, seed, n_xsets=2):
             lam = lam * (n / lam.sum())
             lam_cache[key] = torch.tensor(lam, dtype=torch.float32, device=device).sqrt_()
         sq = lam_cache[key]
-        z = torch.randn(n, n, generator=g, device=device)
-        q, r = torch.linalg.qr(z)
-        q = q * torch.sign(torch.diagonal(r)).unsqueeze(0)
+        if n not in haar_cache:
+            haar_cache[n] = torch.tensor(I.haar_orthogonal(n, np.random.default_rng(seed + n)),
+                                         dtype=torch.float32, device=device)
+        # per-matrix eigenvectors: the shared Haar basis with permuted, sign-flipped rows
+        perm = torch.randperm(n, generator=g, device=device)
+        flip = torch.randint(0, 2, (n, 1), generator=g, device=device).float() * 2 - 1
+        q = haar_cache[n][perm] * flip
         for s in range(n_xsets):
             Z = torch.randn(N_TOKENS, n, generator=g, device=device)
             X = (Z * sq.unsqueeze(0)) @ q.T
@@ -351,10 +357,10 @@ def run_gpu(args):
     wm = work_model(shapes, B_BLOCKS, N_TOKENS)
     alu_peak_tflops = 152 * 128 * 2 * 2.07e9 / 1e12  # FP32 lanes x FMA x max SM clock
     phases = {
-        "update": {"ms": upd_mean, "kernel": "step_ffma_kernel", "bound": "hbm",
+        "update": {"ms": upd_mean, "kernel": "step_tc_kernel", "bound": "hbm",
                    "achieved": wm["update_bytes"] / (upd_mean * 1e-3) / 1e9 if upd_mean else None,
                    "peak": hbm, "unit": "GB/s", "flops": wm["update_flops"], "bytes": wm["update_bytes"]},
-        "accumulate": {"ms": mean(acc_ms), "kernel": "syrk_ema_kernel", "bound": "hbm",
+        "accumulate": {"ms": mean(acc_ms), "kernel": "syrk_tc_kernel", "bound": "hbm",
                        "achieved": wm["acc_bytes"] / (mean(acc_ms) * 1e-3) / 1e9,
                        "peak": hbm, "unit": "GB/s", "flops": wm["acc_flops"], "bytes": wm["acc_bytes"]},
         "refresh": {"ms": refresh_ms, "kernel": "jacobi_kernel", "bound": "alu",

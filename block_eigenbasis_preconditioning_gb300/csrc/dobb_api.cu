@@ -255,7 +255,7 @@ Layout compute_layout(int num, const int64_t* m, const int64_t* n, int B, size_t
   L.off_maps = off;   off = align_up(off + sizeof(CUtensorMap) * (size_t)num);
   L.off_tiles = off;  off = align_up(off + sizeof(Tile) * n_tiles);
   L.off_pack = off;   off = align_up(off + L.pack_bytes);
-  L.off_scratch = off; off = align_up(off + 8 * L.a_floats);
+  L.off_scratch = off; off = align_up(off + 12 * L.a_floats);  // 3 k^2 floats per block
   L.total = off;
   L.n_tiles = n_tiles;
   return L;
@@ -282,6 +282,7 @@ struct dobb_ctx {
   size_t smem_per_sm = 0;
   int64_t launches = 0;
   int path = 0;            // 0: tensor-core kernel where eligible, 1: FFMA only
+  bool cluster_ok = true;  // cluster eigensolver usable for 168 < k <= 448
   // cached X tensor maps (pointer and token count they were encoded for)
   std::vector<CUtensorMap> xmaps;
   std::vector<const void*> xmap_ptr;
@@ -328,20 +329,20 @@ dobb_status do_pack(dobb_handle h, cudaStream_t s) {
 }
 
 dobb_status do_refresh(dobb_handle h, cudaStream_t s) {
+  const int smem_max_k = jacobi_smem_max_k(h->smem_limit);
   for (const Chunk& ch : h->wl.chunks) {
     if (ch.eig_n == 0) continue;
-    // blocks whose U and V fit in shared memory keep them there; larger
-    // blocks use the global scratch area and only sort in shared memory
-    size_t smem = 0;
-    for (int i = ch.mat_base; i < ch.mat_end; ++i) {
-      const int k = (int)(h->n[i] / h->B);
-      const size_t full = jacobi_smem_for(k);
-      smem = std::max(smem, full <= h->smem_limit ? full : jacobi_sort_smem_for(k));
-    }
+    // the list is sorted by decreasing k: [global-memory | cluster | shared-memory]
+    const Tile* items = h->wl.tiles.data() + ch.eig_off;
+    auto kof = [&](int idx) { return (int)(h->n[items[idx].mat] / h->B); };
+    int b1 = 0;
+    while (b1 < ch.eig_n && !(kof(b1) <= smem_max_k ||
+                              (h->cluster_ok && jacobi_cluster_fits(kof(b1), h->smem_limit))))
+      ++b1;
+    int b2 = b1;
+    while (b2 < ch.eig_n && kof(b2) > smem_max_k) ++b2;
     EigArgs a{};
     a.info = h->dinfo();
-    a.tiles = h->dtiles() + ch.eig_off;
-    a.num_tiles = ch.eig_n;
     a.max_sweeps = h->max_sweeps;
     a.A = h->A();
     a.Q = h->Q();
@@ -350,11 +351,36 @@ dobb_status do_refresh(dobb_handle h, cudaStream_t s) {
     a.flags = h->flags();
     a.stats = h->stats();
     a.tol = h->tol;
-    const int by_smem = std::max(1, (int)(h->smem_per_sm / (smem + 1024)));
-    const int g = std::max(1, std::min(ch.eig_n, h->sm_count * std::min(jacobi_ctas_per_sm(), by_smem)));
-    cudaError_t e = launch_jacobi(a, g, smem, s);
-    if (e != cudaSuccess) return fail(DOBB_ERR_CUDA, "eigen launch: %s", cudaGetErrorString(e));
-    ++h->launches;
+    // single-CTA kernel: wide blocks from global scratch, narrow ones in shared memory
+    for (int part = 0; part < 2; ++part) {
+      const int lo = part == 0 ? 0 : b2, hi = part == 0 ? b1 : ch.eig_n;
+      if (hi <= lo) continue;
+      size_t smem = 0;
+      for (int idx = lo; idx < hi; ++idx) {
+        const int k = kof(idx);
+        const size_t full = jacobi_smem_for(k);
+        smem = std::max(smem, full <= h->smem_limit ? full : jacobi_sort_smem_for(k));
+      }
+      a.tiles = h->dtiles() + ch.eig_off + lo;
+      a.num_tiles = hi - lo;
+      const int by_smem = std::max(1, (int)(h->smem_per_sm / (smem + 1024)));
+      const int g = std::max(1, std::min(a.num_tiles, h->sm_count * std::min(jacobi_ctas_per_sm(), by_smem)));
+      cudaError_t e = launch_jacobi(a, g, smem, s);
+      if (e != cudaSuccess) return fail(DOBB_ERR_CUDA, "eigen launch: %s", cudaGetErrorString(e));
+      ++h->launches;
+    }
+    if (b2 > b1) {
+      size_t smem = 0;
+      for (int idx = b1; idx < b2; ++idx) smem = std::max(smem, jacobi_cluster_smem(kof(idx)));
+      a.tiles = h->dtiles() + ch.eig_off + b1;
+      a.num_tiles = b2 - b1;
+      int clusters = jacobi_cluster_max_active(smem);
+      if (clusters <= 0) clusters = std::max(1, h->sm_count / 8);
+      clusters = std::min(clusters, a.num_tiles);
+      cudaError_t e = launch_jacobi_cluster(a, clusters, smem, s);
+      if (e != cudaSuccess) return fail(DOBB_ERR_CUDA, "cluster eigen launch: %s", cudaGetErrorString(e));
+      ++h->launches;
+    }
   }
   return do_pack(h, s);
 }
@@ -494,7 +520,8 @@ dobb_status dobb_create(dobb_handle* out, int num_matrices, const int64_t* m, co
   if ((e = configure_jacobi(h->smem_limit)) != cudaSuccess ||
       (e = configure_step(h->smem_limit)) != cudaSuccess ||
       (e = configure_step_tc(h->smem_limit)) != cudaSuccess ||
-      (e = configure_syrk_tc(h->smem_limit)) != cudaSuccess) {
+      (e = configure_syrk_tc(h->smem_limit)) != cudaSuccess ||
+      (e = configure_jacobi_cluster(h->smem_limit)) != cudaSuccess) {
     delete h;
     return fail(DOBB_ERR_CUDA, "kernel configuration: %s", cudaGetErrorString(e));
   }

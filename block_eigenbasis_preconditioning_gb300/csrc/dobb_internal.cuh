@@ -92,7 +92,7 @@ struct EigArgs {
   const float* A;
   float* Q;
   float* lam;
-  float* scratch;         // 2 * (floats of the A region): U and V of each block
+  float* scratch;         // 3 * (floats of the A region): U, V and the polish matrix of each block
   uint32_t* flags;
   float* stats;
   float tol;              // relative orthogonality threshold (0 = default)
@@ -140,6 +140,11 @@ size_t jacobi_sort_smem_for(int k);
 int jacobi_ctas_per_sm();
 size_t step_smem_for(int k);
 cudaError_t configure_jacobi(size_t smem_limit);
+size_t jacobi_cluster_smem(int k);
+bool jacobi_cluster_fits(int k, size_t smem_limit);
+cudaError_t configure_jacobi_cluster(size_t smem_limit);
+int jacobi_cluster_max_active(size_t smem);
+cudaError_t launch_jacobi_cluster(const EigArgs& a, int clusters, size_t smem, cudaStream_t s);
 cudaError_t configure_step(size_t smem_limit);
 size_t step_tc_smem(int max_k);
 size_t step_tc_bstage(int max_k);
