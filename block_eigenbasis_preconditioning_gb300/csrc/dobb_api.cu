@@ -282,7 +282,6 @@ struct dobb_ctx {
   size_t smem_per_sm = 0;
   int64_t launches = 0;
   int path = 0;            // 0: tensor-core kernel where eligible, 1: FFMA only
-  bool cluster_ok = true;  // cluster eigensolver usable for 168 < k <= 448
   // cached X tensor maps (pointer and token count they were encoded for)
   std::vector<CUtensorMap> xmaps;
   std::vector<const void*> xmap_ptr;
@@ -332,15 +331,10 @@ dobb_status do_refresh(dobb_handle h, cudaStream_t s) {
   const int smem_max_k = jacobi_smem_max_k(h->smem_limit);
   for (const Chunk& ch : h->wl.chunks) {
     if (ch.eig_n == 0) continue;
-    // the list is sorted by decreasing k: [global-memory | cluster | shared-memory]
+    // the list is sorted by decreasing k: [U, V in global scratch | in shared memory]
     const Tile* items = h->wl.tiles.data() + ch.eig_off;
-    auto kof = [&](int idx) { return (int)(h->n[items[idx].mat] / h->B); };
-    int b1 = 0;
-    while (b1 < ch.eig_n && !(kof(b1) <= smem_max_k ||
-                              (h->cluster_ok && jacobi_cluster_fits(kof(b1), h->smem_limit))))
-      ++b1;
-    int b2 = b1;
-    while (b2 < ch.eig_n && kof(b2) > smem_max_k) ++b2;
+    int b = 0;
+    while (b < ch.eig_n && (int)(h->n[items[b].mat] / h->B) > smem_max_k) ++b;
     EigArgs a{};
     a.info = h->dinfo();
     a.max_sweeps = h->max_sweeps;
@@ -351,34 +345,21 @@ dobb_status do_refresh(dobb_handle h, cudaStream_t s) {
     a.flags = h->flags();
     a.stats = h->stats();
     a.tol = h->tol;
-    // single-CTA kernel: wide blocks from global scratch, narrow ones in shared memory
     for (int part = 0; part < 2; ++part) {
-      const int lo = part == 0 ? 0 : b2, hi = part == 0 ? b1 : ch.eig_n;
+      const int lo = part == 0 ? 0 : b, hi = part == 0 ? b : ch.eig_n;
       if (hi <= lo) continue;
       size_t smem = 0;
       for (int idx = lo; idx < hi; ++idx) {
-        const int k = kof(idx);
-        const size_t full = jacobi_smem_for(k);
-        smem = std::max(smem, full <= h->smem_limit ? full : jacobi_sort_smem_for(k));
+        const int k = (int)(h->n[items[idx].mat] / h->B);
+        smem = std::max(smem, part == 0 ? jacobi_sort_smem_for(k) : jacobi_smem_for(k));
       }
       a.tiles = h->dtiles() + ch.eig_off + lo;
       a.num_tiles = hi - lo;
       const int by_smem = std::max(1, (int)(h->smem_per_sm / (smem + 1024)));
-      const int g = std::max(1, std::min(a.num_tiles, h->sm_count * std::min(jacobi_ctas_per_sm(), by_smem)));
-      cudaError_t e = launch_jacobi(a, g, smem, s);
+      const int per_sm = part == 0 ? 1 : std::min(jacobi_ctas_per_sm(), by_smem);
+      const int g = std::max(1, std::min(a.num_tiles, h->sm_count * per_sm));
+      cudaError_t e = launch_jacobi(a, g, smem, s, part == 0);
       if (e != cudaSuccess) return fail(DOBB_ERR_CUDA, "eigen launch: %s", cudaGetErrorString(e));
-      ++h->launches;
-    }
-    if (b2 > b1) {
-      size_t smem = 0;
-      for (int idx = b1; idx < b2; ++idx) smem = std::max(smem, jacobi_cluster_smem(kof(idx)));
-      a.tiles = h->dtiles() + ch.eig_off + b1;
-      a.num_tiles = b2 - b1;
-      int clusters = jacobi_cluster_max_active(smem);
-      if (clusters <= 0) clusters = std::max(1, h->sm_count / 8);
-      clusters = std::min(clusters, a.num_tiles);
-      cudaError_t e = launch_jacobi_cluster(a, clusters, smem, s);
-      if (e != cudaSuccess) return fail(DOBB_ERR_CUDA, "cluster eigen launch: %s", cudaGetErrorString(e));
       ++h->launches;
     }
   }
@@ -520,8 +501,7 @@ dobb_status dobb_create(dobb_handle* out, int num_matrices, const int64_t* m, co
   if ((e = configure_jacobi(h->smem_limit)) != cudaSuccess ||
       (e = configure_step(h->smem_limit)) != cudaSuccess ||
       (e = configure_step_tc(h->smem_limit)) != cudaSuccess ||
-      (e = configure_syrk_tc(h->smem_limit)) != cudaSuccess ||
-      (e = configure_jacobi_cluster(h->smem_limit)) != cudaSuccess) {
+      (e = configure_syrk_tc(h->smem_limit)) != cudaSuccess) {
     delete h;
     return fail(DOBB_ERR_CUDA, "kernel configuration: %s", cudaGetErrorString(e));
   }

@@ -126,7 +126,8 @@ struct CheckArgs {
 
 // Launchers (return cudaGetLastError() of the launch).
 cudaError_t launch_syrk_ema(const AccArgs& a, int act_dtype, int grid, cudaStream_t s);
-cudaError_t launch_jacobi(const EigArgs& a, int grid, size_t smem_limit, cudaStream_t s);
+cudaError_t launch_jacobi(const EigArgs& a, int grid, size_t smem_bytes, cudaStream_t s,
+                          bool wide);
 cudaError_t launch_step_ffma(const StepArgs& a, int param_dtype, int grid, size_t smem,
                              cudaStream_t s);
 cudaError_t launch_check(const CheckArgs& a, int grid, cudaStream_t s);
@@ -140,11 +141,6 @@ size_t jacobi_sort_smem_for(int k);
 int jacobi_ctas_per_sm();
 size_t step_smem_for(int k);
 cudaError_t configure_jacobi(size_t smem_limit);
-size_t jacobi_cluster_smem(int k);
-bool jacobi_cluster_fits(int k, size_t smem_limit);
-cudaError_t configure_jacobi_cluster(size_t smem_limit);
-int jacobi_cluster_max_active(size_t smem);
-cudaError_t launch_jacobi_cluster(const EigArgs& a, int clusters, size_t smem, cudaStream_t s);
 cudaError_t configure_step(size_t smem_limit);
 size_t step_tc_smem(int max_k);
 size_t step_tc_bstage(int max_k);

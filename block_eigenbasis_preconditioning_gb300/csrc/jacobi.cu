@@ -68,10 +68,229 @@ __device__ __forceinline__ void newton_schulz_cols(const float* V, float* E, int
   }
 }
 
+// One rotation of the column pair (p, q) with the four columns held in
+// registers (k <= 32 kRegCols): all loads are issued at once, the dot products
+// and the rotation use the registers, results are stored once.  Same
+// arithmetic, in the same order, as the streaming loop.
+template <int kRegCols>
+__device__ __forceinline__ void rotate_pair_regs(float* up, float* uq, float* vp, float* vq, int k,
+                                                 int lane, float tol, float tau, int& rots) {
+  float xu[kRegCols], yu[kRegCols], xv[kRegCols], yv[kRegCols];
+#pragma unroll
+  for (int e = 0; e < kRegCols; ++e) {
+    const int i = lane + 32 * e;
+    const bool ok = i < k;
+    xu[e] = ok ? up[i] : 0.f;
+    yu[e] = ok ? uq[i] : 0.f;
+    xv[e] = ok ? vp[i] : 0.f;
+    yv[e] = ok ? vq[i] : 0.f;
+  }
+  float al = 0.f, be = 0.f, ga = 0.f;
+#pragma unroll
+  for (int e = 0; e < kRegCols; ++e) {
+    al = fmaf(xu[e], xu[e], al);
+    be = fmaf(yu[e], yu[e], be);
+    ga = fmaf(xu[e], yu[e], ga);
+  }
+  al = warp_sum(al);
+  be = warp_sum(be);
+  ga = warp_sum(ga);
+  if (fabsf(ga) > tol * sqrtf(al) * sqrtf(be) && fabsf(ga) > tau * sqrtf(fmaxf(al, be))) {
+    const float zeta = (be - al) / (2.f * ga);
+    const float tt = copysignf(1.f, zeta) / (fabsf(zeta) + sqrtf(1.f + zeta * zeta));
+    const float c = 1.f / sqrtf(1.f + tt * tt);
+    const float sn = c * tt;
+#pragma unroll
+    for (int e = 0; e < kRegCols; ++e) {
+      const int i = lane + 32 * e;
+      if (i < k) {
+        up[i] = c * xu[e] - sn * yu[e];
+        uq[i] = sn * xu[e] + c * yu[e];
+        vp[i] = c * xv[e] - sn * yv[e];
+        vq[i] = sn * xv[e] + c * yv[e];
+      }
+    }
+    ++rots;
+  }
+}
+
+// Shared-memory tiled product over the k x k operands of one block, FP32:
+//   C(i, j) = alpha * sum_l X(i, l) Y(l, j) + D(i, j) + (eye ? delta_ij : 0)
+// with Y(l, j) = Y[j k + l], X(i, l) = X[l k + i] (XT = false) or X[i k + l]
+// (XT = true); C(i, j) and D(i, j) are stored at [j k + i].  64 x 64 output
+// tiles, 32-deep reduction chunks, the CTA's 512 threads own 2 x 4 outputs.
+constexpr int kGT = 64, kGK = 32, kGP = kGT + 4;
+constexpr size_t kGemmSmemFloats = 2 * kGK * kGP;
+
+template <bool XT>
+__device__ void block_gemm(const float* X, const float* Y, float* C, const float* D, float alpha,
+                           bool eye, int k, float* gs) {
+  float* Xs = gs;
+  float* Ys = gs + kGK * kGP;
+  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;  // ty < 32 for 512 threads
+  const int nt = (k + kGT - 1) / kGT;
+  for (int tile = 0; tile < nt * nt; ++tile) {
+    const int i0 = (tile % nt) * kGT, j0 = (tile / nt) * kGT;
+    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    for (int l0 = 0; l0 < k; l0 += kGK) {
+      for (int e = tid; e < kGK * kGT; e += blockDim.x) {
+        // X tile: rows i0.., reduction l0..; coalesced along the contiguous index
+        int l, i;
+        if (XT) { l = e % kGK; i = e / kGK; } else { i = e % kGT; l = e / kGT; }
+        float xv = 0.f;
+        if (i0 + i < k && l0 + l < k)
+          xv = XT ? X[(int64_t)(i0 + i) * k + l0 + l] : X[(int64_t)(l0 + l) * k + i0 + i];
+        Xs[l * kGP + i] = xv;
+        const int ly = e % kGK, j = e / kGK;
+        float yv = 0.f;
+        if (j0 + j < k && l0 + ly < k) yv = Y[(int64_t)(j0 + j) * k + l0 + ly];
+        Ys[ly * kGP + j] = yv;
+      }
+      __syncthreads();
+#pragma unroll 8
+      for (int l = 0; l < kGK; ++l) {
+        const float a0 = Xs[l * kGP + ty * 2], a1 = Xs[l * kGP + ty * 2 + 1];
+        float b[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) b[q] = Ys[l * kGP + tx * 4 + q];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          acc[0][q] = fmaf(a0, b[q], acc[0][q]);
+          acc[1][q] = fmaf(a1, b[q], acc[1][q]);
+        }
+      }
+      __syncthreads();
+    }
+#pragma unroll
+    for (int p = 0; p < 2; ++p) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int i = i0 + ty * 2 + p, j = j0 + tx * 4 + q;
+        if (i < k && j < k) {
+          float v = alpha * acc[p][q];
+          if (D) v += D[(int64_t)j * k + i];
+          if (eye && i == j) v += 1.f;
+          C[(int64_t)j * k + i] = v;
+        }
+      }
+    }
+  }
+  __syncthreads();
+}
+
 __host__ __device__ __forceinline__ size_t smem_bytes_for(int k) {
   return (size_t)8 * k * k + (size_t)8 * pow2_ceil(k);
 }
 
+// Polish of a block whose U, V live in global scratch, with the tiled
+// products above (same steps as the in-shared-memory polish of the kernel):
+// E = I - V^T V; V1 = V + V E / 2; T = A V1; B = sym(V1^T T); one two-sided
+// Jacobi sweep on B accumulating W; V2 = V1 W; E2 = I - V2^T V2;
+// Q = (V2 + V2 E2 / 2) with columns sorted by descending diag(B).
+__device__ void polish_global(const float* Ab, float* U, float* V, float* Bm, float* Qb,
+                              float* lamv, int* perm, int k, int kp2, float fro2, float* gs) {
+  const int tid = threadIdx.x;
+  block_gemm<true>(V, V, Bm, nullptr, -1.f, true, k, gs);        // E
+  block_gemm<false>(V, Bm, U, V, 0.5f, false, k, gs);            // V1 (in U)
+  block_gemm<false>(Ab, U, V, nullptr, 1.f, false, k, gs);       // T = A V1 (A symmetric)
+  block_gemm<true>(U, V, Bm, nullptr, 1.f, false, k, gs);        // B = V1^T T
+  for (int64_t e = tid; e < (int64_t)k * k; e += blockDim.x) {
+    const int i = (int)(e % k), j = (int)(e / k);
+    if (i < j) {
+      const float v = 0.5f * (Bm[(int64_t)j * k + i] + Bm[(int64_t)i * k + j]);
+      Bm[(int64_t)j * k + i] = v;
+      Bm[(int64_t)i * k + j] = v;
+    }
+  }
+  for (int64_t e = tid; e < (int64_t)k * k; e += blockDim.x) V[e] = ((e / k) == (e % k)) ? 1.f : 0.f;
+  __syncthreads();
+  const int kk = k + (k & 1);
+  float* cs = lamv;
+  float* sn = lamv + (kp2 >> 1);
+  const float bfloor = 1e-3f * kEps * sqrtf(fro2);
+  for (int r = 0; r < kk - 1; ++r) {
+    for (int i = tid; i < kk / 2; i += blockDim.x) {
+      int p, q;
+      rr_pair(r, i, kk, p, q);
+      float c = 1.f, sv = 0.f;
+      if (p < k && q < k) {
+        if (p > q) { const int tt = p; p = q; q = tt; }
+        const float bpq = Bm[(int64_t)p * k + q];
+        if (fabsf(bpq) > bfloor) {
+          const float ta = (Bm[(int64_t)q * k + q] - Bm[(int64_t)p * k + p]) / (2.f * bpq);
+          const float tt = ta >= 0.f ? 1.f / (ta + sqrtf(1.f + ta * ta)) : -1.f / (-ta + sqrtf(1.f + ta * ta));
+          c = 1.f / sqrtf(1.f + tt * tt);
+          sv = tt * c;
+        }
+      }
+      cs[i] = c;
+      sn[i] = sv;
+    }
+    __syncthreads();
+    for (int64_t e = tid; e < (int64_t)(kk / 2) * k; e += blockDim.x) {
+      const int i = (int)(e / k), j = (int)(e % k);
+      if (sn[i] == 0.f) continue;
+      int p, q;
+      rr_pair(r, i, kk, p, q);
+      if (p > q) { const int tt = p; p = q; q = tt; }
+      const float x = Bm[(int64_t)p * k + j], y = Bm[(int64_t)q * k + j];
+      Bm[(int64_t)p * k + j] = cs[i] * x - sn[i] * y;
+      Bm[(int64_t)q * k + j] = sn[i] * x + cs[i] * y;
+    }
+    __syncthreads();
+    for (int64_t e = tid; e < (int64_t)(kk / 2) * k; e += blockDim.x) {
+      const int i = (int)(e / k), j = (int)(e % k);
+      if (sn[i] == 0.f) continue;
+      int p, q;
+      rr_pair(r, i, kk, p, q);
+      if (p > q) { const int tt = p; p = q; q = tt; }
+      float x = Bm[(int64_t)j * k + p], y = Bm[(int64_t)j * k + q];
+      Bm[(int64_t)j * k + p] = cs[i] * x - sn[i] * y;
+      Bm[(int64_t)j * k + q] = sn[i] * x + cs[i] * y;
+      x = V[(int64_t)p * k + j];
+      y = V[(int64_t)q * k + j];
+      V[(int64_t)p * k + j] = cs[i] * x - sn[i] * y;
+      V[(int64_t)q * k + j] = sn[i] * x + cs[i] * y;
+    }
+    __syncthreads();
+  }
+  block_gemm<false>(U, V, Qb, nullptr, 1.f, false, k, gs);       // V2 = V1 W (in Qb)
+  for (int p = tid; p < kp2; p += blockDim.x) {
+    lamv[p] = p < k ? Bm[(int64_t)p * k + p] : -INFINITY;
+    perm[p] = p;
+  }
+  __syncthreads();
+  block_gemm<true>(Qb, Qb, Bm, nullptr, -1.f, true, k, gs);      // E2
+  block_gemm<false>(Qb, Bm, U, Qb, 0.5f, false, k, gs);          // R = V2 + V2 E2 / 2 (in U)
+  for (int size = 2; size <= kp2; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = tid; i < kp2; i += blockDim.x) {
+        const int j = i ^ stride;
+        if (j > i) {
+          const bool desc = (i & size) == 0;
+          const float li = lamv[i], lj = lamv[j];
+          if (desc ? (li < lj) : (li > lj)) {
+            lamv[i] = lj;
+            lamv[j] = li;
+            const int pt = perm[i];
+            perm[i] = perm[j];
+            perm[j] = pt;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+  for (int64_t e = tid; e < (int64_t)k * k; e += blockDim.x) {
+    const int j = (int)(e / k), i = (int)(e % k);
+    int p = perm[j];
+    if (p < 0 || p >= k) p = j;  // only reachable with a NaN eigenvalue
+    Qb[(int64_t)i * k + j] = U[(int64_t)p * k + i];
+  }
+  __syncthreads();
+}
+
+template <int kRegCols>
 __global__ void __launch_bounds__(kThreads)
 jacobi_kernel(const __grid_constant__ EigArgs a, int smem_floats) {
   extern __shared__ __align__(16) float sm[];
@@ -145,6 +364,12 @@ jacobi_kernel(const __grid_constant__ EigArgs a, int smem_floats) {
           if (p >= k || q >= k) continue;
           float* up = U + (int64_t)p * k;
           float* uq = U + (int64_t)q * k;
+          if (kRegCols > 0 && k <= 32 * kRegCols) {
+            rotate_pair_regs<(kRegCols > 0 ? kRegCols : 1)>(up, uq, V + (int64_t)p * k,
+                                                            V + (int64_t)q * k, k, lane, tol, tau,
+                                                            my_rot);
+            continue;
+          }
           float al = 0.f, be = 0.f, ga = 0.f;
           for (int i = lane; i < k; i += 32) {
             const float x = up[i], y = uq[i];
@@ -184,6 +409,18 @@ jacobi_kernel(const __grid_constant__ EigArgs a, int smem_floats) {
       if (last_rot == 0) break;
     }
 
+    if (!in_smem) {
+      polish_global(Ab, U, V, Bm, a.Q + boff, lamv, perm, k, kp2, fro2, sm + 2 * kp2);
+      for (int j = tid; j < k; j += blockDim.x) a.lam[mi.lam_off + (int64_t)t.blk * k + j] = lamv[j];
+      if (tid == 0) {
+        float* st = a.stats + 4 * (int64_t)(mi.blk0 + t.blk);
+        st[2] = (float)sweep;
+        st[3] = (float)last_rot;
+        if (sweep >= a.max_sweeps && last_rot > 0) atomicOr(flag, (uint32_t)DOBB_FLAG_NOT_CONVERGED);
+      }
+      __syncthreads();
+      continue;
+    }
     float* Qb = a.Q + boff;  // holds V1 (column-major) until the final write
     // (1) E = I - V^T V into U (column q at U + q k), then V1 = V + V E / 2
     newton_schulz_cols(V, U, k, warp, nw, lane);
@@ -346,435 +583,27 @@ int jacobi_smem_max_k(size_t smem_limit) {
   return k;
 }
 
-cudaError_t launch_jacobi(const EigArgs& a, int grid, size_t smem_bytes, cudaStream_t s) {
+// wide = blocks whose U, V live in global scratch: those rotate column pairs
+// held in registers (k <= 512) and polish with the tiled products.
+cudaError_t launch_jacobi(const EigArgs& a, int grid, size_t smem_bytes, cudaStream_t s, bool wide) {
   if (a.num_tiles <= 0) return cudaSuccess;
-  jacobi_kernel<<<grid, kThreads, smem_bytes, s>>>(a, (int)(smem_bytes / 4));
+  if (wide)
+    jacobi_kernel<16><<<grid, kThreads, smem_bytes, s>>>(a, (int)(smem_bytes / 4));
+  else
+    jacobi_kernel<0><<<grid, kThreads, smem_bytes, s>>>(a, (int)(smem_bytes / 4));
   return cudaGetLastError();
 }
 
 size_t jacobi_smem_for(int k) { return smem_bytes_for(k); }
-size_t jacobi_sort_smem_for(int k) { return (size_t)8 * pow2_ceil(k); }
+size_t jacobi_sort_smem_for(int k) { return (size_t)8 * pow2_ceil(k) + 4 * kGemmSmemFloats; }
 int jacobi_ctas_per_sm() { return 2048 / kThreads; }
 
 cudaError_t configure_jacobi(size_t smem_limit) {
-  return cudaFuncSetAttribute(jacobi_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(jacobi_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem_limit);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(jacobi_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)smem_limit);
-}
-
-}  // namespace dobb
-
-// ===========================================================================
-// Cluster variant for blocks too wide for one CTA's shared memory (k <= 448).
-//
-// The same one-sided Jacobi and polish, spread over a cluster of kCl CTAs.
-// Columns are split into 2 kCl groups of g = ceil(k / (2 kCl)) columns; the
-// groups play a round-robin tournament (2 kCl - 1 block rounds per sweep).
-// In each block round CTA c loads its two groups (U and V columns) from the
-// L2-resident scratch into shared memory, rotates every cross pair (g rounds
-// of g disjoint pairs, one warp per pair; in the first block round of a sweep
-// also every pair inside each group), writes them back, and the cluster
-// synchronises.  Every pair of columns is thus rotated once per sweep.  The
-// polish phases split their columns (or pairs) over the cluster's CTAs, with
-// a cluster barrier between phases.
-// ===========================================================================
-#include <cooperative_groups.h>
-
-namespace dobb {
-namespace {
-
-namespace cg = cooperative_groups;
-constexpr int kCl = 8;           // CTAs per cluster
-constexpr int kClThreads = 1024;
-
-__device__ __forceinline__ void rotate_pair(float* up, float* uq, float* vp, float* vq, int k,
-                                            int lane, float tol, float tau, int& rots) {
-  float al = 0.f, be = 0.f, ga = 0.f;
-  for (int i = lane; i < k; i += 32) {
-    const float x = up[i], y = uq[i];
-    al = fmaf(x, x, al);
-    be = fmaf(y, y, be);
-    ga = fmaf(x, y, ga);
-  }
-  al = warp_sum(al);
-  be = warp_sum(be);
-  ga = warp_sum(ga);
-  if (fabsf(ga) > tol * sqrtf(al) * sqrtf(be) && fabsf(ga) > tau * sqrtf(fmaxf(al, be))) {
-    const float zeta = (be - al) / (2.f * ga);
-    const float tt = copysignf(1.f, zeta) / (fabsf(zeta) + sqrtf(1.f + zeta * zeta));
-    const float c = 1.f / sqrtf(1.f + tt * tt);
-    const float s = c * tt;
-    for (int i = lane; i < k; i += 32) {
-      const float x = up[i], y = uq[i];
-      up[i] = c * x - s * y;
-      uq[i] = s * x + c * y;
-    }
-    for (int i = lane; i < k; i += 32) {
-      const float x = vp[i], y = vq[i];
-      vp[i] = c * x - s * y;
-      vq[i] = s * x + c * y;
-    }
-    ++rots;
-  }
-}
-
-__global__ void __launch_bounds__(kClThreads, 1)
-jacobi_cluster_kernel(const __grid_constant__ EigArgs a, int num_clusters) {
-  extern __shared__ __align__(16) float sm[];
-  __shared__ float red[32];
-  __shared__ int s_rot;
-  cg::cluster_group cl = cg::this_cluster();
-  const int rank = (int)cl.block_rank();
-  const int cid = blockIdx.x / kCl;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
-  for (int w = cid; w < a.num_tiles; w += num_clusters) {
-    const Tile t = a.tiles[w];
-    const MatInfo mi = a.info[t.mat];
-    const int k = mi.k;
-    const int kp2 = pow2_ceil(k);
-    const int64_t kk2 = (int64_t)k * k;
-    const int64_t boff = mi.a_off + (int64_t)t.blk * kk2;
-    const float* Ab = a.A + boff;
-    uint32_t* flag = a.flags + mi.blk0 + t.blk;
-    float* U = a.scratch + 3 * boff;
-    float* V = U + kk2;
-    float* Bm = U + 2 * kk2;
-    float* Qb = a.Q + boff;
-    // per-block rotation counters (two, alternating by sweep) after the moments
-    int* counters = reinterpret_cast<int*>(a.lam + mi.lam_off + (int64_t)t.blk * k);
-    const int g = (k + 2 * kCl - 1) / (2 * kCl);
-    float* sU = sm;                     // [2g][k]
-    float* sV = sm + 2 * g * k;         // [2g][k]
-    float* lamv = sm + 4 * g * k;       // kp2
-    int* perm = reinterpret_cast<int*>(lamv + kp2);
-    // columns of phase-split work: [c0, c1)
-    const int per = (k + kCl - 1) / kCl;
-    const int c0 = min(k, rank * per), c1 = min(k, c0 + per);
-
-    // ||A||_F and finiteness (every CTA, identical result)
-    float ss = 0.f;
-    int bad = 0;
-    for (int64_t e = tid; e < kk2; e += blockDim.x) {
-      const float v = Ab[e];
-      bad |= !isfinite(v);
-      ss = fmaf(v, v, ss);
-    }
-    bad = __syncthreads_or(bad);
-    if (bad) {
-      if (rank == 0 && tid == 0) atomicOr(flag, (uint32_t)DOBB_FLAG_NONFINITE_A);
-      cl.sync();
-      continue;
-    }
-    const float fro2 = block_sum(ss, red);
-    const float tol = a.tol > 0.f ? a.tol : 4.f * sqrtf((float)k) * kEps;
-    const float tau = 0.25f * kEps * sqrtf(fro2);
-    // warm start: V = Q (columns), U = A V, for this CTA's columns
-    for (int64_t e = tid; e < (int64_t)(c1 - c0) * k; e += blockDim.x) {
-      const int j = c0 + (int)(e / k), l = (int)(e % k);
-      V[(int64_t)j * k + l] = Qb[(int64_t)l * k + j];
-    }
-    __syncthreads();
-    for (int p = c0 + warp; p < c1; p += nw) {
-      const float* vp = V + (int64_t)p * k;
-      for (int i = lane; i < k; i += 32) {
-        float acc = 0.f;
-        for (int l = 0; l < k; ++l) acc = fmaf(Ab[(int64_t)l * k + i], vp[l], acc);
-        U[(int64_t)p * k + i] = acc;
-      }
-    }
-    if (rank == 0 && tid < 2) counters[tid] = 0;
-    cl.sync();
-
-    int sweep = 0, last_rot = 0;
-    const int G2 = 2 * kCl;
-    for (; sweep < a.max_sweeps; ++sweep) {
-      if (tid == 0) s_rot = 0;
-      int my_rot = 0;
-      for (int br = 0; br < G2 - 1; ++br) {
-        int gI, gJ;
-        rr_pair(br, rank, G2, gI, gJ);
-        const int nI = max(0, min(g, k - gI * g)), nJ = max(0, min(g, k - gJ * g));
-        // load both groups (local columns 0..g-1 = I, g..2g-1 = J)
-        for (int64_t e = tid; e < (int64_t)2 * g * k; e += blockDim.x) {
-          const int lc = (int)(e / k), i = (int)(e % k);
-          const int gc = lc < g ? gI * g + lc : gJ * g + (lc - g);
-          const bool ok = lc < g ? lc < nI : (lc - g) < nJ;
-          sU[e] = ok ? U[(int64_t)gc * k + i] : 0.f;
-          sV[e] = ok ? V[(int64_t)gc * k + i] : 0.f;
-        }
-        __syncthreads();
-        if (br == 0) {
-          // pairs inside each group: round robin over gg players
-          const int gg = g + (g & 1);
-          for (int r = 0; r < gg - 1; ++r) {
-            for (int pw = warp; pw < gg; pw += nw) {  // gg/2 pairs per group, two groups
-              const int grp = pw / (gg / 2), i = pw % (gg / 2);
-              int p, q;
-              rr_pair(r, i, gg, p, q);
-              const int n = grp == 0 ? nI : nJ;
-              if (p >= n || q >= n) continue;
-              const int lp = grp * g + p, lq = grp * g + q;
-              rotate_pair(sU + (int64_t)lp * k, sU + (int64_t)lq * k, sV + (int64_t)lp * k,
-                          sV + (int64_t)lq * k, k, lane, tol, tau, my_rot);
-            }
-            __syncthreads();
-          }
-        }
-        // cross pairs: round rho pairs I-column i with J-column (i + rho) mod g
-        for (int rho = 0; rho < g; ++rho) {
-          for (int i = warp; i < g; i += nw) {
-            const int j = (i + rho) % g;
-            if (i >= nI || j >= nJ) continue;
-            rotate_pair(sU + (int64_t)i * k, sU + (int64_t)(g + j) * k, sV + (int64_t)i * k,
-                        sV + (int64_t)(g + j) * k, k, lane, tol, tau, my_rot);
-          }
-          __syncthreads();
-        }
-        // write back
-        for (int64_t e = tid; e < (int64_t)2 * g * k; e += blockDim.x) {
-          const int lc = (int)(e / k), i = (int)(e % k);
-          const int gc = lc < g ? gI * g + lc : gJ * g + (lc - g);
-          const bool ok = lc < g ? lc < nI : (lc - g) < nJ;
-          if (ok) {
-            U[(int64_t)gc * k + i] = sU[e];
-            V[(int64_t)gc * k + i] = sV[e];
-          }
-        }
-        cl.sync();
-      }
-      if (lane == 0 && my_rot) atomicAdd(&s_rot, my_rot);
-      __syncthreads();
-      if (tid == 0 && s_rot) atomicAdd(&counters[sweep & 1], s_rot);
-      cl.sync();
-      last_rot = *reinterpret_cast<volatile int*>(&counters[sweep & 1]);
-      cl.sync();
-      if (rank == 0 && tid == 0) counters[sweep & 1] = 0;
-      if (last_rot == 0) break;
-    }
-    cl.sync();
-
-    // ---- polish (columns / pairs split over the cluster) ----
-    // (1) E = I - V^T V (columns c0..c1) into U; then V1 = V + V E / 2 into Q
-    for (int q = c0 + warp; q < c1; q += nw) {
-      const float* vq = V + (int64_t)q * k;
-      for (int p = 0; p < k; ++p) {
-        const float* vp = V + (int64_t)p * k;
-        float d = 0.f;
-        for (int i = lane; i < k; i += 32) d = fmaf(vp[i], vq[i], d);
-        d = warp_sum(d);
-        if (lane == 0) U[(int64_t)q * k + p] = (p == q ? 1.f : 0.f) - d;
-      }
-    }
-    cl.sync();
-    for (int j = c0 + warp; j < c1; j += nw) {
-      const float* ej = U + (int64_t)j * k;
-      for (int i = lane; i < k; i += 32) {
-        float acc = 0.f;
-        for (int q = 0; q < k; ++q) acc = fmaf(V[(int64_t)q * k + i], ej[q], acc);
-        Qb[(int64_t)j * k + i] = fmaf(0.5f, acc, V[(int64_t)j * k + i]);
-      }
-    }
-    cl.sync();
-    // (2) T = A V1 into U; B = V1^T T into Bm; W = I into V
-    for (int p = c0 + warp; p < c1; p += nw) {
-      const float* v1 = Qb + (int64_t)p * k;
-      for (int i = lane; i < k; i += 32) {
-        float acc = 0.f;
-        for (int l = 0; l < k; ++l) acc = fmaf(Ab[(int64_t)l * k + i], v1[l], acc);
-        U[(int64_t)p * k + i] = acc;
-      }
-    }
-    cl.sync();
-    for (int p = c0 + warp; p < c1; p += nw) {
-      const float* v1p = Qb + (int64_t)p * k;
-      const float* tp = U + (int64_t)p * k;
-      for (int q = 0; q < k; ++q) {
-        const float* v1q = Qb + (int64_t)q * k;
-        const float* tq = U + (int64_t)q * k;
-        float d = 0.f;
-        for (int i = lane; i < k; i += 32) d = fmaf(v1p[i], tq[i], fmaf(v1q[i], tp[i], d));
-        d = 0.5f * warp_sum(d);
-        if (lane == 0) Bm[(int64_t)p * k + q] = d;  // row p; symmetric by construction
-      }
-    }
-    for (int64_t e = (int64_t)c0 * k + tid; e < (int64_t)c1 * k; e += blockDim.x)
-      V[e] = ((e / k) == (e % k)) ? 1.f : 0.f;
-    cl.sync();
-    // (3) one two-sided sweep on B; pairs of a round split over the cluster
-    const int kk = k + (k & 1);
-    float* cs = lamv;
-    float* sn = lamv + (kp2 >> 1);
-    const float bfloor = 1e-3f * kEps * sqrtf(fro2);
-    for (int r = 0; r < kk - 1; ++r) {
-      for (int i = tid; i < kk / 2; i += blockDim.x) {
-        int p, q;
-        rr_pair(r, i, kk, p, q);
-        float c = 1.f, sv = 0.f;
-        if (p < k && q < k) {
-          if (p > q) { const int tt = p; p = q; q = tt; }
-          const float bpq = Bm[(int64_t)p * k + q];
-          if (fabsf(bpq) > bfloor) {
-            const float tau2 = (Bm[(int64_t)q * k + q] - Bm[(int64_t)p * k + p]) / (2.f * bpq);
-            const float tt = tau2 >= 0.f ? 1.f / (tau2 + sqrtf(1.f + tau2 * tau2))
-                                         : -1.f / (-tau2 + sqrtf(1.f + tau2 * tau2));
-            c = 1.f / sqrtf(1.f + tt * tt);
-            sv = tt * c;
-          }
-        }
-        cs[i] = c;
-        sn[i] = sv;
-      }
-      __syncthreads();
-      // rows p, q of B (pairs i with i % kCl == rank)
-      for (int64_t e = tid; e < (int64_t)(kk / 2) * k; e += blockDim.x) {
-        const int i = (int)(e / k), j = (int)(e % k);
-        if (i % kCl != rank || sn[i] == 0.f) continue;
-        int p, q;
-        rr_pair(r, i, kk, p, q);
-        if (p > q) { const int tt = p; p = q; q = tt; }
-        const float x = Bm[(int64_t)p * k + j], y = Bm[(int64_t)q * k + j];
-        Bm[(int64_t)p * k + j] = cs[i] * x - sn[i] * y;
-        Bm[(int64_t)q * k + j] = sn[i] * x + cs[i] * y;
-      }
-      cl.sync();
-      // columns p, q of B and W
-      for (int64_t e = tid; e < (int64_t)(kk / 2) * k; e += blockDim.x) {
-        const int i = (int)(e / k), j = (int)(e % k);
-        if (i % kCl != rank || sn[i] == 0.f) continue;
-        int p, q;
-        rr_pair(r, i, kk, p, q);
-        if (p > q) { const int tt = p; p = q; q = tt; }
-        float x = Bm[(int64_t)j * k + p], y = Bm[(int64_t)j * k + q];
-        Bm[(int64_t)j * k + p] = cs[i] * x - sn[i] * y;
-        Bm[(int64_t)j * k + q] = sn[i] * x + cs[i] * y;
-        x = V[(int64_t)p * k + j];
-        y = V[(int64_t)q * k + j];
-        V[(int64_t)p * k + j] = cs[i] * x - sn[i] * y;
-        V[(int64_t)q * k + j] = sn[i] * x + cs[i] * y;
-      }
-      cl.sync();
-    }
-    // (4) V2 = V1 W into U; eigenvalues = diag(B), sorted in every CTA
-    for (int j = c0 + warp; j < c1; j += nw) {
-      const float* wj = V + (int64_t)j * k;
-      for (int i = lane; i < k; i += 32) {
-        float acc = 0.f;
-        for (int q = 0; q < k; ++q) acc = fmaf(Qb[(int64_t)q * k + i], wj[q], acc);
-        U[(int64_t)j * k + i] = acc;
-      }
-    }
-    for (int p = tid; p < kp2; p += blockDim.x) {
-      lamv[p] = p < k ? Bm[(int64_t)p * k + p] : -INFINITY;
-      perm[p] = p;
-    }
-    cl.sync();
-    // (5) E2 = I - V2^T V2 into Bm (columns c0..c1)
-    for (int q = c0 + warp; q < c1; q += nw) {
-      const float* vq = U + (int64_t)q * k;
-      for (int p = 0; p < k; ++p) {
-        const float* vp = U + (int64_t)p * k;
-        float d = 0.f;
-        for (int i = lane; i < k; i += 32) d = fmaf(vp[i], vq[i], d);
-        d = warp_sum(d);
-        if (lane == 0) Bm[(int64_t)q * k + p] = (p == q ? 1.f : 0.f) - d;
-      }
-    }
-    for (int size = 2; size <= kp2; size <<= 1) {
-      for (int stride = size >> 1; stride > 0; stride >>= 1) {
-        __syncthreads();
-        for (int i = tid; i < kp2; i += blockDim.x) {
-          const int j = i ^ stride;
-          if (j > i) {
-            const bool desc = (i & size) == 0;
-            const float li = lamv[i], lj = lamv[j];
-            if (desc ? (li < lj) : (li > lj)) {
-              lamv[i] = lj;
-              lamv[j] = li;
-              const int pt = perm[i];
-              perm[i] = perm[j];
-              perm[j] = pt;
-            }
-          }
-        }
-      }
-    }
-    cl.sync();
-    // (6) Q columns c0..c1 (row-major)
-    for (int j = c0 + warp; j < c1; j += nw) {
-      int p = perm[j];
-      if (p < 0 || p >= k) p = j;
-      const float* vp = U + (int64_t)p * k;
-      const float* ep = Bm + (int64_t)p * k;
-      for (int i = lane; i < k; i += 32) {
-        float acc = 0.f;
-        for (int q = 0; q < k; ++q) acc = fmaf(U[(int64_t)q * k + i], ep[q], acc);
-        Qb[(int64_t)i * k + j] = fmaf(0.5f, acc, vp[i]);
-      }
-    }
-    if (rank == 0) {
-      for (int j = tid; j < k; j += blockDim.x) a.lam[mi.lam_off + (int64_t)t.blk * k + j] = lamv[j];
-      if (tid == 0) {
-        float* st = a.stats + 4 * (int64_t)(mi.blk0 + t.blk);
-        st[2] = (float)sweep;
-        st[3] = (float)last_rot;
-        if (sweep >= a.max_sweeps && last_rot > 0) atomicOr(flag, (uint32_t)DOBB_FLAG_NOT_CONVERGED);
-      }
-    }
-    cl.sync();
-  }
-}
-
-}  // namespace
-
-size_t jacobi_cluster_smem(int k) {
-  const int g = (k + 2 * kCl - 1) / (2 * kCl);
-  return (size_t)16 * g * k + (size_t)8 * pow2_ceil(k);
-}
-
-bool jacobi_cluster_fits(int k, size_t smem_limit) {
-  const int g = (k + 2 * kCl - 1) / (2 * kCl);
-  return g <= 32 && jacobi_cluster_smem(k) <= smem_limit;
-}
-
-cudaError_t configure_jacobi_cluster(size_t smem_limit) {
-  return cudaFuncSetAttribute(jacobi_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)smem_limit);
-}
-
-int jacobi_cluster_max_active(size_t smem) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(kCl * 64);
-  cfg.blockDim = dim3(kClThreads);
-  cfg.dynamicSmemBytes = smem;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = kCl;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, jacobi_cluster_kernel, &cfg) != cudaSuccess) {
-    cudaGetLastError();
-    return 0;
-  }
-  return n;
-}
-
-cudaError_t launch_jacobi_cluster(const EigArgs& a, int clusters, size_t smem, cudaStream_t s) {
-  if (a.num_tiles <= 0) return cudaSuccess;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(kCl * clusters);
-  cfg.blockDim = dim3(kClThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = kCl;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, jacobi_cluster_kernel, a, clusters);
 }
 
 }  // namespace dobb

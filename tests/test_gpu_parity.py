@@ -113,7 +113,7 @@ def test_refresh_on_accumulated_moments(k, eff):
     ([(37, 96)], 2),            # k = 48, ragged rows
     ([(1, 24), (17, 24)], 3),   # m = 1, k = 8
     ([(130, 200)], 2),          # k = 100
-    ([(20, 400)], 1),           # k = 400
+    ([(200, 400)], 1),          # k = 400
     ([(9, 15)], 5),             # k = 3 (odd)
 ])
 def test_update_matches_oracle_with_gpu_basis(pdt, shapes, B):
