@@ -60,6 +60,9 @@ SIGNATURES = [
     ("dobb_launch_count", _c.c_int64, [_VP]),
     ("dobb_set_step_path", _c.c_int, [_VP, _c.c_int]),
     ("dobb_sync_bases", _c.c_int, [_VP, _VP]),
+    ("dobb_eigh_noalloc", _c.c_int, [_VP, _VP, _VP, _c.c_int, _c.c_int, _c.c_int,
+                                     _c.POINTER(_c.c_uint32), _VP]),
+    ("dobb_eigh_noalloc_last_error", _c.c_char_p, []),
 ]
 
 

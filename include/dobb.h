@@ -182,6 +182,40 @@ dobb_status dobb_set_step_path(dobb_handle h, int path);
  * and dobb_set_state do this themselves. */
 dobb_status dobb_sync_bases(dobb_handle h, void* stream);
 
+/* ------------------------------------------------------------------------
+ * Allocation-free block eigendecomposition.
+ *
+ * The pages have no counterpart of this call; it exists for callers of this
+ * library that cannot call cudaMalloc: code inside a stream-captured region
+ * that must not allocate, runtimes whose device memory is reserved up front
+ * by an arena they do not control, and plugins of frameworks that forbid
+ * allocations outside their own allocator.  It runs the eigensolver of the
+ * refresh (one-sided Jacobi from the identity, then the Newton-Schulz /
+ * two-sided polish) on caller buffers and allocates nothing: its working
+ * memory is a file-scope device array of DOBB_NOALLOC_SCRATCH_FLOATS floats
+ * (16 MiB) plus small fixed work-list arrays, which every GPU that loads the
+ * library holds until the process exits.
+ *
+ *   A_dev    count symmetric k x k fp32 matrices, row-major, back to back (in)
+ *   Q_dev    count k x k fp32 outputs, row-major, column j = eigenvector of
+ *            the j-th largest eigenvalue (out; its contents are overwritten)
+ *   lam_dev  count x k fp32 eigenvalues, descending (out)
+ *   k        1 <= k <= 1024;  count 0 <= count <= 4096 and
+ *            count * 3 * k * k <= DOBB_NOALLOC_SCRATCH_FLOATS, otherwise the
+ *            call returns DOBB_ERR_INVALID_ARG without touching the device
+ *   max_sweeps  sweep cap of the Jacobi iteration (e.g. 40)
+ *   flags_host  optional host array of count uint32 (DOBB_FLAG_* bits); when
+ *               non-NULL the call synchronises `stream` and fills it
+ * Asynchronous on `stream` otherwise.  The first call on a device resolves
+ * the device addresses of the arrays (cudaGetSymbolAddress) and should come
+ * before any stream capture.  All calls share the arrays, which keep the
+ * last call's contents: calls that overlap on the GPU race.  Errors are
+ * reported by dobb_eigh_noalloc_last_error() (thread-local). */
+#define DOBB_NOALLOC_SCRATCH_FLOATS (4u << 20)
+dobb_status dobb_eigh_noalloc(const float* A_dev, float* Q_dev, float* lam_dev, int k, int count,
+                              int max_sweeps, uint32_t* flags_host, void* stream);
+const char* dobb_eigh_noalloc_last_error(void);
+
 #ifdef __cplusplus
 }
 #endif
