@@ -328,13 +328,15 @@ dobb_status do_pack(dobb_handle h, cudaStream_t s) {
 }
 
 dobb_status do_refresh(dobb_handle h, cudaStream_t s) {
-  const int smem_max_k = jacobi_smem_max_k(h->smem_limit);
+  // blocks whose solver fits in half of an SM's shared memory run two CTAs per SM
+  const size_t half = h->smem_per_sm / 2 > 2048 ? h->smem_per_sm / 2 - 2048 : 0;
   for (const Chunk& ch : h->wl.chunks) {
     if (ch.eig_n == 0) continue;
-    // the list is sorted by decreasing k: [U, V in global scratch | in shared memory]
+    // the list is sorted by decreasing k: [one CTA per SM | two or more]
     const Tile* items = h->wl.tiles.data() + ch.eig_off;
+    auto kof = [&](int idx) { return (int)(h->n[items[idx].mat] / h->B); };
     int b = 0;
-    while (b < ch.eig_n && (int)(h->n[items[b].mat] / h->B) > smem_max_k) ++b;
+    while (b < ch.eig_n && jacobi_smem_for(kof(b), half) == 0) ++b;
     EigArgs a{};
     a.info = h->dinfo();
     a.max_sweeps = h->max_sweeps;
@@ -350,15 +352,16 @@ dobb_status do_refresh(dobb_handle h, cudaStream_t s) {
       if (hi <= lo) continue;
       size_t smem = 0;
       for (int idx = lo; idx < hi; ++idx) {
-        const int k = (int)(h->n[items[idx].mat] / h->B);
-        smem = std::max(smem, part == 0 ? jacobi_sort_smem_for(k) : jacobi_smem_for(k));
+        const size_t need = jacobi_smem_for(kof(idx), part == 0 ? h->smem_limit : half);
+        if (need == 0) return fail(DOBB_ERR_UNSUPPORTED, "block width %d exceeds the eigensolver's shared memory", kof(idx));
+        smem = std::max(smem, need);
       }
       a.tiles = h->dtiles() + ch.eig_off + lo;
       a.num_tiles = hi - lo;
       const int by_smem = std::max(1, (int)(h->smem_per_sm / (smem + 1024)));
-      const int per_sm = part == 0 ? 1 : std::min(jacobi_ctas_per_sm(), by_smem);
+      const int per_sm = std::min(jacobi_ctas_per_sm(), by_smem);
       const int g = std::max(1, std::min(a.num_tiles, h->sm_count * per_sm));
-      cudaError_t e = launch_jacobi(a, g, smem, s, part == 0);
+      cudaError_t e = launch_jacobi(a, g, smem, s);
       if (e != cudaSuccess) return fail(DOBB_ERR_CUDA, "eigen launch: %s", cudaGetErrorString(e));
       ++h->launches;
     }

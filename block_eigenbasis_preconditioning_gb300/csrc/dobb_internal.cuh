@@ -92,10 +92,10 @@ struct EigArgs {
   const float* A;
   float* Q;
   float* lam;
-  float* scratch;         // 3 * (floats of the A region): U, V and the polish matrix of each block
+  float* scratch;         // 3 * (floats of the A region): B, V and a work matrix of each block
   uint32_t* flags;
   float* stats;
-  float tol;              // relative orthogonality threshold (0 = default)
+  float tol;              // relative off-diagonal norm of the last sweep's B (0 = default)
 };
 
 struct StepArgs {
@@ -126,8 +126,7 @@ struct CheckArgs {
 
 // Launchers (return cudaGetLastError() of the launch).
 cudaError_t launch_syrk_ema(const AccArgs& a, int act_dtype, int grid, cudaStream_t s);
-cudaError_t launch_jacobi(const EigArgs& a, int grid, size_t smem_bytes, cudaStream_t s,
-                          bool wide);
+cudaError_t launch_jacobi(const EigArgs& a, int grid, size_t smem_bytes, cudaStream_t s);
 cudaError_t launch_step_ffma(const StepArgs& a, int param_dtype, int grid, size_t smem,
                              cudaStream_t s);
 cudaError_t launch_check(const CheckArgs& a, int grid, cudaStream_t s);
@@ -135,9 +134,9 @@ cudaError_t launch_check(const CheckArgs& a, int grid, cudaStream_t s);
 // Kernel resource queries used by the scheduler at create time.
 int step_rows_per_tile();
 int syrk_tile();
-int jacobi_smem_max_k(size_t smem_limit);
-size_t jacobi_smem_for(int k);
-size_t jacobi_sort_smem_for(int k);
+// shared memory of the eigensolver for a block of width k within `budget`
+// bytes (0 when it does not fit)
+size_t jacobi_smem_for(int k, size_t budget);
 int jacobi_ctas_per_sm();
 size_t step_smem_for(int k);
 cudaError_t configure_jacobi(size_t smem_limit);

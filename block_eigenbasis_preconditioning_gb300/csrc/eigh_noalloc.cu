@@ -24,8 +24,8 @@
 namespace dobb {
 namespace {
 
-// fp32 scratch: three k x k matrices per block (rotated columns, basis, and
-// the polish matrix), 16 MiB in total.
+// fp32 scratch: three k x k matrices per block (the rotated moment, the
+// basis and a work matrix), 16 MiB in total.
 constexpr size_t kNoAllocScratchFloats = (size_t)4 << 20;
 constexpr int kNoAllocMaxBlocks = 4096;
 constexpr int kNoAllocMaxK = 1024;
@@ -158,11 +158,13 @@ extern "C" dobb_status dobb_eigh_noalloc(const float* A_dev, float* Q_dev, float
   a.flags = d->flags;
   a.stats = d->stats;
   a.tol = 0.f;
-  const size_t full = jacobi_smem_for(k);
-  const size_t smem = full <= d->smem_limit ? full : jacobi_sort_smem_for(k);
+  const size_t half = d->smem_per_sm / 2 > 2048 ? d->smem_per_sm / 2 - 2048 : 0;
+  size_t smem = jacobi_smem_for(k, half);
+  if (smem == 0) smem = jacobi_smem_for(k, d->smem_limit);
+  if (smem == 0) return noalloc_fail(DOBB_ERR_UNSUPPORTED, "block width exceeds the eigensolver's shared memory");
   const int by_smem = std::max(1, (int)(d->smem_per_sm / (smem + 1024)));
   const int g = std::max(1, std::min(count, d->sm_count * std::min(jacobi_ctas_per_sm(), by_smem)));
-  e = launch_jacobi(a, g, smem, s, full > d->smem_limit);
+  e = launch_jacobi(a, g, smem, s);
   if (e != cudaSuccess) return noalloc_fail(DOBB_ERR_CUDA, "eigensolver launch failed", e);
   if (flags_host) {
     e = cudaMemcpyAsync(flags_host, d->flags, sizeof(uint32_t) * count, cudaMemcpyDeviceToHost, s);

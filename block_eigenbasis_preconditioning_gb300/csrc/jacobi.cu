@@ -2,39 +2,64 @@
 // ("Dobb", Abstract: a complete basis within each block; Table 15: exact
 // eigendecomposition refresh).
 //
-// One-sided (Hestenes) Jacobi with V accumulated: V starts as the current
-// basis Q (the identity before the first refresh) and U as A V; each
-// rotation of a column pair (p, q) makes u_p and u_q orthogonal and applies
-// the same rotation to v_p, v_q, so A V = U is kept.  Pairs are visited in
-// round-robin (circle) order: each round holds k/2 disjoint pairs that the
-// warps of one CTA rotate in parallel; k - 1 rounds form a sweep.  A pair is
-// rotated only when its columns are measurably non-orthogonal both relative
-// to their own norms (|u_p.u_q| > tol |u_p||u_q|) and relative to the block
-// (|u_p.u_q| > tau ||A||_F max(|u_p|, |u_q|), tau = eps / 4): below that the
-// residual the rotation would remove is under fp32 rounding of A, and
-// rotating there only adds rounding noise to V.  Sweeps stop when one sweep
-// rotates nothing, or at the sweep cap.
+// Method: cyclic two-sided Jacobi (Golub & Van Loan's 2x2 symmetric Schur
+// rotation, applied as B <- J^T B J, V <- V J) inside a Rayleigh-Ritz
+// restart loop:
 //
-// Finish (a polish that brings the backward error to the fp32 floor of a
-// Householder-based solver instead of the ~sqrt(rotations) eps that the
-// accumulated rotations leave):
-//   V1 = V + V (I - V^T V) / 2          (Newton-Schulz re-orthogonalisation)
-//   B  = V1^T A V1                      (nearly diagonal)
-//   one two-sided cyclic Jacobi sweep on B (rotations J, Golub & Van Loan's
-//   2x2 symmetric Schur step), accumulating W = J_1 J_2 ...
-//   V2 = V1 W, Q = V2 + V2 (I - V2^T V2) / 2, Lambda = diag(B)
-// then eigenpairs are sorted by descending eigenvalue and written as
-// row-major Q (column j = j-th eigenvector) and Lambda.
+//   V = current basis (the identity before the first refresh)
+//   B = V^T (A V)
+//   repeat
+//     off = ||off(B)||_F / ||B||_F
+//     one sweep on B, rotating V along
+//     stop when B was freshly formed and off <= tol (that sweep was the
+//       last, small correction) or the sweep rotated nothing
+//     while off > 1e-3 keep sweeping the same B (far from diagonal the
+//       rotations are large and a restart buys nothing); otherwise restart:
+//       V <- V + V (I - V^T V) / 2 (Newton-Schulz), B = V^T (A V); a B
+//       that has been swept is never the last one, since its entries carry
+//       the rounding of every rotation so far
+//   Lambda = diag(B), V <- V + V (I - V^T V) / 2, columns sorted by
+//   descending eigenvalue, written as row-major Q (column j = eigenvector j).
 //
-// One CTA per block.  U and V live in shared memory when 8 k^2 bytes fit,
-// otherwise in a global scratch area of the state buffer.
+// The restart is what keeps fp32 results at the level of a Householder
+// solver: every sweep adds rounding to B and to the column norms of V (each
+// column takes ~k rotations per sweep), and recomputing B from A and a
+// re-orthogonalised V removes that before the final, small sweep.  A warm
+// start from the previous basis usually needs two or three restarts.
+//
+// A sweep is blocked so that all O(k^3) work is small dense products.  The
+// k columns form nG = 2 ceil(k / 64) groups of g <= 32; the groups play a
+// round-robin tournament (nG - 1 rounds of nG / 2 tables).  In a round each
+// table (two groups, index set P_t of 2g columns) loads its diagonal tile
+// S_t = B[P_t, P_t] into shared memory and rotates every pair of its columns
+// once (in the first round also the pairs inside each group), accumulating
+// R_t.  The round then updates the rest of B tile pair by tile pair,
+// B[P_s, P_t] <- R_s^T B[P_s, P_t] R_t, and V panel by panel,
+// V[:, P_t] <- V[:, P_t] R_t.  Every column pair is rotated once per sweep.
+// A pair is rotated when |b_pq| exceeds 1e-3 eps ||A||_F.
+//
+// One CTA of 256 threads per block; B, V and a third k x k work matrix live
+// in a global scratch area of the state buffer (L2-resident), staged through
+// shared memory by the products.
+#include <algorithm>
+
 #include "common.cuh"
 
 namespace dobb {
 namespace {
 
-constexpr int kThreads = 512;
+constexpr int kThreads = 256;
 constexpr float kEps = 5.9604645e-8f;  // 2^-24, fp32 unit roundoff
+constexpr float kColdOff = 1e-3f;      // sweep the same B while off(B) is above this
+constexpr float kStopOff = 1e-5f;      // default: the sweep on a B this close to diagonal is the last
+
+constexpr int kT = 64;                 // tile edge of every product
+constexpr int kLd = kT + 4;            // padded row of a staged 64-wide tile
+constexpr int kGK = 32;                // reduction depth of one stage of the k x k product
+constexpr int kGemmFloats = 2 * 2 * kGK * kLd;  // two stages of the X and Y tiles
+constexpr int kApplyFloats = 4 * kT * kLd;      // R_s, R_t, X, Y^T of the tile updates
+constexpr int kMaxTables = kThreads / 32;       // tables solved together, a warp each
+static_assert(kGemmFloats <= kApplyFloats, "product stages live in the tile-update area");
 
 __host__ __device__ __forceinline__ int pow2_ceil(int v) {
   int p = 1;
@@ -43,7 +68,7 @@ __host__ __device__ __forceinline__ int pow2_ceil(int v) {
 }
 
 // Pair i of round r in the circle schedule over kk (even) players.
-__device__ __forceinline__ void rr_pair(int r, int i, int kk, int& p, int& q) {
+__host__ __device__ __forceinline__ void rr_pair(int r, int i, int kk, int& p, int& q) {
   if (i == 0) {
     p = kk - 1;
     q = r;
@@ -53,250 +78,520 @@ __device__ __forceinline__ void rr_pair(int r, int i, int kk, int& p, int& q) {
   }
 }
 
-// E = I - V^T V (symmetric), column q of E at E + q k; one warp per column.
-__device__ __forceinline__ void newton_schulz_cols(const float* V, float* E, int k, int warp, int nw,
-                                                   int lane) {
-  for (int q = warp; q < k; q += nw) {
-    const float* vq = V + (int64_t)q * k;
-    for (int p = 0; p < k; ++p) {
-      const float* vp = V + (int64_t)p * k;
-      float d = 0.f;
-      for (int i = lane; i < k; i += 32) d = fmaf(vp[i], vq[i], d);
-      d = warp_sum(d);
-      if (lane == 0) E[(int64_t)q * k + p] = (p == q ? 1.f : 0.f) - d;
-    }
+// Group geometry of the blocked sweep.
+struct Geo {
+  int nG;  // groups (even)
+  int g;   // columns per group (<= 32)
+  int n2;  // columns per table, 2 g
+  int nT;  // tables per round, nG / 2
+};
+
+__host__ __device__ __forceinline__ Geo geo_for(int k) {
+  Geo o;
+  o.nG = 2 * ((k + kT - 1) / kT);
+  o.g = (k + o.nG - 1) / o.nG;
+  o.n2 = 2 * o.g;
+  o.nT = o.nG / 2;
+  return o;
+}
+
+// eigenvalues and permutation of the sort, rounded to 16 bytes
+__host__ __device__ __forceinline__ int sort_floats(int k) { return (2 * pow2_ceil(k) + 3) & ~3; }
+__host__ __device__ __forceinline__ int fixed_floats(int k) { return sort_floats(k); }
+
+// Tables solved together for a given shared-memory size (floats); 0 when it
+// does not fit.
+__host__ __device__ __forceinline__ int tables_per_chunk(int k, int smem_floats) {
+  const Geo G = geo_for(k);
+  const int per_table = 2 * G.n2 * G.n2;
+  const int avail = smem_floats - fixed_floats(k);
+  if (G.nT == 1) return avail >= kApplyFloats + per_table ? 1 : 0;
+  if (avail < kApplyFloats) return 0;
+  const int tc = avail / per_table;
+  return tc < G.nT ? (tc < kMaxTables ? tc : kMaxTables) : (G.nT < kMaxTables ? G.nT : kMaxTables);
+}
+
+// ---------------------------------------------------------------------------
+// 64 x 64 register-blocked product: acc[i][j] += sum_{c < n} P[c][4ty+i] Q[c][4tx+j]
+// (rows of P and Q at stride ld, 16-byte aligned); 4 x 4 outputs per thread.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void micro_tn(const float* P, const float* Q, int ld, int n,
+                                         float acc[4][4]) {
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  const float* pp = P + 4 * ty;
+  const float* qq = Q + 4 * tx;
+#pragma unroll 4
+  for (int c = 0; c < n; ++c) {
+    const float4 a = *reinterpret_cast<const float4*>(pp + c * ld);
+    const float4 b = *reinterpret_cast<const float4*>(qq + c * ld);
+    const float av[4] = {a.x, a.y, a.z, a.w};
+    const float bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
   }
 }
 
-// One rotation of the column pair (p, q) with the four columns held in
-// registers (k <= 32 kRegCols): all loads are issued at once, the dot products
-// and the rotation use the registers, results are stored once.  Same
-// arithmetic, in the same order, as the streaming loop.
-template <int kRegCols>
-__device__ __forceinline__ void rotate_pair_regs(float* up, float* uq, float* vp, float* vq, int k,
-                                                 int lane, float tol, float tau, int& rots) {
-  float xu[kRegCols], yu[kRegCols], xv[kRegCols], yv[kRegCols];
+__device__ __forceinline__ void zero_acc(float acc[4][4]) {
 #pragma unroll
-  for (int e = 0; e < kRegCols; ++e) {
-    const int i = lane + 32 * e;
-    const bool ok = i < k;
-    xu[e] = ok ? up[i] : 0.f;
-    yu[e] = ok ? uq[i] : 0.f;
-    xv[e] = ok ? vp[i] : 0.f;
-    yv[e] = ok ? vq[i] : 0.f;
-  }
-  float al = 0.f, be = 0.f, ga = 0.f;
+  for (int i = 0; i < 4; ++i)
 #pragma unroll
-  for (int e = 0; e < kRegCols; ++e) {
-    al = fmaf(xu[e], xu[e], al);
-    be = fmaf(yu[e], yu[e], be);
-    ga = fmaf(xu[e], yu[e], ga);
-  }
-  al = warp_sum(al);
-  be = warp_sum(be);
-  ga = warp_sum(ga);
-  if (fabsf(ga) > tol * sqrtf(al) * sqrtf(be) && fabsf(ga) > tau * sqrtf(fmaxf(al, be))) {
-    const float zeta = (be - al) / (2.f * ga);
-    const float tt = copysignf(1.f, zeta) / (fabsf(zeta) + sqrtf(1.f + zeta * zeta));
-    const float c = 1.f / sqrtf(1.f + tt * tt);
-    const float sn = c * tt;
-#pragma unroll
-    for (int e = 0; e < kRegCols; ++e) {
-      const int i = lane + 32 * e;
-      if (i < k) {
-        up[i] = c * xu[e] - sn * yu[e];
-        uq[i] = sn * xu[e] + c * yu[e];
-        vp[i] = c * xv[e] - sn * yv[e];
-        vq[i] = sn * xv[e] + c * yv[e];
-      }
-    }
-    ++rots;
-  }
+    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
 }
 
-// Shared-memory tiled product over the k x k operands of one block, FP32:
+// out[4ty+i][4tx+j] = acc[i][j] (rows of stride ld)
+__device__ __forceinline__ void store_acc(float* out, int ld, const float acc[4][4]) {
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    *reinterpret_cast<float4*>(out + (4 * ty + i) * ld + 4 * tx) =
+        make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+}
+
+// out[4tx+j][4ty+i] = acc[i][j]
+__device__ __forceinline__ void store_acc_t(float* out, int ld, const float acc[4][4]) {
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    *reinterpret_cast<float4*>(out + (4 * tx + j) * ld + 4 * ty) =
+        make_float4(acc[0][j], acc[1][j], acc[2][j], acc[3][j]);
+}
+
+// ---------------------------------------------------------------------------
+// Product over the k x k operands of one block, FP32:
 //   C(i, j) = alpha * sum_l X(i, l) Y(l, j) + D(i, j) + (eye ? delta_ij : 0)
 // with Y(l, j) = Y[j k + l], X(i, l) = X[l k + i] (XT = false) or X[i k + l]
-// (XT = true); C(i, j) and D(i, j) are stored at [j k + i].  64 x 64 output
-// tiles, 32-deep reduction chunks, the CTA's 512 threads own 2 x 4 outputs.
-constexpr int kGT = 64, kGK = 32, kGP = kGT + 4;
-constexpr size_t kGemmSmemFloats = 2 * kGK * kGP;
-
+// (XT = true); C and D at [j k + i].  sym: the result is symmetric by
+// construction, so only tiles on or above the diagonal are computed and each
+// value is written to both (i, j) and (j, i) (on diagonal tiles the i <= j
+// triangle is kept, so C is exactly symmetric).  64 x 64 output tiles; the
+// reduction is staged 32 deep through shared memory, the next stage loaded
+// into registers while the current one is multiplied.
+// ---------------------------------------------------------------------------
 template <bool XT>
 __device__ void block_gemm(const float* X, const float* Y, float* C, const float* D, float alpha,
-                           bool eye, int k, float* gs) {
-  float* Xs = gs;
-  float* Ys = gs + kGK * kGP;
-  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;  // ty < 32 for 512 threads
-  const int nt = (k + kGT - 1) / kGT;
+                           bool eye, bool sym, int k, float* gs) {
+  float* xs[2] = {gs, gs + 2 * kGK * kLd};
+  float* ys[2] = {gs + kGK * kLd, gs + 3 * kGK * kLd};
+  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+  const int nt = (k + kT - 1) / kT;
+  const int nch = (k + kGK - 1) / kGK;
+  constexpr int kPer = kGK * kT / kThreads;  // elements of each operand per thread and stage
   for (int tile = 0; tile < nt * nt; ++tile) {
-    const int i0 = (tile % nt) * kGT, j0 = (tile / nt) * kGT;
-    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-    for (int l0 = 0; l0 < k; l0 += kGK) {
-      for (int e = tid; e < kGK * kGT; e += blockDim.x) {
-        // X tile: rows i0.., reduction l0..; coalesced along the contiguous index
+    const int ti = tile % nt, tj = tile / nt;
+    if (sym && ti > tj) continue;
+    const int i0 = ti * kT, j0 = tj * kT;
+    float acc[4][4];
+    zero_acc(acc);
+    float rx[kPer], ry[kPer];
+    auto gload = [&](int l0) {
+#pragma unroll
+      for (int r = 0; r < kPer; ++r) {
+        const int e = tid + r * kThreads;
         int l, i;
-        if (XT) { l = e % kGK; i = e / kGK; } else { i = e % kGT; l = e / kGT; }
+        if (XT) {
+          l = e % kGK;
+          i = e / kGK;
+        } else {
+          i = e % kT;
+          l = e / kT;
+        }
         float xv = 0.f;
-        if (i0 + i < k && l0 + l < k)
-          xv = XT ? X[(int64_t)(i0 + i) * k + l0 + l] : X[(int64_t)(l0 + l) * k + i0 + i];
-        Xs[l * kGP + i] = xv;
+        if (i0 + i < k && l0 + l < k) xv = XT ? X[(i0 + i) * k + l0 + l] : X[(l0 + l) * k + i0 + i];
+        rx[r] = xv;
         const int ly = e % kGK, j = e / kGK;
-        float yv = 0.f;
-        if (j0 + j < k && l0 + ly < k) yv = Y[(int64_t)(j0 + j) * k + l0 + ly];
-        Ys[ly * kGP + j] = yv;
+        ry[r] = (j0 + j < k && l0 + ly < k) ? Y[(j0 + j) * k + l0 + ly] : 0.f;
       }
+    };
+    auto sstore = [&](float* xd, float* yd) {
+#pragma unroll
+      for (int r = 0; r < kPer; ++r) {
+        const int e = tid + r * kThreads;
+        int l, i;
+        if (XT) {
+          l = e % kGK;
+          i = e / kGK;
+        } else {
+          i = e % kT;
+          l = e / kT;
+        }
+        xd[l * kLd + i] = rx[r];
+        const int ly = e % kGK, j = e / kGK;
+        yd[ly * kLd + j] = ry[r];
+      }
+    };
+    gload(0);
+    sstore(xs[0], ys[0]);
+    __syncthreads();
+    for (int c = 0; c < nch; ++c) {
+      if (c + 1 < nch) gload((c + 1) * kGK);
+      micro_tn(xs[c & 1], ys[c & 1], kLd, min(kGK, k - c * kGK), acc);
+      if (c + 1 < nch) sstore(xs[(c + 1) & 1], ys[(c + 1) & 1]);
       __syncthreads();
-#pragma unroll 8
-      for (int l = 0; l < kGK; ++l) {
-        const float a0 = Xs[l * kGP + ty * 2], a1 = Xs[l * kGP + ty * 2 + 1];
-        float b[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) b[q] = Ys[l * kGP + tx * 4 + q];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          acc[0][q] = fmaf(a0, b[q], acc[0][q]);
-          acc[1][q] = fmaf(a1, b[q], acc[1][q]);
-        }
-      }
-      __syncthreads();
     }
 #pragma unroll
-    for (int p = 0; p < 2; ++p) {
+    for (int i = 0; i < 4; ++i) {
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int i = i0 + ty * 2 + p, j = j0 + tx * 4 + q;
-        if (i < k && j < k) {
-          float v = alpha * acc[p][q];
-          if (D) v += D[(int64_t)j * k + i];
-          if (eye && i == j) v += 1.f;
-          C[(int64_t)j * k + i] = v;
-        }
-      }
-    }
-  }
-  __syncthreads();
-}
-
-__host__ __device__ __forceinline__ size_t smem_bytes_for(int k) {
-  return (size_t)8 * k * k + (size_t)8 * pow2_ceil(k);
-}
-
-// Polish of a block whose U, V live in global scratch, with the tiled
-// products above (same steps as the in-shared-memory polish of the kernel):
-// E = I - V^T V; V1 = V + V E / 2; T = A V1; B = sym(V1^T T); one two-sided
-// Jacobi sweep on B accumulating W; V2 = V1 W; E2 = I - V2^T V2;
-// Q = (V2 + V2 E2 / 2) with columns sorted by descending diag(B).
-__device__ void polish_global(const float* Ab, float* U, float* V, float* Bm, float* Qb,
-                              float* lamv, int* perm, int k, int kp2, float fro2, float* gs) {
-  const int tid = threadIdx.x;
-  block_gemm<true>(V, V, Bm, nullptr, -1.f, true, k, gs);        // E
-  block_gemm<false>(V, Bm, U, V, 0.5f, false, k, gs);            // V1 (in U)
-  block_gemm<false>(Ab, U, V, nullptr, 1.f, false, k, gs);       // T = A V1 (A symmetric)
-  block_gemm<true>(U, V, Bm, nullptr, 1.f, false, k, gs);        // B = V1^T T
-  for (int64_t e = tid; e < (int64_t)k * k; e += blockDim.x) {
-    const int i = (int)(e % k), j = (int)(e / k);
-    if (i < j) {
-      const float v = 0.5f * (Bm[(int64_t)j * k + i] + Bm[(int64_t)i * k + j]);
-      Bm[(int64_t)j * k + i] = v;
-      Bm[(int64_t)i * k + j] = v;
-    }
-  }
-  for (int64_t e = tid; e < (int64_t)k * k; e += blockDim.x) V[e] = ((e / k) == (e % k)) ? 1.f : 0.f;
-  __syncthreads();
-  const int kk = k + (k & 1);
-  float* cs = lamv;
-  float* sn = lamv + (kp2 >> 1);
-  const float bfloor = 1e-3f * kEps * sqrtf(fro2);
-  for (int r = 0; r < kk - 1; ++r) {
-    for (int i = tid; i < kk / 2; i += blockDim.x) {
-      int p, q;
-      rr_pair(r, i, kk, p, q);
-      float c = 1.f, sv = 0.f;
-      if (p < k && q < k) {
-        if (p > q) { const int tt = p; p = q; q = tt; }
-        const float bpq = Bm[(int64_t)p * k + q];
-        if (fabsf(bpq) > bfloor) {
-          const float ta = (Bm[(int64_t)q * k + q] - Bm[(int64_t)p * k + p]) / (2.f * bpq);
-          const float tt = ta >= 0.f ? 1.f / (ta + sqrtf(1.f + ta * ta)) : -1.f / (-ta + sqrtf(1.f + ta * ta));
-          c = 1.f / sqrtf(1.f + tt * tt);
-          sv = tt * c;
-        }
-      }
-      cs[i] = c;
-      sn[i] = sv;
-    }
-    __syncthreads();
-    for (int64_t e = tid; e < (int64_t)(kk / 2) * k; e += blockDim.x) {
-      const int i = (int)(e / k), j = (int)(e % k);
-      if (sn[i] == 0.f) continue;
-      int p, q;
-      rr_pair(r, i, kk, p, q);
-      if (p > q) { const int tt = p; p = q; q = tt; }
-      const float x = Bm[(int64_t)p * k + j], y = Bm[(int64_t)q * k + j];
-      Bm[(int64_t)p * k + j] = cs[i] * x - sn[i] * y;
-      Bm[(int64_t)q * k + j] = sn[i] * x + cs[i] * y;
-    }
-    __syncthreads();
-    for (int64_t e = tid; e < (int64_t)(kk / 2) * k; e += blockDim.x) {
-      const int i = (int)(e / k), j = (int)(e % k);
-      if (sn[i] == 0.f) continue;
-      int p, q;
-      rr_pair(r, i, kk, p, q);
-      if (p > q) { const int tt = p; p = q; q = tt; }
-      float x = Bm[(int64_t)j * k + p], y = Bm[(int64_t)j * k + q];
-      Bm[(int64_t)j * k + p] = cs[i] * x - sn[i] * y;
-      Bm[(int64_t)j * k + q] = sn[i] * x + cs[i] * y;
-      x = V[(int64_t)p * k + j];
-      y = V[(int64_t)q * k + j];
-      V[(int64_t)p * k + j] = cs[i] * x - sn[i] * y;
-      V[(int64_t)q * k + j] = sn[i] * x + cs[i] * y;
-    }
-    __syncthreads();
-  }
-  block_gemm<false>(U, V, Qb, nullptr, 1.f, false, k, gs);       // V2 = V1 W (in Qb)
-  for (int p = tid; p < kp2; p += blockDim.x) {
-    lamv[p] = p < k ? Bm[(int64_t)p * k + p] : -INFINITY;
-    perm[p] = p;
-  }
-  __syncthreads();
-  block_gemm<true>(Qb, Qb, Bm, nullptr, -1.f, true, k, gs);      // E2
-  block_gemm<false>(Qb, Bm, U, Qb, 0.5f, false, k, gs);          // R = V2 + V2 E2 / 2 (in U)
-  for (int size = 2; size <= kp2; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int i = tid; i < kp2; i += blockDim.x) {
-        const int j = i ^ stride;
-        if (j > i) {
-          const bool desc = (i & size) == 0;
-          const float li = lamv[i], lj = lamv[j];
-          if (desc ? (li < lj) : (li > lj)) {
-            lamv[i] = lj;
-            lamv[j] = li;
-            const int pt = perm[i];
-            perm[i] = perm[j];
-            perm[j] = pt;
+      for (int j = 0; j < 4; ++j) {
+        const int gi = i0 + 4 * ty + i, gj = j0 + 4 * tx + j;
+        if (gi < k && gj < k) {
+          float v = alpha * acc[i][j];
+          if (D) v += D[gj * k + gi];
+          if (eye && gi == gj) v += 1.f;
+          if (!sym) {
+            C[gj * k + gi] = v;
+          } else if (ti < tj || gi <= gj) {
+            C[gj * k + gi] = v;
+            C[gi * k + gj] = v;
           }
         }
       }
-      __syncthreads();
     }
-  }
-  for (int64_t e = tid; e < (int64_t)k * k; e += blockDim.x) {
-    const int j = (int)(e / k), i = (int)(e % k);
-    int p = perm[j];
-    if (p < 0 || p >= k) p = j;  // only reachable with a NaN eigenvalue
-    Qb[(int64_t)i * k + j] = U[(int64_t)p * k + i];
   }
   __syncthreads();
 }
 
-template <int kRegCols>
-__global__ void __launch_bounds__(kThreads)
+// T = A V, B = V^T T (A symmetric; V, T column-major; B symmetric)
+__device__ void rayleigh_ritz(const float* A, const float* V, float* T, float* B, int k, float* gs) {
+  block_gemm<false>(A, V, T, nullptr, 1.f, false, false, k, gs);
+  block_gemm<true>(V, T, B, nullptr, 1.f, false, true, k, gs);
+}
+
+// Vout = V + V (I - V^T V) / 2, with E = I - V^T V in Ebuf
+__device__ void newton_schulz(const float* V, float* Vout, float* Ebuf, int k, float* gs) {
+  block_gemm<true>(V, V, Ebuf, nullptr, -1.f, true, true, k, gs);
+  block_gemm<false>(V, Ebuf, Vout, V, 0.5f, false, false, k, gs);
+}
+
+// ||off(B)||_F / ||B||_F, the off-diagonal part summed directly (a
+// difference of the two squares would cancel).
+__device__ float off_rel(const float* B, int k, float* red) {
+  float tot = 0.f, off = 0.f;
+  for (int e = threadIdx.x; e < k * k; e += blockDim.x) {
+    const float v = B[e];
+    tot = fmaf(v, v, tot);
+    const int i = e / k;
+    if (e - i * k != i) off = fmaf(v, v, off);
+  }
+  tot = block_sum(tot, red);
+  off = block_sum(off, red);
+  return tot > 0.f ? sqrtf(off / tot) : 0.f;
+}
+
+// Column of B for local index a of the table made of groups gI, gJ (k when
+// the index lies past the last column).
+__device__ __forceinline__ int table_col(int a, int gI, int gJ, int g, int k) {
+  const int c = a < g ? gI * g + a : gJ * g + (a - g);
+  return c < k ? c : k;
+}
+
+// Local pair (p < q) number i of an inner round; false when the pair has an
+// index past the group (odd g) or past the last column.
+__device__ __forceinline__ bool inner_pair(bool intra, int r, int i, int g, int gI, int gJ, int k,
+                                           int& p, int& q) {
+  if (intra) {
+    const int gp = g + (g & 1), half = gp >> 1;
+    const int grp = i / half, ii = i - grp * half;
+    rr_pair(r, ii, gp, p, q);
+    if (p >= g || q >= g) return false;
+    p += grp * g;
+    q += grp * g;
+  } else {
+    p = i;
+    q = g + (i + r) % g;
+  }
+  if (p > q) {
+    const int tt = p;
+    p = q;
+    q = tt;
+  }
+  return table_col(p, gI, gJ, g, k) < k && table_col(q, gI, gJ, g, k) < k;
+}
+
+// Rotations of one table's diagonal tile by one warp: each inner round
+// rotates a set of disjoint column pairs of S (n2 x n2, row-major, shared
+// memory), S <- J^T S J, and accumulates R <- R J.  Lane i owns pair i of
+// the round (at most 32 pairs), so the pair's indices and rotation stay in
+// registers and are broadcast by shuffles for the row updates.  The pairs
+// are disjoint, so each lane loads four pairs' rows (row update) or four rows
+// (column update) before storing any, which keeps several shared-memory
+// loads in flight.  Returns the lane's count of rotations.
+__device__ int solve_table(float* S, float* R, int br, int t, const Geo& G, int k, float bfloor) {
+  const int lane = threadIdx.x & 31;
+  const int n2 = G.n2;
+  int gI, gJ;
+  rr_pair(br, t, G.nG, gI, gJ);
+  const int gp = G.g + (G.g & 1);
+  const int n_intra = br == 0 ? gp - 1 : 0;
+  int rots = 0;
+  for (int step = 0; step < n_intra + G.g; ++step) {
+    const bool intra = step < n_intra;
+    const int r = intra ? step : step - n_intra;
+    const int npairs = intra ? gp : G.g;
+    int p = 0, q = 0;
+    float c = 1.f, s = 0.f;
+    if (lane < npairs && inner_pair(intra, r, lane, G.g, gI, gJ, k, p, q)) {
+      const float bpq = S[p * n2 + q];
+      if (fabsf(bpq) > bfloor) {
+        const float ta = (S[q * n2 + q] - S[p * n2 + p]) / (2.f * bpq);
+        const float tn = ta >= 0.f ? 1.f / (ta + sqrtf(1.f + ta * ta)) : -1.f / (-ta + sqrtf(1.f + ta * ta));
+        c = 1.f / sqrtf(1.f + tn * tn);
+        s = tn * c;
+        ++rots;
+      }
+    }
+    __syncwarp();
+    // rows p, q of S, lanes along the row (n2 <= 64: two elements per lane)
+    for (int i0 = 0; i0 < npairs; i0 += 4) {
+      float cu[4], su[4], x[4][2], y[4][2];
+      int pu[4], qu[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int src = (i0 + u) & 31;
+        cu[u] = __shfl_sync(0xffffffffu, c, src);
+        su[u] = __shfl_sync(0xffffffffu, s, src);
+        pu[u] = __shfl_sync(0xffffffffu, p, src);
+        qu[u] = __shfl_sync(0xffffffffu, q, src);
+        if (i0 + u >= npairs) su[u] = 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int j = lane + 32 * h;
+          const bool ok = su[u] != 0.f && j < n2;
+          x[u][h] = ok ? S[pu[u] * n2 + j] : 0.f;
+          y[u][h] = ok ? S[qu[u] * n2 + j] : 0.f;
+        }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int j = lane + 32 * h;
+          if (su[u] != 0.f && j < n2) {
+            S[pu[u] * n2 + j] = cu[u] * x[u][h] - su[u] * y[u][h];
+            S[qu[u] * n2 + j] = su[u] * x[u][h] + cu[u] * y[u][h];
+          }
+        }
+    }
+    __syncwarp();
+    // columns p, q of S and R, lane i on pair i, four rows at a time
+    if (s != 0.f) {
+      for (int j0 = 0; j0 < n2; j0 += 4) {
+        float a[4], b[4], ra[4], rb[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int j = j0 + u < n2 ? j0 + u : n2 - 1;
+          a[u] = S[j * n2 + p];
+          b[u] = S[j * n2 + q];
+          ra[u] = R[j * n2 + p];
+          rb[u] = R[j * n2 + q];
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int j = j0 + u;
+          if (j < n2) {
+            S[j * n2 + p] = c * a[u] - s * b[u];
+            S[j * n2 + q] = s * a[u] + c * b[u];
+            R[j * n2 + p] = c * ra[u] - s * rb[u];
+            R[j * n2 + q] = s * ra[u] + c * rb[u];
+          }
+        }
+      }
+    }
+    __syncwarp();
+  }
+  return rots;
+}
+
+// Load an n2 x n2 rotation (row stride n2) into a zero-padded 64 x kLd tile.
+__device__ __forceinline__ void load_rot(float* dst, const float* src, int n2) {
+  for (int e = threadIdx.x; e < kT * kT; e += blockDim.x) {
+    const int a = e / kT, b = e - a * kT;
+    dst[a * kLd + b] = (a < n2 && b < n2) ? src[a * n2 + b] : 0.f;
+  }
+}
+
+constexpr int kPre = kT * kT / kThreads;  // elements of a 64 x 64 tile per thread
+
+// One blocked sweep on B (row-major = column-major, symmetric) rotating the
+// columns of V (column-major).  Rbuf: nT n2^2 floats of global scratch for the
+// tables' rotations (unused when there is a single table).  Returns the
+// number of rotations (the same value in every thread).
+__device__ int blocked_sweep(float* B, float* V, float* Rbuf, int k, const Geo& G, int tc,
+                             float bfloor, float* work, int* s_cnt) {
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int n2 = G.n2, nn = n2 * n2;
+  float* Rs = work;
+  float* Rt = work + kT * kLd;
+  float* Xt = work + 2 * kT * kLd;
+  float* Yt = work + 3 * kT * kLd;
+  // tables' S and R (2 nn floats per table): after the tile buffers when a
+  // single table keeps R in shared memory, else over them
+  float* solve = G.nT == 1 ? work + kApplyFloats : work;
+  const int nI = (k + kT - 1) / kT;
+  int rots = 0;
+  for (int br = 0; br < G.nG - 1; ++br) {
+    // ---- diagonal tiles of the round's tables, tc at a time, a warp per table
+    for (int t0 = 0; t0 < G.nT; t0 += tc) {
+      const int tcn = min(tc, G.nT - t0);
+      for (int e = tid; e < tcn * nn; e += blockDim.x) {
+        const int tt = e / nn, rem = e - tt * nn;
+        const int a = rem / n2, b = rem - a * n2;
+        int gI, gJ;
+        rr_pair(br, t0 + tt, G.nG, gI, gJ);
+        const int ca = table_col(a, gI, gJ, G.g, k), cb = table_col(b, gI, gJ, G.g, k);
+        solve[tt * 2 * nn + rem] = (ca < k && cb < k) ? B[ca * k + cb] : 0.f;
+        solve[tt * 2 * nn + nn + rem] = a == b ? 1.f : 0.f;
+      }
+      __syncthreads();
+      if (warp < tcn)
+        rots += solve_table(solve + warp * 2 * nn, solve + warp * 2 * nn + nn, br, t0 + warp, G, k, bfloor);
+      __syncthreads();
+      for (int e = tid; e < tcn * nn; e += blockDim.x) {
+        const int tt = e / nn, rem = e - tt * nn;
+        const int a = rem / n2, b = rem - a * n2;
+        int gI, gJ;
+        rr_pair(br, t0 + tt, G.nG, gI, gJ);
+        const int ca = table_col(a, gI, gJ, G.g, k), cb = table_col(b, gI, gJ, G.g, k);
+        if (ca < k && cb < k) B[ca * k + cb] = solve[tt * 2 * nn + rem];
+        if (G.nT > 1) Rbuf[(t0 + tt) * nn + rem] = solve[tt * 2 * nn + nn + rem];
+      }
+      __syncthreads();
+    }
+    // ---- off-diagonal tile pairs (s < t): B[P_s, P_t] <- R_s^T B[P_s, P_t] R_t
+    // and its transpose; the next pair's tile and R_t are fetched into
+    // registers while the current pair is multiplied
+    const int npair = G.nT * (G.nT - 1) / 2;
+    if (npair > 0) {
+      float preX[kPre], preR[kPre];
+      auto fetch_pair = [&](int s, int t) {
+        int sI, sJ, tI, tJ;
+        rr_pair(br, s, G.nG, sI, sJ);
+        rr_pair(br, t, G.nG, tI, tJ);
+#pragma unroll
+        for (int r = 0; r < kPre; ++r) {
+          const int e = tid + r * kThreads;
+          const int a = e / kT, b = e - a * kT;
+          const int ca = a < n2 ? table_col(a, sI, sJ, G.g, k) : k;
+          const int cb = b < n2 ? table_col(b, tI, tJ, G.g, k) : k;
+          preX[r] = (ca < k && cb < k) ? B[ca * k + cb] : 0.f;
+          preR[r] = (a < n2 && b < n2) ? Rbuf[t * nn + a * n2 + b] : 0.f;
+        }
+      };
+      int s = 0, t = 1, cur_s = -1;
+      fetch_pair(0, 1);
+      for (int idx = 0; idx < npair; ++idx) {
+        if (s != cur_s) {
+          load_rot(Rs, Rbuf + s * nn, n2);
+          cur_s = s;
+        }
+#pragma unroll
+        for (int r = 0; r < kPre; ++r) {
+          const int e = tid + r * kThreads;
+          const int a = e / kT, b = e - a * kT;
+          Xt[a * kLd + b] = preX[r];
+          Rt[a * kLd + b] = preR[r];
+        }
+        __syncthreads();
+        int sn = s, tn = t + 1;
+        if (tn == G.nT) {
+          ++sn;
+          tn = sn + 1;
+        }
+        if (idx + 1 < npair) fetch_pair(sn, tn);
+        float acc[4][4];
+        zero_acc(acc);
+        micro_tn(Rs, Xt, kLd, n2, acc);  // Y = R_s^T X
+        store_acc_t(Yt, kLd, acc);       // Y^T
+        __syncthreads();
+        zero_acc(acc);
+        micro_tn(Yt, Rt, kLd, n2, acc);  // Z = Y R_t
+        __syncthreads();
+        store_acc(Xt, kLd, acc);         // Z
+        store_acc_t(Yt, kLd, acc);       // Z^T
+        __syncthreads();
+        int sI, sJ, tI, tJ;
+        rr_pair(br, s, G.nG, sI, sJ);
+        rr_pair(br, t, G.nG, tI, tJ);
+        for (int e = tid; e < n2 * n2; e += blockDim.x) {
+          const int a = e / n2, b = e - a * n2;
+          const int ca = table_col(a, sI, sJ, G.g, k), cb = table_col(b, tI, tJ, G.g, k);
+          if (ca < k && cb < k) B[ca * k + cb] = Xt[a * kLd + b];
+          // transposed copy, consecutive threads along a row of B
+          const int ct = table_col(a, tI, tJ, G.g, k), cs = table_col(b, sI, sJ, G.g, k);
+          if (ct < k && cs < k) B[ct * k + cs] = Yt[a * kLd + b];
+        }
+        __syncthreads();
+        s = sn;
+        t = tn;
+      }
+    }
+    // ---- panels of V: V[i0:i0+64, P_t] <- V[i0:i0+64, P_t] R_t, the next
+    // panel fetched into registers while the current one is multiplied
+    {
+      float pre[kPre];
+      auto fetch_panel = [&](int task) {
+        const int t = task / nI, i0 = (task - t * nI) * kT;
+        int tI, tJ;
+        rr_pair(br, t, G.nG, tI, tJ);
+#pragma unroll
+        for (int r = 0; r < kPre; ++r) {
+          const int e = tid + r * kThreads;
+          const int a = e / kT, i = e - a * kT;
+          const int ca = a < n2 ? table_col(a, tI, tJ, G.g, k) : k;
+          pre[r] = (ca < k && i0 + i < k) ? V[ca * k + i0 + i] : 0.f;
+        }
+      };
+      const int ntask = G.nT * nI;
+      int cur_t = -1;
+      fetch_panel(0);
+      for (int task = 0; task < ntask; ++task) {
+        const int t = task / nI, i0 = (task - t * nI) * kT;
+        if (t != cur_t) {
+          load_rot(Rt, G.nT > 1 ? Rbuf + t * nn : solve + nn, n2);
+          cur_t = t;
+        }
+#pragma unroll
+        for (int r = 0; r < kPre; ++r) {
+          const int e = tid + r * kThreads;
+          const int a = e / kT, i = e - a * kT;
+          Xt[a * kLd + i] = pre[r];
+        }
+        __syncthreads();
+        if (task + 1 < ntask) fetch_panel(task + 1);
+        float acc[4][4];
+        zero_acc(acc);
+        micro_tn(Xt, Rt, kLd, n2, acc);  // rows i of V times R_t
+        store_acc_t(Yt, kLd, acc);
+        __syncthreads();
+        int tI, tJ;
+        rr_pair(br, t, G.nG, tI, tJ);
+        for (int e = tid; e < n2 * kT; e += blockDim.x) {
+          const int b = e / kT, i = e - b * kT;
+          const int cb = table_col(b, tI, tJ, G.g, k);
+          if (cb < k && i0 + i < k) V[cb * k + i0 + i] = Yt[b * kLd + i];
+        }
+        __syncthreads();
+      }
+    }
+  }
+  if (tid == 0) *s_cnt = 0;
+  __syncthreads();
+  if (rots) atomicAdd(s_cnt, rots);
+  __syncthreads();
+  const int total = *s_cnt;
+  __syncthreads();
+  return total;
+}
+
+__global__ void __launch_bounds__(kThreads, 2)
 jacobi_kernel(const __grid_constant__ EigArgs a, int smem_floats) {
   extern __shared__ __align__(16) float sm[];
   __shared__ float red[32];
-  __shared__ int s_rot;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
+  __shared__ int s_cnt;
+  const int tid = threadIdx.x;
   for (int w = blockIdx.x; w < a.num_tiles; w += gridDim.x) {
     const Tile t = a.tiles[w];
     const MatInfo mi = a.info[t.mat];
@@ -305,236 +600,75 @@ jacobi_kernel(const __grid_constant__ EigArgs a, int smem_floats) {
     const int64_t kk2 = (int64_t)k * k;
     const int64_t boff = mi.a_off + (int64_t)t.blk * kk2;
     const float* Ab = a.A + boff;
+    float* Qb = a.Q + boff;
     uint32_t* flag = a.flags + mi.blk0 + t.blk;
-    const bool in_smem = smem_bytes_for(k) <= (size_t)smem_floats * 4;
-    float* U;
-    float* V;
-    float* lamv;
-    float* Bm = a.scratch + 3 * boff + 2 * kk2;  // polish matrix, global
-    if (in_smem) {
-      U = sm;
-      V = sm + kk2;
-      lamv = sm + 2 * kk2;
-    } else {
-      U = a.scratch + 3 * boff;
-      V = U + kk2;
-      lamv = sm;
+    const Geo G = geo_for(k);
+    const int tc = tables_per_chunk(k, smem_floats);
+    if (tc < 1) {  // launch configured with too little shared memory for this k
+      if (tid == 0) atomicOr(flag, (uint32_t)DOBB_FLAG_NOT_CONVERGED);
+      continue;
     }
-    int* perm = reinterpret_cast<int*>(lamv + kp2);
+    float* lamv = sm;
+    int* perm = reinterpret_cast<int*>(sm + kp2);
+    float* work = sm + sort_floats(k);
+    float* Bm = a.scratch + 3 * boff;
+    float* V = Bm + kk2;
+    float* T = V + kk2;
 
-    // Warm start from the current basis: V = Q (column j of V is column j of
-    // the row-major Q), U = A V.  With Q = I (no refresh yet) this is the
-    // plain start U = A, V = I.  ||A||_F^2 and a finiteness check on the way.
+    // V = current basis (column j of V = column j of the row-major Q); the
+    // finiteness of A and ||A||_F^2 on the way
     float ss = 0.f;
     int bad = 0;
-    const float* Qold = a.Q + boff;
-    for (int64_t e = tid; e < kk2; e += blockDim.x) {
+    for (int e = tid; e < k * k; e += blockDim.x) {
       const float v = Ab[e];
       bad |= !isfinite(v);
       ss = fmaf(v, v, ss);
-      const int j = (int)(e / k), l = (int)(e % k);
-      V[e] = Qold[(int64_t)l * k + j];
+      const int c = e / k, i = e - c * k;
+      V[e] = Qb[i * k + c];
     }
     if (__syncthreads_or(bad)) {
       if (tid == 0) atomicOr(flag, (uint32_t)DOBB_FLAG_NONFINITE_A);
       continue;  // keep the previous basis
     }
     const float fro2 = block_sum(ss, red);
-    for (int p = warp; p < k; p += nw) {
-      const float* vp = V + (int64_t)p * k;
-      for (int i = lane; i < k; i += 32) {
-        float acc = 0.f;
-        for (int l = 0; l < k; ++l) acc = fmaf(Ab[(int64_t)l * k + i], vp[l], acc);  // A symmetric
-        U[(int64_t)p * k + i] = acc;
-      }
-    }
-    __syncthreads();
-    const float tol = a.tol > 0.f ? a.tol : 4.f * sqrtf((float)k) * kEps;
-    const float tau = 0.25f * kEps * sqrtf(fro2);
-    const int kk = k + (k & 1);
-    int sweep = 0, last_rot = 0;
-    for (; sweep < a.max_sweeps; ++sweep) {
-      if (tid == 0) s_rot = 0;
-      __syncthreads();
-      int my_rot = 0;
-      for (int r = 0; r < kk - 1; ++r) {
-        for (int pi = warp; pi < kk / 2; pi += nw) {
-          int p, q;
-          rr_pair(r, pi, kk, p, q);
-          if (p >= k || q >= k) continue;
-          float* up = U + (int64_t)p * k;
-          float* uq = U + (int64_t)q * k;
-          if (kRegCols > 0 && k <= 32 * kRegCols) {
-            rotate_pair_regs<(kRegCols > 0 ? kRegCols : 1)>(up, uq, V + (int64_t)p * k,
-                                                            V + (int64_t)q * k, k, lane, tol, tau,
-                                                            my_rot);
-            continue;
-          }
-          float al = 0.f, be = 0.f, ga = 0.f;
-          for (int i = lane; i < k; i += 32) {
-            const float x = up[i], y = uq[i];
-            al = fmaf(x, x, al);
-            be = fmaf(y, y, be);
-            ga = fmaf(x, y, ga);
-          }
-          al = warp_sum(al);
-          be = warp_sum(be);
-          ga = warp_sum(ga);
-          if (fabsf(ga) > tol * sqrtf(al) * sqrtf(be) && fabsf(ga) > tau * sqrtf(fmaxf(al, be))) {
-            const float zeta = (be - al) / (2.f * ga);
-            const float tt = copysignf(1.f, zeta) / (fabsf(zeta) + sqrtf(1.f + zeta * zeta));
-            const float c = 1.f / sqrtf(1.f + tt * tt);
-            const float s = c * tt;
-            for (int i = lane; i < k; i += 32) {
-              const float x = up[i], y = uq[i];
-              up[i] = c * x - s * y;
-              uq[i] = s * x + c * y;
-            }
-            float* vp = V + (int64_t)p * k;
-            float* vq = V + (int64_t)q * k;
-            for (int i = lane; i < k; i += 32) {
-              const float x = vp[i], y = vq[i];
-              vp[i] = c * x - s * y;
-              vq[i] = s * x + c * y;
-            }
-            ++my_rot;
-          }
-        }
-        __syncthreads();
-      }
-      if (lane == 0 && my_rot) atomicAdd(&s_rot, my_rot);
-      __syncthreads();
-      last_rot = s_rot;
-      __syncthreads();
-      if (last_rot == 0) break;
-    }
-
-    if (!in_smem) {
-      polish_global(Ab, U, V, Bm, a.Q + boff, lamv, perm, k, kp2, fro2, sm + 2 * kp2);
-      for (int j = tid; j < k; j += blockDim.x) a.lam[mi.lam_off + (int64_t)t.blk * k + j] = lamv[j];
-      if (tid == 0) {
-        float* st = a.stats + 4 * (int64_t)(mi.blk0 + t.blk);
-        st[2] = (float)sweep;
-        st[3] = (float)last_rot;
-        if (sweep >= a.max_sweeps && last_rot > 0) atomicOr(flag, (uint32_t)DOBB_FLAG_NOT_CONVERGED);
-      }
-      __syncthreads();
-      continue;
-    }
-    float* Qb = a.Q + boff;  // holds V1 (column-major) until the final write
-    // (1) E = I - V^T V into U (column q at U + q k), then V1 = V + V E / 2
-    newton_schulz_cols(V, U, k, warp, nw, lane);
-    __syncthreads();
-    for (int j = warp; j < k; j += nw) {
-      const float* ej = U + (int64_t)j * k;
-      for (int i = lane; i < k; i += 32) {
-        float acc = 0.f;
-        for (int q = 0; q < k; ++q) acc = fmaf(V[(int64_t)q * k + i], ej[q], acc);
-        Qb[(int64_t)j * k + i] = fmaf(0.5f, acc, V[(int64_t)j * k + i]);
-      }
-    }
-    __syncthreads();
-    // (2) T = A V1 into U; B = V1^T T (symmetrised) into Bm; W = I into V
-    for (int p = warp; p < k; p += nw) {
-      const float* v1 = Qb + (int64_t)p * k;
-      for (int i = lane; i < k; i += 32) {
-        float acc = 0.f;
-        for (int l = 0; l < k; ++l) acc = fmaf(Ab[(int64_t)l * k + i], v1[l], acc);  // A symmetric
-        U[(int64_t)p * k + i] = acc;
-      }
-    }
-    __syncthreads();
-    for (int p = warp; p < k; p += nw) {
-      const float* v1p = Qb + (int64_t)p * k;
-      const float* tp = U + (int64_t)p * k;
-      for (int q = p; q < k; ++q) {
-        const float* v1q = Qb + (int64_t)q * k;
-        const float* tq = U + (int64_t)q * k;
-        float d = 0.f;
-        for (int i = lane; i < k; i += 32) d = fmaf(v1p[i], tq[i], fmaf(v1q[i], tp[i], d));
-        d = 0.5f * warp_sum(d);
-        if (lane == 0) {
-          Bm[(int64_t)p * k + q] = d;
-          Bm[(int64_t)q * k + p] = d;
-        }
-      }
-    }
-    for (int64_t e = tid; e < kk2; e += blockDim.x) V[e] = ((e / k) == (e % k)) ? 1.f : 0.f;
-    __syncthreads();
-    // (3) one two-sided sweep on B, W accumulated (column-major in V)
-    float* cs = lamv;                         // kk/2 cosines
-    float* sn = lamv + (kp2 >> 1);            // kk/2 sines
     const float bfloor = 1e-3f * kEps * sqrtf(fro2);
-    for (int r = 0; r < kk - 1; ++r) {
-      for (int i = tid; i < kk / 2; i += blockDim.x) {
-        int p, q;
-        rr_pair(r, i, kk, p, q);
-        float c = 1.f, sv = 0.f;
-        if (p < k && q < k) {
-          if (p > q) { const int tt = p; p = q; q = tt; }
-          const float bpq = Bm[(int64_t)p * k + q];
-          if (fabsf(bpq) > bfloor) {
-            const float tau = (Bm[(int64_t)q * k + q] - Bm[(int64_t)p * k + p]) / (2.f * bpq);
-            const float tt = tau >= 0.f ? 1.f / (tau + sqrtf(1.f + tau * tau))
-                                        : -1.f / (-tau + sqrtf(1.f + tau * tau));
-            c = 1.f / sqrtf(1.f + tt * tt);
-            sv = tt * c;
-          }
-        }
-        cs[i] = c;
-        sn[i] = sv;
-      }
-      __syncthreads();
-      // rows p, q of B <- J^T B
-      for (int64_t e = tid; e < (int64_t)(kk / 2) * k; e += blockDim.x) {
-        const int i = (int)(e / k), j = (int)(e % k);
-        if (sn[i] == 0.f) continue;
-        int p, q;
-        rr_pair(r, i, kk, p, q);
-        if (p > q) { const int tt = p; p = q; q = tt; }
-        const float x = Bm[(int64_t)p * k + j], y = Bm[(int64_t)q * k + j];
-        Bm[(int64_t)p * k + j] = cs[i] * x - sn[i] * y;
-        Bm[(int64_t)q * k + j] = sn[i] * x + cs[i] * y;
-      }
-      __syncthreads();
-      // columns p, q of B <- B J, and of W <- W J
-      for (int64_t e = tid; e < (int64_t)(kk / 2) * k; e += blockDim.x) {
-        const int i = (int)(e / k), j = (int)(e % k);
-        if (sn[i] == 0.f) continue;
-        int p, q;
-        rr_pair(r, i, kk, p, q);
-        if (p > q) { const int tt = p; p = q; q = tt; }
-        float x = Bm[(int64_t)j * k + p], y = Bm[(int64_t)j * k + q];
-        Bm[(int64_t)j * k + p] = cs[i] * x - sn[i] * y;
-        Bm[(int64_t)j * k + q] = sn[i] * x + cs[i] * y;
-        x = V[(int64_t)p * k + j];
-        y = V[(int64_t)q * k + j];
-        V[(int64_t)p * k + j] = cs[i] * x - sn[i] * y;
-        V[(int64_t)q * k + j] = sn[i] * x + cs[i] * y;
-      }
-      __syncthreads();
-    }
-    // (4) V2 = V1 W into U; eigenvalues = diag(B)
-    for (int j = warp; j < k; j += nw) {
-      const float* wj = V + (int64_t)j * k;
-      for (int i = lane; i < k; i += 32) {
-        float acc = 0.f;
-        for (int q = 0; q < k; ++q) acc = fmaf(Qb[(int64_t)q * k + i], wj[q], acc);
-        U[(int64_t)j * k + i] = acc;
-      }
-    }
+    const float stop = a.tol > 0.f ? a.tol : kStopOff;
     __syncthreads();
+    rayleigh_ritz(Ab, V, T, Bm, k, work);
+    // fresh: B was formed from A and an orthonormal V since the last sweep;
+    // only a sweep on a fresh B may be the last one
+    int sweeps = 0, last_rot = 0;
+    bool conv = false, fresh = true;
+    for (;;) {
+      const float off = off_rel(Bm, k, red);
+      if (fresh || off > kColdOff) {
+        last_rot = blocked_sweep(Bm, V, T, k, G, tc, bfloor, work, &s_cnt);
+        ++sweeps;
+        if (fresh && (off <= stop || last_rot == 0)) {
+          conv = true;
+          break;
+        }
+        if (sweeps >= a.max_sweeps) break;
+        fresh = false;
+        if (off > kColdOff) continue;
+      }
+      newton_schulz(V, T, Bm, k, work);
+      float* tmp = V;
+      V = T;
+      T = tmp;
+      rayleigh_ritz(Ab, V, T, Bm, k, work);
+      fresh = true;
+    }
     for (int p = tid; p < kp2; p += blockDim.x) {
-      lamv[p] = p < k ? Bm[(int64_t)p * k + p] : -INFINITY;
+      lamv[p] = p < k ? Bm[p * k + p] : -INFINITY;
       perm[p] = p;
     }
     __syncthreads();
-    // (5) E2 = I - V2^T V2 into Bm (column q at Bm + q k)
-    newton_schulz_cols(U, Bm, k, warp, nw, lane);
+    newton_schulz(V, T, Bm, k, work);
+    V = T;
     // sort descending by eigenvalue
     for (int size = 2; size <= kp2; size <<= 1) {
       for (int stride = size >> 1; stride > 0; stride >>= 1) {
-        __syncthreads();
         for (int i = tid; i < kp2; i += blockDim.x) {
           const int j = i ^ stride;
           if (j > i) {
@@ -549,27 +683,21 @@ jacobi_kernel(const __grid_constant__ EigArgs a, int smem_floats) {
             }
           }
         }
+        __syncthreads();
       }
     }
-    __syncthreads();
-    // (6) Q[:, j] = v2_p + (1/2) V2 e2_p with p = perm[j]
-    for (int j = warp; j < k; j += nw) {
+    for (int e = tid; e < k * k; e += blockDim.x) {
+      const int i = e / k, j = e - i * k;
       int p = perm[j];
       if (p < 0 || p >= k) p = j;  // only reachable with a NaN eigenvalue
-      const float* vp = U + (int64_t)p * k;
-      const float* ep = Bm + (int64_t)p * k;
-      for (int i = lane; i < k; i += 32) {
-        float acc = 0.f;
-        for (int q = 0; q < k; ++q) acc = fmaf(U[(int64_t)q * k + i], ep[q], acc);
-        Qb[(int64_t)i * k + j] = fmaf(0.5f, acc, vp[i]);
-      }
+      Qb[e] = V[p * k + i];
     }
     for (int j = tid; j < k; j += blockDim.x) a.lam[mi.lam_off + (int64_t)t.blk * k + j] = lamv[j];
     if (tid == 0) {
       float* st = a.stats + 4 * (int64_t)(mi.blk0 + t.blk);
-      st[2] = (float)sweep;
+      st[2] = (float)sweeps;
       st[3] = (float)last_rot;
-      if (sweep >= a.max_sweeps && last_rot > 0) atomicOr(flag, (uint32_t)DOBB_FLAG_NOT_CONVERGED);
+      if (!conv) atomicOr(flag, (uint32_t)DOBB_FLAG_NOT_CONVERGED);
     }
     __syncthreads();
   }
@@ -577,32 +705,32 @@ jacobi_kernel(const __grid_constant__ EigArgs a, int smem_floats) {
 
 }  // namespace
 
-int jacobi_smem_max_k(size_t smem_limit) {
-  int k = 1;
-  while (smem_bytes_for(k + 1) <= smem_limit) ++k;
-  return k;
-}
-
-// wide = blocks whose U, V live in global scratch: those rotate column pairs
-// held in registers (k <= 512) and polish with the tiled products.
-cudaError_t launch_jacobi(const EigArgs& a, int grid, size_t smem_bytes, cudaStream_t s, bool wide) {
+cudaError_t launch_jacobi(const EigArgs& a, int grid, size_t smem_bytes, cudaStream_t s) {
   if (a.num_tiles <= 0) return cudaSuccess;
-  if (wide)
-    jacobi_kernel<16><<<grid, kThreads, smem_bytes, s>>>(a, (int)(smem_bytes / 4));
-  else
-    jacobi_kernel<0><<<grid, kThreads, smem_bytes, s>>>(a, (int)(smem_bytes / 4));
+  jacobi_kernel<<<grid, kThreads, smem_bytes, s>>>(a, (int)(smem_bytes / 4));
   return cudaGetLastError();
 }
 
-size_t jacobi_smem_for(int k) { return smem_bytes_for(k); }
-size_t jacobi_sort_smem_for(int k) { return (size_t)8 * pow2_ceil(k) + 4 * kGemmSmemFloats; }
+size_t jacobi_smem_for(int k, size_t budget) {
+  const Geo G = geo_for(k);
+  const size_t per_table = 2 * (size_t)G.n2 * G.n2;
+  const size_t fixed = fixed_floats(k);
+  size_t work;
+  if (G.nT == 1) {
+    work = kApplyFloats + per_table;
+  } else {
+    const int tc = tables_per_chunk(k, (int)std::min<size_t>(budget / 4, (size_t)1 << 28));
+    if (tc < 1) return 0;
+    work = std::max<size_t>(kApplyFloats, (size_t)tc * per_table);
+  }
+  const size_t bytes = 4 * (fixed + work);
+  return bytes <= budget ? bytes : 0;
+}
+
 int jacobi_ctas_per_sm() { return 2048 / kThreads; }
 
 cudaError_t configure_jacobi(size_t smem_limit) {
-  cudaError_t e = cudaFuncSetAttribute(jacobi_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem_limit);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(jacobi_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  return cudaFuncSetAttribute(jacobi_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)smem_limit);
 }
 

@@ -104,6 +104,25 @@ def test_refresh_on_accumulated_moments(k, eff):
     check_moments(opt, orc)
 
 
+@pytest.mark.parametrize("n,B,eff", [(1600, 16, 0.3), (3200, 8, 0.2)])
+def test_refresh_cold_then_warm_on_every_block(n, B, eff):
+    """Every block of two wide matrices (k = 100 / 400), refreshed from the
+    identity and again from the previous basis after the moments moved with a
+    second batch of the same distribution.  A solver that ends on a sweep of a
+    B carrying the rounding of earlier sweeps misses the tolerance on a few
+    blocks only, so all of them are scored."""
+    shapes = [(8, n), (8, n)]
+    rng = np.random.default_rng(11)
+    X = [I.activations(4096, n, eff, rng, dtype="bf16") for _ in shapes]
+    opt = _dobb(shapes, B, beta2=0.9, refresh_period=0, act_dtype="bf16")
+    for half in (slice(0, 2048), slice(2048, 4096)):
+        opt.accumulate([to_dev(np.ascontiguousarray(x[half]), "bf16") for x in X])
+        opt.refresh()
+        torch.cuda.synchronize()
+        check_bases(opt, [to_np(opt.tensor("moments", i)) for i in range(len(shapes))])
+        assert np.all(opt.block_flags() == 0)
+
+
 # --------------------------------------------------------------------------
 # (a3 - a7) the update, with the GPU's own basis
 # --------------------------------------------------------------------------
