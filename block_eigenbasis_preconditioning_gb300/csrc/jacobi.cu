@@ -9,15 +9,16 @@
 //   V = current basis (the identity before the first refresh)
 //   B = V^T (A V)
 //   repeat
-//     off = ||off(B)||_F / ||B||_F
-//     one sweep on B, rotating V along
-//     stop when B was freshly formed and off <= tol (that sweep was the
-//       last, small correction) or the sweep rotated nothing
+//     one sweep on B, rotating V along; off = ||off(B)||_F / ||B||_F after it
+//     stop when B was freshly formed before this sweep and off <= tol (2e-6
+//       by default), or the sweep rotated nothing, or off <= 1e-5 has
+//       stopped shrinking (the fp32 floor): after a sweep on a fresh B, off
+//       is the residual that the result will have
 //     while off > 1e-3 keep sweeping the same B (far from diagonal the
 //       rotations are large and a restart buys nothing); otherwise restart:
 //       V <- V + V (I - V^T V) / 2 (Newton-Schulz), B = V^T (A V); a B
-//       that has been swept is never the last one, since its entries carry
-//       the rounding of every rotation so far
+//       that has been swept twice is never trusted to end the iteration,
+//       since its entries carry the rounding of every rotation so far
 //   Lambda = diag(B), V <- V + V (I - V^T V) / 2, columns sorted by
 //   descending eigenvalue, written as row-major Q (column j = eigenvector j).
 //
@@ -50,8 +51,9 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr float kEps = 5.9604645e-8f;  // 2^-24, fp32 unit roundoff
-constexpr float kColdOff = 1e-3f;      // sweep the same B while off(B) is above this
-constexpr float kStopOff = 1e-5f;      // default: the sweep on a B this close to diagonal is the last
+constexpr float kColdOff = 1e-3f;      // sweep the same B again while off(B) stays above this
+constexpr float kStopOff = 2e-6f;      // default: done when a fresh B's sweep leaves off(B) below this
+constexpr float kStallOff = 1e-5f;     // ... or leaves it below this without shrinking (fp32 floor)
 
 constexpr int kT = 64;                 // tile edge of every product
 constexpr int kLd = kT + 4;            // padded row of a staged 64-wide tile
@@ -421,7 +423,7 @@ constexpr int kPre = kT * kT / kThreads;  // elements of a 64 x 64 tile per thre
 // number of rotations (the same value in every thread).
 __device__ int blocked_sweep(float* B, float* V, float* Rbuf, int k, const Geo& G, int tc,
                              float bfloor, float* work, int* s_cnt) {
-  const int tid = threadIdx.x, warp = tid >> 5;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
   const int n2 = G.n2, nn = n2 * n2;
   float* Rs = work;
   float* Rt = work + kT * kLd;
@@ -436,27 +438,34 @@ __device__ int blocked_sweep(float* B, float* V, float* Rbuf, int k, const Geo& 
     // ---- diagonal tiles of the round's tables, tc at a time, a warp per table
     for (int t0 = 0; t0 < G.nT; t0 += tc) {
       const int tcn = min(tc, G.nT - t0);
-      for (int e = tid; e < tcn * nn; e += blockDim.x) {
-        const int tt = e / nn, rem = e - tt * nn;
-        const int a = rem / n2, b = rem - a * n2;
+      // rows of the tables' tiles: a warp per row, lanes along it
+      for (int row = warp; row < tcn * n2; row += nw) {
+        const int tt = row / n2, a = row - tt * n2;
         int gI, gJ;
         rr_pair(br, t0 + tt, G.nG, gI, gJ);
-        const int ca = table_col(a, gI, gJ, G.g, k), cb = table_col(b, gI, gJ, G.g, k);
-        solve[tt * 2 * nn + rem] = (ca < k && cb < k) ? B[ca * k + cb] : 0.f;
-        solve[tt * 2 * nn + nn + rem] = a == b ? 1.f : 0.f;
+        const int ca = table_col(a, gI, gJ, G.g, k);
+        float* Srow = solve + tt * 2 * nn + a * n2;
+        for (int b = lane; b < n2; b += 32) {
+          const int cb = table_col(b, gI, gJ, G.g, k);
+          Srow[b] = (ca < k && cb < k) ? B[ca * k + cb] : 0.f;
+          Srow[nn + b] = a == b ? 1.f : 0.f;
+        }
       }
       __syncthreads();
       if (warp < tcn)
         rots += solve_table(solve + warp * 2 * nn, solve + warp * 2 * nn + nn, br, t0 + warp, G, k, bfloor);
       __syncthreads();
-      for (int e = tid; e < tcn * nn; e += blockDim.x) {
-        const int tt = e / nn, rem = e - tt * nn;
-        const int a = rem / n2, b = rem - a * n2;
+      for (int row = warp; row < tcn * n2; row += nw) {
+        const int tt = row / n2, a = row - tt * n2;
         int gI, gJ;
         rr_pair(br, t0 + tt, G.nG, gI, gJ);
-        const int ca = table_col(a, gI, gJ, G.g, k), cb = table_col(b, gI, gJ, G.g, k);
-        if (ca < k && cb < k) B[ca * k + cb] = solve[tt * 2 * nn + rem];
-        if (G.nT > 1) Rbuf[(t0 + tt) * nn + rem] = solve[tt * 2 * nn + nn + rem];
+        const int ca = table_col(a, gI, gJ, G.g, k);
+        const float* Srow = solve + tt * 2 * nn + a * n2;
+        for (int b = lane; b < n2; b += 32) {
+          const int cb = table_col(b, gI, gJ, G.g, k);
+          if (ca < k && cb < k) B[ca * k + cb] = Srow[b];
+          if (G.nT > 1) Rbuf[(t0 + tt) * nn + a * n2 + b] = Srow[nn + b];
+        }
       }
       __syncthreads();
     }
@@ -515,13 +524,14 @@ __device__ int blocked_sweep(float* B, float* V, float* Rbuf, int k, const Geo& 
         int sI, sJ, tI, tJ;
         rr_pair(br, s, G.nG, sI, sJ);
         rr_pair(br, t, G.nG, tI, tJ);
-        for (int e = tid; e < n2 * n2; e += blockDim.x) {
-          const int a = e / n2, b = e - a * n2;
-          const int ca = table_col(a, sI, sJ, G.g, k), cb = table_col(b, tI, tJ, G.g, k);
-          if (ca < k && cb < k) B[ca * k + cb] = Xt[a * kLd + b];
-          // transposed copy, consecutive threads along a row of B
-          const int ct = table_col(a, tI, tJ, G.g, k), cs = table_col(b, sI, sJ, G.g, k);
-          if (ct < k && cs < k) B[ct * k + cs] = Yt[a * kLd + b];
+        // Z to rows P_s and Z^T to rows P_t, a warp per row, lanes along it
+        for (int a = warp; a < n2; a += nw) {
+          const int ca = table_col(a, sI, sJ, G.g, k), ct = table_col(a, tI, tJ, G.g, k);
+          for (int b = lane; b < n2; b += 32) {
+            const int cb = table_col(b, tI, tJ, G.g, k), cs = table_col(b, sI, sJ, G.g, k);
+            if (ca < k && cb < k) B[ca * k + cb] = Xt[a * kLd + b];
+            if (ct < k && cs < k) B[ct * k + cs] = Yt[a * kLd + b];
+          }
         }
         __syncthreads();
         s = sn;
@@ -568,10 +578,11 @@ __device__ int blocked_sweep(float* B, float* V, float* Rbuf, int k, const Geo& 
         __syncthreads();
         int tI, tJ;
         rr_pair(br, t, G.nG, tI, tJ);
-        for (int e = tid; e < n2 * kT; e += blockDim.x) {
-          const int b = e / kT, i = e - b * kT;
+        for (int b = warp; b < n2; b += nw) {
           const int cb = table_col(b, tI, tJ, G.g, k);
-          if (cb < k && i0 + i < k) V[cb * k + i0 + i] = Yt[b * kLd + i];
+          if (cb >= k) continue;
+          for (int i = lane; i < kT; i += 32)
+            if (i0 + i < k) V[cb * k + i0 + i] = Yt[b * kLd + i];
         }
         __syncthreads();
       }
@@ -635,23 +646,27 @@ jacobi_kernel(const __grid_constant__ EigArgs a, int smem_floats) {
     const float stop = a.tol > 0.f ? a.tol : kStopOff;
     __syncthreads();
     rayleigh_ritz(Ab, V, T, Bm, k, work);
-    // fresh: B was formed from A and an orthonormal V since the last sweep;
-    // only a sweep on a fresh B may be the last one
+    // fresh: B was formed from A and an orthonormal V and swept once; only
+    // such a sweep may be the last one.  After it, off(B) measures what the
+    // sweep left undone, i.e. the residual of the result.
     int sweeps = 0, last_rot = 0;
     bool conv = false, fresh = true;
+    float prev = INFINITY;  // off(B) after the previous sweep on a fresh B
     for (;;) {
+      last_rot = blocked_sweep(Bm, V, T, k, G, tc, bfloor, work, &s_cnt);
+      ++sweeps;
       const float off = off_rel(Bm, k, red);
-      if (fresh || off > kColdOff) {
-        last_rot = blocked_sweep(Bm, V, T, k, G, tc, bfloor, work, &s_cnt);
-        ++sweeps;
-        if (fresh && (off <= stop || last_rot == 0)) {
+      if (fresh) {
+        // converged, or at the fp32 floor: small and no longer shrinking
+        if (off <= stop || last_rot == 0 || (off <= kStallOff && off > 0.7f * prev)) {
           conv = true;
           break;
         }
-        if (sweeps >= a.max_sweeps) break;
-        fresh = false;
-        if (off > kColdOff) continue;
+        prev = off;
       }
+      if (sweeps >= a.max_sweeps) break;
+      fresh = false;
+      if (off > kColdOff) continue;  // far from diagonal: sweep the same B again
       newton_schulz(V, T, Bm, k, work);
       float* tmp = V;
       V = T;

@@ -134,8 +134,9 @@ dobb_status dobb_step_with_signs(dobb_handle h, void* const* W, const void* cons
 dobb_status dobb_get_step(dobb_handle h, int64_t* t);
 dobb_status dobb_set_step(dobb_handle h, int64_t t);
 
-/* Eigensolver controls: sweep cap (default 40) and relative column
- * orthogonality threshold (0 = default, a few fp32 ulps times sqrt(k)). */
+/* Eigensolver controls: sweep cap (default 40) and the convergence
+ * threshold, the relative off-diagonal norm ||off(B)||_F / ||B||_F that the
+ * last sweep of B = V^T A V may leave (0 = default 2e-6). */
 dobb_status dobb_set_jacobi(dobb_handle h, int max_sweeps, float tol);
 
 /* Device pointer and byte size of a state tensor of one matrix
