@@ -60,7 +60,7 @@ constexpr int kLd = kT + 4;            // padded row of a staged 64-wide tile
 constexpr int kGK = 32;                // reduction depth of one stage of the k x k product
 constexpr int kGemmFloats = 2 * 2 * kGK * kLd;  // two stages of the X and Y tiles
 constexpr int kApplyFloats = 4 * kT * kLd;      // R_s, R_t, X, Y^T of the tile updates
-constexpr int kMaxTables = kThreads / 32;       // tables solved together, a warp each
+constexpr int kMaxTables = kThreads / 32;       // tables solved together (a team of warps each)
 static_assert(kGemmFloats <= kApplyFloats, "product stages live in the tile-update area");
 
 __host__ __device__ __forceinline__ int pow2_ceil(int v) {
@@ -311,21 +311,35 @@ __device__ __forceinline__ bool inner_pair(bool intra, int r, int i, int g, int 
   return table_col(p, gI, gJ, g, k) < k && table_col(q, gI, gJ, g, k) < k;
 }
 
-// Rotations of one table's diagonal tile by one warp: each inner round
-// rotates a set of disjoint column pairs of S (n2 x n2, row-major, shared
-// memory), S <- J^T S J, and accumulates R <- R J.  Lane i owns pair i of
-// the round (at most 32 pairs), so the pair's indices and rotation stay in
-// registers and are broadcast by shuffles for the row updates.  The pairs
-// are disjoint, so each lane loads four pairs' rows (row update) or four rows
-// (column update) before storing any, which keeps several shared-memory
-// loads in flight.  Returns the lane's count of rotations.
-__device__ int solve_table(float* S, float* R, int br, int t, const Geo& G, int k, float bfloor) {
+// Barrier over the nparts warps that solve one table (named barrier id).
+__device__ __forceinline__ void team_sync(int id, int nparts) {
+  if (nparts == 1)
+    __syncwarp();
+  else
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nparts * 32) : "memory");
+}
+
+// Rotations of one table's diagonal tile by a team of nparts warps (this warp
+// is number `part`): each inner round rotates a set of disjoint column pairs
+// of S (n2 x n2, row-major, shared memory), S <- J^T S J, and accumulates
+// R <- R J.  Every warp of the team computes all the round's rotations, lane
+// i for pair i (at most 32 pairs), so indices and rotations stay in
+// registers (broadcast by shuffles for the row updates) and the warps need no
+// exchange besides the barriers; the row updates are split by pairs and the
+// column updates by rows.  Pairs are disjoint, so each lane loads four pairs'
+// rows (row update) or four rows (column update) before storing any, which
+// keeps several shared-memory loads in flight.  Returns the lane's count of
+// rotations (counted by part 0 only).
+__device__ int solve_table(float* S, float* R, int br, int t, const Geo& G, int k, float bfloor,
+                           int part, int nparts, int bar_id) {
   const int lane = threadIdx.x & 31;
   const int n2 = G.n2;
   int gI, gJ;
   rr_pair(br, t, G.nG, gI, gJ);
   const int gp = G.g + (G.g & 1);
   const int n_intra = br == 0 ? gp - 1 : 0;
+  const int perj = (n2 + nparts - 1) / nparts;
+  const int j_lo = min(n2, part * perj), j_hi = min(n2, j_lo + perj);
   int rots = 0;
   for (int step = 0; step < n_intra + G.g; ++step) {
     const bool intra = step < n_intra;
@@ -340,12 +354,15 @@ __device__ int solve_table(float* S, float* R, int br, int t, const Geo& G, int 
         const float tn = ta >= 0.f ? 1.f / (ta + sqrtf(1.f + ta * ta)) : -1.f / (-ta + sqrtf(1.f + ta * ta));
         c = 1.f / sqrtf(1.f + tn * tn);
         s = tn * c;
-        ++rots;
+        if (part == 0) ++rots;
       }
     }
-    __syncwarp();
-    // rows p, q of S, lanes along the row (n2 <= 64: two elements per lane)
-    for (int i0 = 0; i0 < npairs; i0 += 4) {
+    team_sync(bar_id, nparts);
+    // rows p, q of S for this warp's share of the pairs, lanes along the row
+    // (n2 <= 64: two elements per lane)
+    const int per = (npairs + nparts - 1) / nparts;
+    const int i_lo = min(npairs, part * per), i_hi = min(npairs, i_lo + per);
+    for (int i0 = i_lo; i0 < i_hi; i0 += 4) {
       float cu[4], su[4], x[4][2], y[4][2];
       int pu[4], qu[4];
 #pragma unroll
@@ -355,7 +372,7 @@ __device__ int solve_table(float* S, float* R, int br, int t, const Geo& G, int 
         su[u] = __shfl_sync(0xffffffffu, s, src);
         pu[u] = __shfl_sync(0xffffffffu, p, src);
         qu[u] = __shfl_sync(0xffffffffu, q, src);
-        if (i0 + u >= npairs) su[u] = 0.f;
+        if (i0 + u >= i_hi) su[u] = 0.f;
       }
 #pragma unroll
       for (int u = 0; u < 4; ++u)
@@ -377,14 +394,15 @@ __device__ int solve_table(float* S, float* R, int br, int t, const Geo& G, int 
           }
         }
     }
-    __syncwarp();
-    // columns p, q of S and R, lane i on pair i, four rows at a time
+    team_sync(bar_id, nparts);
+    // columns p, q of S and R for this warp's share of the rows, lane i on
+    // pair i, four rows at a time
     if (s != 0.f) {
-      for (int j0 = 0; j0 < n2; j0 += 4) {
+      for (int j0 = j_lo; j0 < j_hi; j0 += 4) {
         float a[4], b[4], ra[4], rb[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const int j = j0 + u < n2 ? j0 + u : n2 - 1;
+          const int j = j0 + u < j_hi ? j0 + u : j_hi - 1;
           a[u] = S[j * n2 + p];
           b[u] = S[j * n2 + q];
           ra[u] = R[j * n2 + p];
@@ -393,7 +411,7 @@ __device__ int solve_table(float* S, float* R, int br, int t, const Geo& G, int 
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const int j = j0 + u;
-          if (j < n2) {
+          if (j < j_hi) {
             S[j * n2 + p] = c * a[u] - s * b[u];
             S[j * n2 + q] = s * a[u] + c * b[u];
             R[j * n2 + p] = c * ra[u] - s * rb[u];
@@ -402,7 +420,7 @@ __device__ int solve_table(float* S, float* R, int br, int t, const Geo& G, int 
         }
       }
     }
-    __syncwarp();
+    team_sync(bar_id, nparts);
   }
   return rots;
 }
@@ -435,7 +453,7 @@ __device__ int blocked_sweep(float* B, float* V, float* Rbuf, int k, const Geo& 
   const int nI = (k + kT - 1) / kT;
   int rots = 0;
   for (int br = 0; br < G.nG - 1; ++br) {
-    // ---- diagonal tiles of the round's tables, tc at a time, a warp per table
+    // ---- diagonal tiles of the round's tables, tc at a time
     for (int t0 = 0; t0 < G.nT; t0 += tc) {
       const int tcn = min(tc, G.nT - t0);
       // rows of the tables' tiles: a warp per row, lanes along it
@@ -452,8 +470,15 @@ __device__ int blocked_sweep(float* B, float* V, float* Rbuf, int k, const Geo& 
         }
       }
       __syncthreads();
-      if (warp < tcn)
-        rots += solve_table(solve + warp * 2 * nn, solve + warp * 2 * nn + nn, br, t0 + warp, G, k, bfloor);
+      {
+        // a team of wpt warps per table (named barriers 1 ... tcn)
+        int wpt = nw / tcn;
+        wpt = wpt >= 4 ? 4 : (wpt >= 2 ? 2 : 1);
+        const int tt = warp / wpt;
+        if (tt < tcn)
+          rots += solve_table(solve + tt * 2 * nn, solve + tt * 2 * nn + nn, br, t0 + tt, G, k, bfloor,
+                              warp - tt * wpt, wpt, 1 + tt);
+      }
       __syncthreads();
       for (int row = warp; row < tcn * n2; row += nw) {
         const int tt = row / n2, a = row - tt * n2;
