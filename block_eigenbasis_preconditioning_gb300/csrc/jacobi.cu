@@ -179,48 +179,54 @@ __device__ void block_gemm(const float* X, const float* Y, float* C, const float
   const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
   const int nt = (k + kT - 1) / kT;
   const int nch = (k + kGK - 1) / kGK;
-  constexpr int kPer = kGK * kT / kThreads;  // elements of each operand per thread and stage
+  constexpr int kPer4 = kGK * kT / (4 * kThreads);  // float4 groups of each operand per thread and stage
   for (int tile = 0; tile < nt * nt; ++tile) {
     const int ti = tile % nt, tj = tile / nt;
     if (sym && ti > tj) continue;
     const int i0 = ti * kT, j0 = tj * kT;
     float acc[4][4];
     zero_acc(acc);
-    float rx[kPer], ry[kPer];
+    // each thread moves groups of four: four rows (X^T, Y) or four
+    // consecutive elements (X) of one reduction index, stored as one float4
+    float4 rx[kPer4], ry[kPer4];
     auto gload = [&](int l0) {
 #pragma unroll
-      for (int r = 0; r < kPer; ++r) {
+      for (int r = 0; r < kPer4; ++r) {
         const int e = tid + r * kThreads;
-        int l, i;
+        float v[4];
         if (XT) {
-          l = e % kGK;
-          i = e / kGK;
+          const int l = e % kGK, iq = e / kGK;
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int i = 4 * iq + u;
+            v[u] = (i0 + i < k && l0 + l < k) ? X[(i0 + i) * k + l0 + l] : 0.f;
+          }
         } else {
-          i = e % kT;
-          l = e / kT;
+          const int iq = e % (kT / 4), l = e / (kT / 4);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int i = 4 * iq + u;
+            v[u] = (i0 + i < k && l0 + l < k) ? X[(l0 + l) * k + i0 + i] : 0.f;
+          }
         }
-        float xv = 0.f;
-        if (i0 + i < k && l0 + l < k) xv = XT ? X[(i0 + i) * k + l0 + l] : X[(l0 + l) * k + i0 + i];
-        rx[r] = xv;
-        const int ly = e % kGK, j = e / kGK;
-        ry[r] = (j0 + j < k && l0 + ly < k) ? Y[(j0 + j) * k + l0 + ly] : 0.f;
+        rx[r] = make_float4(v[0], v[1], v[2], v[3]);
+        const int l = e % kGK, jq = e / kGK;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int j = 4 * jq + u;
+          v[u] = (j0 + j < k && l0 + l < k) ? Y[(j0 + j) * k + l0 + l] : 0.f;
+        }
+        ry[r] = make_float4(v[0], v[1], v[2], v[3]);
       }
     };
     auto sstore = [&](float* xd, float* yd) {
 #pragma unroll
-      for (int r = 0; r < kPer; ++r) {
+      for (int r = 0; r < kPer4; ++r) {
         const int e = tid + r * kThreads;
-        int l, i;
-        if (XT) {
-          l = e % kGK;
-          i = e / kGK;
-        } else {
-          i = e % kT;
-          l = e / kT;
-        }
-        xd[l * kLd + i] = rx[r];
-        const int ly = e % kGK, j = e / kGK;
-        yd[ly * kLd + j] = ry[r];
+        const int lx = XT ? e % kGK : e / (kT / 4), iq = XT ? e / kGK : e % (kT / 4);
+        *reinterpret_cast<float4*>(xd + lx * kLd + 4 * iq) = rx[r];
+        const int l = e % kGK, jq = e / kGK;
+        *reinterpret_cast<float4*>(yd + l * kLd + 4 * jq) = ry[r];
       }
     };
     gload(0);
