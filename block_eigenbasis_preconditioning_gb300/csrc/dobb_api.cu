@@ -55,13 +55,17 @@ struct Layout {
 };
 
 constexpr int kTcRows = 128;
+// tensor-core tiles of blocks up to this width get their own launch, whose
+// small operand stages leave room for many in flight
+constexpr int kTcSmallK = 128;
 
 int64_t pad16f(int64_t v) { return (v + 15) / 16 * 16; }
 
 struct Chunk {
   int mat_base = 0, mat_end = 0;
   int step_off = 0, step_n = 0;     // FFMA tiles of every matrix
-  int tc_off = 0, tc_n = 0;         // tensor-core tiles (eligible matrices)
+  int tc_off = 0, tc_n = 0;         // tensor-core tiles (eligible matrices), widest first
+  int tc_small = 0;                 // index (within them) of the first tile with k <= 128
   int rest_off = 0, rest_n = 0;     // FFMA tiles of the other matrices
   int max_k_tc = 0, max_k_rest = 1;
   int syrk_off = 0, syrk_n = 0;
@@ -152,6 +156,9 @@ WorkLists build_work(int num, const int64_t* m, const int64_t* n, int B) {
     std::stable_sort(rest.begin(), rest.end(), [](auto& x, auto& y) { return x.first > y.first; });
     ch.tc_off = (int)wl.tiles.size();
     ch.tc_n = (int)v.size();
+    ch.tc_small = ch.tc_n;
+    for (int j = 0; j < ch.tc_n; ++j)
+      if (v[j].first <= kTcSmallK) { ch.tc_small = j; break; }
     for (auto& e : v) wl.tiles.push_back(e.second);
     ch.rest_off = (int)wl.tiles.size();
     ch.rest_n = (int)rest.size();
@@ -404,19 +411,32 @@ dobb_status do_step(dobb_handle h, void* const* W, const void* const* G, float l
       a.S[i - ch.mat_base] = S_out ? S_out[i] : nullptr;
     }
     if (use_tc && ch.tc_n > 0) {
-      StepArgs at = a;
-      at.tiles = h->dtiles() + ch.tc_off;
-      at.num_tiles = ch.tc_n;
-      TcArgs t{};
-      t.maps = h->dmaps();
-      t.qpack = h->pack();
-      t.err = h->err();
-      t.bstage = (int32_t)step_tc_bstage(ch.max_k_tc);
-      const size_t smem = step_tc_smem(ch.max_k_tc);
-      const int g = std::max(1, std::min(ch.tc_n, h->sm_count));
-      cudaError_t e = launch_step_tc(at, t, h->pdt, g, smem, s);
-      if (e != cudaSuccess) return fail(DOBB_ERR_CUDA, "tensor-core step launch: %s", cudaGetErrorString(e));
-      ++h->launches;
+      // two launches: blocks wider than kTcSmallK, then the narrow ones
+      for (int part = 0; part < 2; ++part) {
+        const int lo = part == 0 ? 0 : ch.tc_small, hi = part == 0 ? ch.tc_small : ch.tc_n;
+        if (hi <= lo) continue;
+        int kmax = 4;
+        for (int j = lo; j < hi; ++j) {
+          const Tile& tl = h->wl.tiles[ch.tc_off + j];
+          kmax = std::max(kmax, (int)(h->n[tl.mat] / h->B));
+        }
+        StepArgs at = a;
+        at.tiles = h->dtiles() + ch.tc_off + lo;
+        at.num_tiles = hi - lo;
+        TcArgs t{};
+        t.maps = h->dmaps();
+        t.qpack = h->pack();
+        t.err = h->err();
+        t.bstage = (int32_t)step_tc_bstage(kmax);
+        t.nbstage = step_tc_bstages(kmax, h->smem_limit);
+        if (t.nbstage < 2)
+          return fail(DOBB_ERR_UNSUPPORTED, "block width %d leaves no room for operand stages", kmax);
+        const size_t smem = step_tc_smem(kmax, t.nbstage);
+        const int g = std::max(1, std::min(hi - lo, h->sm_count));
+        cudaError_t e = launch_step_tc(at, t, h->pdt, g, smem, s);
+        if (e != cudaSuccess) return fail(DOBB_ERR_CUDA, "tensor-core step launch: %s", cudaGetErrorString(e));
+        ++h->launches;
+      }
     }
     const bool rest_only = use_tc && ch.tc_n > 0;
     const int n_ffma = rest_only ? ch.rest_n : ch.step_n;

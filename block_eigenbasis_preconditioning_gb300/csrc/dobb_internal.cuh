@@ -43,6 +43,7 @@ struct TcArgs {
   const unsigned char* qpack;
   uint32_t* err;           // device error word (timeouts)
   int32_t bstage;          // bytes of one B stage
+  int32_t nbstage;         // B stages (2 ... 16)
 };
 
 // One unit of grouped work: matrix, block and two phase-specific indices.
@@ -141,8 +142,9 @@ int jacobi_ctas_per_sm();
 size_t step_smem_for(int k);
 cudaError_t configure_jacobi(size_t smem_limit);
 cudaError_t configure_step(size_t smem_limit);
-size_t step_tc_smem(int max_k);
+size_t step_tc_smem(int max_k, int nbstage);
 size_t step_tc_bstage(int max_k);
+int step_tc_bstages(int max_k, size_t smem_limit);  // B stages that fit (0: none)
 int64_t tc_block_image_bytes(int k);
 bool tc_eligible(int64_t m, int64_t n, int k);
 cudaError_t configure_step_tc(size_t smem_limit);

@@ -38,14 +38,14 @@ using namespace ptx;
 constexpr int kThreads = 320;
 constexpr int kTM = 128;
 constexpr int kAStages = 2;
-constexpr int kBStages = 4;
+constexpr int kMaxBStages = 16;  // the launch picks how many fit (small blocks: many)
 constexpr int kAChunkBytes = kTM * 32 * 4;  // 32 fp32 columns, 128B swizzle
 constexpr int kUCols = 128;
 constexpr uint32_t kTmemCols = 512;
 
 struct TcSmem {
   uint64_t a_full[kAStages], a_conv[kAStages], a_empty[kAStages];
-  uint64_t b_full[kBStages], b_empty[kBStages];
+  uint64_t b_full[kMaxBStages], b_empty[kMaxBStages];
   uint64_t c_full, s_full;
   uint64_t u_full[2], u_empty[2];
   uint64_t r_done, fin;
@@ -120,16 +120,17 @@ step_tc_kernel(const __grid_constant__ StepArgs a, const __grid_constant__ TcArg
       (reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
   unsigned char* a_buf = base;                                   // [stage][hi|lo]
   unsigned char* b_buf = base + kAStages * 2 * kAChunkBytes;     // [stage] t.bstage bytes
-  TcSmem* sh = reinterpret_cast<TcSmem*>(b_buf + kBStages * t.bstage);
+  TcSmem* sh = reinterpret_cast<TcSmem*>(b_buf + t.nbstage * t.bstage);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t nbs = (uint32_t)t.nbstage;  // B stages of this launch
   if (threadIdx.x == 0) {
     for (int i = 0; i < kAStages; ++i) {
       mbar_init(&sh->a_full[i], 1);
       mbar_init(&sh->a_conv[i], 4);
       mbar_init(&sh->a_empty[i], 1);
     }
-    for (int i = 0; i < kBStages; ++i) {
+    for (int i = 0; i < t.nbstage; ++i) {
       mbar_init(&sh->b_full[i], 1);
       mbar_init(&sh->b_empty[i], 1);
     }
@@ -178,7 +179,7 @@ step_tc_kernel(const __grid_constant__ StepArgs a, const __grid_constant__ TcArg
             const uint32_t bytes = 2u * kpN * 32u;
             mbar_arrive_expect_tx(&sh->b_full[bs], bytes);
             bulk_load(b_buf + bs * t.bstage, qp + (int64_t)sub * bytes, bytes, &sh->b_full[bs]);
-            if (++bs == kBStages) { bs = 0; bp ^= 1; }
+            if (++bs == nbs) { bs = 0; bp ^= 1; }
           }
         }
         // reconstruct operands: chunks of 128 output columns, 16-wide K steps
@@ -191,7 +192,7 @@ step_tc_kernel(const __grid_constant__ StepArgs a, const __grid_constant__ TcArg
             mbar_arrive_expect_tx(&sh->b_full[bs], bytes);
             bulk_load(b_buf + bs * t.bstage, qr + off, bytes, &sh->b_full[bs]);
             off += bytes;
-            if (++bs == kBStages) { bs = 0; bp ^= 1; }
+            if (++bs == nbs) { bs = 0; bp ^= 1; }
           }
         }
       }
@@ -261,7 +262,7 @@ step_tc_kernel(const __grid_constant__ StepArgs a, const __grid_constant__ TcArg
             tc_commit(&sh->b_empty[bs]);
           }
           __syncwarp();
-          if (++bs == kBStages) { bs = 0; bp ^= 1; }
+          if (++bs == nbs) { bs = 0; bp ^= 1; }
         }
         if (lane == 0) tc_commit(&sh->a_empty[as]);
         __syncwarp();
@@ -295,7 +296,7 @@ step_tc_kernel(const __grid_constant__ StepArgs a, const __grid_constant__ TcArg
             tc_commit(&sh->b_empty[bs]);
           }
           __syncwarp();
-          if (++bs == kBStages) { bs = 0; bp ^= 1; }
+          if (++bs == nbs) { bs = 0; bp ^= 1; }
         }
         if (!ok) break;
         if (lane == 0) tc_commit(&sh->u_full[b]);
@@ -552,15 +553,20 @@ pack_bases_kernel(const float* Q, unsigned char* qpack, const MatInfo* info, con
 
 }  // namespace
 
-size_t step_tc_smem(int max_k) {
-  const int kpN = (max_k + 15) & ~15;
-  const size_t bstage = (size_t)std::max(2 * kpN * 32, 2 * kUCols * 32);
-  return 1024 + (size_t)kAStages * 2 * kAChunkBytes + kBStages * bstage + sizeof(TcSmem) + 64;
-}
-
 size_t step_tc_bstage(int max_k) {
   const int kpN = (max_k + 15) & ~15;
   return (size_t)std::max(2 * kpN * 32, 2 * kUCols * 32);
+}
+
+size_t step_tc_smem(int max_k, int nbstage) {
+  return 1024 + (size_t)kAStages * 2 * kAChunkBytes + nbstage * step_tc_bstage(max_k) + sizeof(TcSmem) + 64;
+}
+
+int step_tc_bstages(int max_k, size_t smem_limit) {
+  const size_t fixed = step_tc_smem(max_k, 0);
+  const size_t per = step_tc_bstage(max_k);
+  const int nb = smem_limit > fixed ? (int)((smem_limit - fixed) / per) : 0;
+  return std::min(kMaxBStages, nb);
 }
 
 int64_t tc_block_image_bytes(int k) {
