@@ -67,6 +67,7 @@ __all__ = [
     "reconstruct",
     "apply_update",
     "round_to_bf16",
+    "basis_for_update",
     "update_from_bases",
     "DobbOracle",
 ]
@@ -258,16 +259,32 @@ def apply_update(W: np.ndarray, U: np.ndarray, lr: float, s: float,
     return out
 
 
+def basis_for_update(Q: np.ndarray, basis_dtype: str = "f32") -> np.ndarray:
+    """The block bases the update multiplies with.  "bf16": the stored basis
+    is bfloat16 ([Dobb, Table 18]: fp32 moment accumulation with a bf16
+    basis is the principal setting, 6 n^2 / B bytes per matrix), i.e. every
+    entry of Q rounded once to bf16; the products themselves stay exact here.
+    "f32": Q as given."""
+    if basis_dtype == "bf16":
+        return round_to_bf16(Q)
+    if basis_dtype != "f32":
+        raise ValueError(f"basis_dtype {basis_dtype!r}")
+    return _f64(Q)
+
+
 def update_from_bases(W, M, G, Q, beta1: float, lr: float, s: float,
-                      param_dtype: str = "f32", S_override: Optional[np.ndarray] = None):
+                      param_dtype: str = "f32", S_override: Optional[np.ndarray] = None,
+                      basis_dtype: str = "f32"):
     """One update of a single matrix with given block bases Q (B, k, k).
     Returns dict with the new M, C, S, U and W.  `S_override` substitutes a
     given sign matrix (used to score a second implementation's signs at the
-    entries where the sign is numerically undetermined)."""
+    entries where the sign is numerically undetermined).  `basis_dtype`
+    selects the stored precision of the basis (see `basis_for_update`)."""
+    Qu = basis_for_update(Q, basis_dtype)
     Mn = momentum(M, G, beta1)
-    C = project(Mn, Q)
+    C = project(Mn, Qu)
     S = sign(C) if S_override is None else _f64(S_override)
-    U = reconstruct(S, Q)
+    U = reconstruct(S, Qu)
     Wn = apply_update(W, U, lr, s, param_dtype)
     return {"M": Mn, "C": C, "S": S, "U": U, "W": Wn}
 
@@ -291,6 +308,7 @@ class DobbOracle:
     scale_s: float = 1.0
     param_dtype: str = "f32"
     eig_method: str = "auto"
+    basis_dtype: str = "f32"
 
     def __post_init__(self):
         self.t = 0
@@ -323,7 +341,7 @@ class DobbOracle:
         out_W, parts = [], []
         for i, (W, G) in enumerate(zip(W_list, G_list)):
             r = update_from_bases(W, self.M[i], G, self.Q[i], self.beta1, lr,
-                                  self.scale_s, self.param_dtype)
+                                  self.scale_s, self.param_dtype, basis_dtype=self.basis_dtype)
             self.M[i] = r["M"]
             out_W.append(r["W"])
             if keep_parts:

@@ -224,6 +224,73 @@ def test_invariances():
     assert np.abs(Qa - Qb).max() < 1e-12 and np.abs(5.0 * la - lb).max() < 1e-12
 
 
+# --------------------------------------------------------------------------
+# bf16 basis storage ([Dobb, Table 18]: the principal precision setting)
+# --------------------------------------------------------------------------
+
+def test_bf16_basis_identity_and_invariances():
+    rng = np.random.default_rng(41)
+    M, G, W, Q = _rand_case(rng, m=20, n=12, B=3)
+    # the identity is exact in bf16: U = sign(M) as with the fp32 basis
+    I4 = np.broadcast_to(np.eye(4), (3, 4, 4)).copy()
+    r = O.update_from_bases(W, M, G, I4, 0.95, 0.02, 1.0, basis_dtype="bf16")
+    assert np.array_equal(r["U"], np.sign(0.95 * M + G))
+    # column sign flips and permutations of Q_b still leave U unchanged
+    base = O.update_from_bases(W, M, G, Q, 0.95, 0.02, 1.0, basis_dtype="bf16")["U"]
+    Q2 = Q.copy()
+    for b in range(3):
+        Q2[b] = (Q[b] * rng.choice([-1.0, 1.0], size=4)[None, :])[:, rng.permutation(4)]
+    U2 = O.update_from_bases(W, M, G, Q2, 0.95, 0.02, 1.0, basis_dtype="bf16")["U"]
+    assert np.abs(U2 - base).max() < 1e-12
+
+
+def test_bf16_basis_brute_force_with_torch_rounding():
+    """Hand loops with the basis rounded by torch's bf16 conversion (Q chosen
+    exactly representable in fp32, so torch's fp32 -> bf16 rounding is the
+    single rounding the oracle applies)."""
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(42)
+    m, n, B = 3, 4, 2
+    k = n // B
+    M = rng.standard_normal((m, n))
+    G = rng.standard_normal((m, n))
+    W = rng.standard_normal((m, n))
+    Q = np.stack([np.linalg.qr(rng.standard_normal((k, k)))[0] for _ in range(B)])
+    Q = Q.astype(np.float32).astype(np.float64)
+    Qb = torch.from_numpy(Q.astype(np.float32)).to(torch.bfloat16).to(torch.float64).numpy()
+    beta1, lr, s = 0.9, 0.05, 2.0
+    W_exp = np.zeros((m, n))
+    for i in range(m):
+        for b in range(B):
+            cols = range(b * k, (b + 1) * k)
+            mn = [beta1 * M[i, c] + G[i, c] for c in cols]
+            sg = [math.copysign(1.0, sum(mn[l] * Qb[b, l, j] for l in range(k))) for j in range(k)]
+            for l in range(k):
+                u = sum(sg[j] * Qb[b, l, j] for j in range(k))
+                W_exp[i, b * k + l] = W[i, b * k + l] - lr * s * u
+    r = O.update_from_bases(W, M, G, Q, beta1, lr, s, basis_dtype="bf16")
+    assert np.abs(r["W"] - W_exp).max() < 1e-12
+    assert not np.array_equal(Qb, Q)  # the rounding did act
+
+
+def test_bf16_basis_update_within_rounding_bound():
+    """With the same signs, |U_bf16 - U_f32| <= ||S_b||_F ||bf16(Q_b) - Q_b||_2
+    per block, and each basis entry moves by at most half a bf16 quantum,
+    i.e. 2^-8 of its size (8 significant bits)."""
+    rng = np.random.default_rng(43)
+    M, G, W, Q = _rand_case(rng, m=40, n=24, B=3)
+    r32 = O.update_from_bases(W, M, G, Q, 0.95, 0.02, 1.0)
+    r16 = O.update_from_bases(W, M, G, Q, 0.95, 0.02, 1.0, S_override=r32["S"], basis_dtype="bf16")
+    Qb = O.basis_for_update(Q, "bf16")
+    assert np.all(np.abs(Qb - Q) <= 2.0 ** -8 * np.abs(Q))
+    k = 8
+    for b in range(3):
+        sl = slice(b * k, (b + 1) * k)
+        bound = np.linalg.norm(r32["S"][:, sl]) * np.linalg.norm(Qb[b] - Q[b], 2)
+        assert np.linalg.norm(r16["U"][:, sl] - r32["U"][:, sl]) <= bound * (1 + 1e-12)
+        assert np.linalg.norm(r16["U"][:, sl] - r32["U"][:, sl]) > 0
+
+
 def test_ema_linearity_block_diagonal():
     """Block moments are the diagonal blocks of the full moment's EMA, and
     the EMA is linear (averaging replicas' EMAs = EMA of averaged moments)."""
