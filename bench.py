@@ -208,7 +208,7 @@ def _traffic_for(kernel_key):
 # CPU baseline: the oracle on a bounded sample
 # ---------------------------------------------------------------------------
 
-def cpu_baseline(layers_sample=2, seed=0):
+def cpu_baseline(layers_sample=2, seed=0, basis="f32"):
     import numpy as np
     from block_eigenbasis_preconditioning_gb300 import inputs as I
     from oracle import dobb as O
@@ -218,7 +218,7 @@ def cpu_baseline(layers_sample=2, seed=0):
         shapes += [(1600, 1600)] * 4 + [(6400, 1600), (1600, 6400)]
     params = sum(m * n for m, n in shapes)
     orc = O.DobbOracle(shapes, B_BLOCKS, BETA1, BETA2, refresh_period=0, scale_s=SCALE,
-                       param_dtype="bf16", eig_method="lapack")
+                       param_dtype="bf16", eig_method="lapack", basis_dtype=basis)
     Xs = [I.round_bf16_np(rng.standard_normal((N_TOKENS, n)).astype(np.float32)) for _, n in shapes]
     Gs = [I.round_bf16_np((rng.standard_normal((m, n)) * 1e-3).astype(np.float32)) for m, n in shapes]
     Ws = [I.round_bf16_np((rng.standard_normal((m, n)) * 0.02).astype(np.float32)) for m, n in shapes]
@@ -238,6 +238,20 @@ def cpu_baseline(layers_sample=2, seed=0):
             "seconds": {"accumulate": acc, "refresh": ref, "update": upd}}
 
 
+def workload_config(args, n_matrices=None, params=None):
+    """The workload both arms report (the reference arm runs a bounded sample
+    of it on the host, described in its cpu_baseline)."""
+    if args.layers is None:
+        name = ("gpt2-xl B=16: 289 matrices, 1.555e9 params, bf16 W/G, fp32 M, "
+                "X 8192 bf16 tokens/matrix, refresh every 10")
+    else:
+        name = (f"gpt2-xl shapes, first {args.layers} layers ({n_matrices} matrices, "
+                f"{params} params), B=16")
+    return {"workload": name, "B": B_BLOCKS, "refresh_period": REFRESH, "tokens": N_TOKENS,
+            "basis": args.basis, "l2": "inputs larger than L2 (22 GB streamed per step)",
+            "parallelism": "single GPU"}
+
+
 def run_reference(args):
     rank, world, _ = _env_rank()
     if rank != 0:
@@ -245,14 +259,13 @@ def run_reference(args):
     steps = []
     res = None
     for _ in range(max(1, args.steps)):
-        res = cpu_baseline(layers_sample=1)
+        res = cpu_baseline(layers_sample=1, basis=args.basis)
         steps.append(res["value"])
     v = sorted(steps)[len(steps) // 2]
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": 1,
             "steps": args.steps, "warmup": 0, "ms_per_step": 1.5549712e9 / v * 1e3 if v else None,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": "gpt2-xl B=16 (bounded CPU sample)",
-                                            "B": B_BLOCKS, "refresh_period": REFRESH},
+            "data": "synthetic", "config": workload_config(args),
             "cpu_baseline": {"value": v, "unit": UNIT, "cores": res["cores"], "kind": "oracle",
                              "sample": res["sample"]},
             "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -284,7 +297,7 @@ def run_gpu(args):
     params = sum(m * n for m, n in shapes)
     Xsets, Gs, Ws = make_inputs(torch, shapes, layers, device, seed=1234 + rank)
     opt = Dobb(shapes, B_BLOCKS, BETA1, BETA2, refresh_period=REFRESH, scale_s=SCALE,
-               param_dtype="bf16", act_dtype="bf16", device=device)
+               param_dtype="bf16", act_dtype="bf16", device=device, basis_dtype=args.basis)
     stream = torch.cuda.current_stream()
     moments = opt.tensor("moments")
 
@@ -386,7 +399,7 @@ def run_gpu(args):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
         try:
-            cpu = cpu_baseline()
+            cpu = cpu_baseline(basis=args.basis)
         except Exception as ex:  # pragma: no cover
             cpu = {"error": repr(ex)}
 
@@ -396,15 +409,9 @@ def run_gpu(args):
                 "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": ms_step,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
                 "data": "synthetic",
-                "config": {"workload": ("gpt2-xl B=16: 289 matrices, 1.555e9 params, bf16 W/G, "
-                                        "fp32 M, X 8192 bf16 tokens/matrix, refresh every 10")
-                           if args.layers is None else
-                           f"gpt2-xl shapes, first {args.layers} layers ({len(shapes)} matrices, "
-                           f"{params} params), B=16",
-                           "B": B_BLOCKS, "refresh_period": REFRESH, "tokens": N_TOKENS,
-                           "refresh_steps_timed": sum(is_refresh),
-                           "l2": "inputs larger than L2 (22 GB streamed per step)",
-                           "parallelism": f"dp{world} replicas" if world > 1 else "single GPU"},
+                "config": dict(workload_config(args, len(shapes), params),
+                               refresh_steps_timed=sum(is_refresh),
+                               parallelism=f"dp{world} replicas" if world > 1 else "single GPU"),
                 "phases_ms": {"accumulate": mean(acc_ms), "update": upd_mean, "refresh": refresh_ms,
                               "amortized_step": amort},
                 "phases": phases, "roofline": roofline, "clocks": clk,
@@ -456,6 +463,9 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--basis", default="f32", choices=["f32", "bf16"],
+                    help="precision of the basis the update multiplies with (bf16: the "
+                         "pages' principal storage setting)")
     ap.add_argument("--layers", type=int, default=None,
                     help="smaller model of the same layer shapes (first L layers, no "
                          "embedding), for profiler captures")

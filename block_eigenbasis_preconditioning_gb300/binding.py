@@ -45,6 +45,7 @@ SIGNATURES = [
                                         _c.POINTER(_VP), _VP]),
     ("dobb_get_step", _c.c_int, [_VP, _I64P]),
     ("dobb_set_step", _c.c_int, [_VP, _c.c_int64]),
+    ("dobb_set_basis_dtype", _c.c_int, [_VP, _c.c_int, _VP]),
     ("dobb_set_jacobi", _c.c_int, [_VP, _c.c_int, _c.c_float]),
     ("dobb_state_tensor", _c.c_int, [_VP, _c.c_int, _c.c_int, _c.POINTER(_VP),
                                      _c.POINTER(_c.c_size_t)]),

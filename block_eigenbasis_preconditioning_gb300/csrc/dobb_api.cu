@@ -284,6 +284,7 @@ struct dobb_ctx {
   int64_t t = 0;
   int max_sweeps = 40;
   float tol = 0.f;
+  bool basis_bf16 = false;  // the update multiplies with bf16(Q)
   int sm_count = 1;
   size_t smem_limit = 0;
   size_t smem_per_sm = 0;
@@ -328,7 +329,7 @@ dobb_status do_pack(dobb_handle h, cudaStream_t s) {
   if (!h->any_tc) return DOBB_OK;
   const int g = std::max(1, std::min(h->wl.blocks_n, h->sm_count * 8));
   cudaError_t e = launch_pack_bases(h->Q(), h->pack(), h->dinfo(), h->dtiles() + h->wl.blocks_off,
-                                    h->wl.blocks_n, g, s);
+                                    h->wl.blocks_n, h->basis_bf16 ? 1 : 2, g, s);
   if (e != cudaSuccess) return fail(DOBB_ERR_CUDA, "pack launch: %s", cudaGetErrorString(e));
   ++h->launches;
   return DOBB_OK;
@@ -405,6 +406,7 @@ dobb_status do_step(dobb_handle h, void* const* W, const void* const* G, float l
     a.stats = h->stats();
     a.beta1 = h->beta1;
     a.lr_s = lr * h->scale_s;
+    a.basis_bf16 = h->basis_bf16 ? 1 : 0;
     for (int i = ch.mat_base; i < ch.mat_end; ++i) {
       a.W[i - ch.mat_base] = W[i];
       a.G[i - ch.mat_base] = G[i];
@@ -429,6 +431,7 @@ dobb_status do_step(dobb_handle h, void* const* W, const void* const* G, float l
         t.err = h->err();
         t.bstage = (int32_t)step_tc_bstage(kmax);
         t.nbstage = step_tc_bstages(kmax, h->smem_limit);
+        t.npieces = h->basis_bf16 ? 1 : 2;
         if (t.nbstage < 2)
           return fail(DOBB_ERR_UNSUPPORTED, "block width %d leaves no room for operand stages", kmax);
         const size_t smem = step_tc_smem(kmax, t.nbstage);
@@ -757,6 +760,15 @@ dobb_status dobb_set_step(dobb_handle h, int64_t t) {
   if (!h || t < 0) return fail(DOBB_ERR_INVALID_ARG, "bad handle or negative step");
   h->t = t;
   return DOBB_OK;
+}
+
+dobb_status dobb_set_basis_dtype(dobb_handle h, dobb_dtype basis_dtype, void* stream) {
+  if (!h) return fail(DOBB_ERR_INVALID_ARG, "NULL handle");
+  if (basis_dtype != DOBB_F32 && basis_dtype != DOBB_BF16)
+    return fail(DOBB_ERR_INVALID_ARG, "basis dtype must be DOBB_F32 or DOBB_BF16");
+  h->basis_bf16 = basis_dtype == DOBB_BF16;
+  // the tensor-core operand images hold the basis in the chosen precision
+  return do_pack(h, static_cast<cudaStream_t>(stream));
 }
 
 dobb_status dobb_set_jacobi(dobb_handle h, int max_sweeps, float tol) {

@@ -44,6 +44,7 @@ struct TcArgs {
   uint32_t* err;           // device error word (timeouts)
   int32_t bstage;          // bytes of one B stage
   int32_t nbstage;         // B stages (2 ... 16)
+  int32_t npieces;         // basis operand pieces: 2 (fp32 basis: hi, lo) or 1 (bf16 basis)
 };
 
 // One unit of grouped work: matrix, block and two phase-specific indices.
@@ -110,6 +111,7 @@ struct StepArgs {
   float* stats;
   float beta1;
   float lr_s;             // lr * s
+  int32_t basis_bf16;     // multiply with bf16(Q) (bf16 basis storage)
   void* W[kMaxMatPerLaunch];
   const void* G[kMaxMatPerLaunch];
   int8_t* S[kMaxMatPerLaunch];
@@ -151,7 +153,8 @@ cudaError_t configure_step_tc(size_t smem_limit);
 cudaError_t launch_step_tc(const StepArgs& a, const TcArgs& t, int param_dtype, int grid,
                            size_t smem, cudaStream_t s);
 cudaError_t launch_pack_bases(const float* Q, unsigned char* qpack, const MatInfo* info,
-                              const Tile* items, int num_items, int grid, cudaStream_t s);
+                              const Tile* items, int num_items, int npieces, int grid,
+                              cudaStream_t s);
 size_t syrk_tc_stage_bytes(int max_k);
 int syrk_tc_stages(int max_k, size_t smem_limit);
 size_t syrk_tc_smem(int max_k, int stages);

@@ -76,6 +76,7 @@ step_ffma_kernel(const __grid_constant__ StepArgs a) {
           const int ll = e / kNC, cc = e % kNC;
           float v = 0.f;
           if (l0 + ll < k && jc + cc < k) v = Qb[(int64_t)(l0 + ll) * k + jc + cc];
+          if (a.basis_bf16) v = __bfloat162float(__float2bfloat16_rn(v));
           Qs[ll * kQS + cc] = v;
         }
         for (int e = tid; e < kTM * kKC; e += kThreads) {
@@ -130,6 +131,7 @@ step_ffma_kernel(const __grid_constant__ StepArgs a) {
           const int cc = e / kKC, jj = e % kKC;
           float v = 0.f;
           if (lc + cc < k && j0 + jj < k) v = Qb[(int64_t)(lc + cc) * k + j0 + jj];
+          if (a.basis_bf16) v = __bfloat162float(__float2bfloat16_rn(v));
           Qs[jj * kQS + cc] = v;
         }
         for (int e = tid; e < kTM * kKC; e += kThreads) {

@@ -124,6 +124,7 @@ step_tc_kernel(const __grid_constant__ StepArgs a, const __grid_constant__ TcArg
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t nbs = (uint32_t)t.nbstage;  // B stages of this launch
+  const bool two = t.npieces == 2;           // fp32 basis: hi and lo operand pieces
   if (threadIdx.x == 0) {
     for (int i = 0; i < kAStages; ++i) {
       mbar_init(&sh->a_full[i], 1);
@@ -164,7 +165,7 @@ step_tc_kernel(const __grid_constant__ StepArgs a, const __grid_constant__ TcArg
         const int k = mi.k, kpN = (k + 15) & ~15;
         const int nsub = (k + 7) / 8, nk32 = (k + 31) / 32;
         const unsigned char* qp = t.qpack + mi.qp_off + (int64_t)tl.blk * mi.qblk_bytes;
-        const unsigned char* qr = qp + (int64_t)nsub * 2 * kpN * 32;
+        const unsigned char* qr = qp + (int64_t)nsub * t.npieces * kpN * 32;
         const CUtensorMap* map = reinterpret_cast<const CUtensorMap*>(t.maps) + tl.mat;
         for (int kc = 0; kc < nk32; ++kc) {
           if (!mbar_wait(&sh->a_empty[as], ap ^ 1)) { raise(sh, t.err, 1); break; }
@@ -176,7 +177,7 @@ step_tc_kernel(const __grid_constant__ StepArgs a, const __grid_constant__ TcArg
             const int sub = kc * 4 + s4;
             if (sub >= nsub) break;
             if (!mbar_wait(&sh->b_empty[bs], bp ^ 1)) { raise(sh, t.err, 2); break; }
-            const uint32_t bytes = 2u * kpN * 32u;
+            const uint32_t bytes = (uint32_t)t.npieces * kpN * 32u;
             mbar_arrive_expect_tx(&sh->b_full[bs], bytes);
             bulk_load(b_buf + bs * t.bstage, qp + (int64_t)sub * bytes, bytes, &sh->b_full[bs]);
             if (++bs == nbs) { bs = 0; bp ^= 1; }
@@ -186,7 +187,7 @@ step_tc_kernel(const __grid_constant__ StepArgs a, const __grid_constant__ TcArg
         int64_t off = 0;
         for (int c0 = 0; c0 < kpN && !aborted(sh); c0 += kUCols) {
           const int nn = min(kUCols, kpN - c0);
-          const uint32_t bytes = 2u * nn * 32u;
+          const uint32_t bytes = (uint32_t)t.npieces * nn * 32u;
           for (int s = 0; s < kpN / 16; ++s) {
             if (!mbar_wait(&sh->b_empty[bs], bp ^ 1)) { raise(sh, t.err, 3); break; }
             mbar_arrive_expect_tx(&sh->b_full[bs], bytes);
@@ -245,18 +246,17 @@ step_tc_kernel(const __grid_constant__ StepArgs a, const __grid_constant__ TcArg
             const uint64_t dah = smem_desc(a_hi + s4 * 32, 16, 1024, kSw128);
             const uint64_t dal = smem_desc(a_lo + s4 * 32, 16, 1024, kSw128);
             const uint32_t first = (sub == 0) ? 0u : 1u;
+            // fp32 basis: Mh Qh + Mh Ql + Ml Qh; bf16 basis (exact in TF32): Mh Q + Ml Q
             {
               const uint64_t dbh = smem_desc(b_hi, 16, 256, kSw32);
-              const uint64_t dbl = smem_desc(b_lo, 16, 256, kSw32);
               mma_tf32_ss(tmem + cb, dah, dbh, id0, first);
-              mma_tf32_ss(tmem + cb, dah, dbl, id0, 1);
+              if (two) mma_tf32_ss(tmem + cb, dah, smem_desc(b_lo, 16, 256, kSw32), id0, 1);
               mma_tf32_ss(tmem + cb, dal, dbh, id0, 1);
             }
             if (n1a > 0) {
               const uint64_t dbh = smem_desc(b_hi + 256 * 32, 16, 256, kSw32);
-              const uint64_t dbl = smem_desc(b_lo + 256 * 32, 16, 256, kSw32);
               mma_tf32_ss(tmem + cb + 256, dah, dbh, id1, first);
-              mma_tf32_ss(tmem + cb + 256, dah, dbl, id1, 1);
+              if (two) mma_tf32_ss(tmem + cb + 256, dah, smem_desc(b_lo + 256 * 32, 16, 256, kSw32), id1, 1);
               mma_tf32_ss(tmem + cb + 256, dal, dbh, id1, 1);
             }
             tc_commit(&sh->b_empty[bs]);
@@ -292,7 +292,7 @@ step_tc_kernel(const __grid_constant__ StepArgs a, const __grid_constant__ TcArg
             const uint32_t b_hi = smem_u32(b_buf + bs * t.bstage);
             const uint32_t b_lo = b_hi + nn * 32;
             mma_f16_ts(d, tmem + cb + 8 * s, smem_desc(b_hi, 16, 256, kSw32), idr, s == 0 ? 0u : 1u);
-            mma_f16_ts(d, tmem + cb + 8 * s, smem_desc(b_lo, 16, 256, kSw32), idr, 1u);
+            if (two) mma_f16_ts(d, tmem + cb + 8 * s, smem_desc(b_lo, 16, 256, kSw32), idr, 1u);
             tc_commit(&sh->b_empty[bs]);
           }
           __syncwarp();
@@ -503,15 +503,17 @@ step_tc_kernel(const __grid_constant__ StepArgs a, const __grid_constant__ TcArg
 }
 
 // ---------------------------------------------------------------- packing
-// Q (row-major, column j = eigenvector j) -> the two operand images.
-//   project, K = l, N = j: per 8-wide K step s and piece (TF32 hi, lo),
+// Q (row-major, column j = eigenvector j) -> the two operand images, with
+// npieces = 2 (fp32 basis: hi and lo pieces) or 1 (bf16 basis, "Dobb",
+// Table 18: Q rounded once to bf16, exact in both TF32 and bf16).
+//   project, K = l, N = j: per 8-wide K step s and piece (TF32 hi[, lo]),
 //     kpN rows of 32 bytes (row n holds Q[8s .. 8s+7][n]), 32-byte swizzle;
 //   reconstruct, K = j, N = l: per 128-wide output chunk, per 16-wide K step
-//     and piece (bf16 hi, lo), nn rows of 32 bytes (row n holds
+//     and piece (bf16 hi[, lo]), nn rows of 32 bytes (row n holds
 //     Q[c0 + n][16s .. 16s+15]), 32-byte swizzle.
 __global__ void __launch_bounds__(256)
 pack_bases_kernel(const float* Q, unsigned char* qpack, const MatInfo* info, const Tile* items,
-                  int num_items) {
+                  int num_items, int npieces) {
   for (int w = blockIdx.x; w < num_items; w += gridDim.x) {
     const Tile tl = items[w];
     const MatInfo mi = info[tl.mat];
@@ -524,16 +526,16 @@ pack_bases_kernel(const float* Q, unsigned char* qpack, const MatInfo* info, con
     for (int e = threadIdx.x; e < np; e += blockDim.x) {
       const int kk = e & 7, n = (e >> 3) % kpN, s = (e >> 3) / kpN;
       const int l = 8 * s + kk;
-      const float q = (l < k && n < k) ? Qb[(int64_t)l * k + n] : 0.f;
+      float q = (l < k && n < k) ? Qb[(int64_t)l * k + n] : 0.f;
+      if (npieces == 1) q = __bfloat162float(__float2bfloat16_rn(q));
       const float h = ptx::tf32_rna(q);
-      const float lo = ptx::tf32_rna(q - h);
       const uint32_t off = ptx::swz_offset((uint32_t)(n * 32 + kk * 4), 1);
-      unsigned char* sub = img + (int64_t)s * 2 * kpN * 32;
+      unsigned char* sub = img + (int64_t)s * npieces * kpN * 32;
       *reinterpret_cast<float*>(sub + off) = h;
-      *reinterpret_cast<float*>(sub + kpN * 32 + off) = lo;
+      if (npieces == 2) *reinterpret_cast<float*>(sub + kpN * 32 + off) = ptx::tf32_rna(q - h);
     }
     // reconstruct image
-    unsigned char* rimg = img + (int64_t)nsub * 2 * kpN * 32;
+    unsigned char* rimg = img + (int64_t)nsub * npieces * kpN * 32;
     const int nr = kpN * kpN;  // (l, j) over the padded square
     for (int e = threadIdx.x; e < nr; e += blockDim.x) {
       const int l = e / kpN, j = e % kpN;
@@ -541,12 +543,12 @@ pack_bases_kernel(const float* Q, unsigned char* qpack, const MatInfo* info, con
       const int s = j / 16, jj = j % 16;
       const float q = (l < k && j < k) ? Qb[(int64_t)l * k + j] : 0.f;
       const __nv_bfloat16 h = __float2bfloat16_rn(q);
-      const __nv_bfloat16 lo = __float2bfloat16_rn(q - __bfloat162float(h));
-      const int64_t cbase = (int64_t)c0 * (kpN / 16) * 2 * 32;  // chunks before: 128 rows each
-      unsigned char* sub = rimg + cbase + (int64_t)s * 2 * nn * 32;
+      const int64_t cbase = (int64_t)c0 * (kpN / 16) * npieces * 32;  // chunks before: 128 rows each
+      unsigned char* sub = rimg + cbase + (int64_t)s * npieces * nn * 32;
       const uint32_t off = ptx::swz_offset((uint32_t)(nrow * 32 + jj * 2), 1);
       *reinterpret_cast<__nv_bfloat16*>(sub + off) = h;
-      *reinterpret_cast<__nv_bfloat16*>(sub + nn * 32 + off) = lo;
+      if (npieces == 2)
+        *reinterpret_cast<__nv_bfloat16*>(sub + nn * 32 + off) = __float2bfloat16_rn(q - __bfloat162float(h));
     }
   }
 }
@@ -599,9 +601,9 @@ cudaError_t launch_step_tc(const StepArgs& a, const TcArgs& t, int param_dtype, 
 }
 
 cudaError_t launch_pack_bases(const float* Q, unsigned char* qpack, const MatInfo* info,
-                              const Tile* items, int num_items, int grid, cudaStream_t s) {
+                              const Tile* items, int num_items, int npieces, int grid, cudaStream_t s) {
   if (num_items <= 0) return cudaSuccess;
-  pack_bases_kernel<<<grid, 256, 0, s>>>(Q, qpack, info, items, num_items);
+  pack_bases_kernel<<<grid, 256, 0, s>>>(Q, qpack, info, items, num_items, npieces);
   return cudaGetLastError();
 }
 

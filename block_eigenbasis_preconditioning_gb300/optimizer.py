@@ -27,12 +27,14 @@ class Dobb:
     Arguments follow the C ABI's dobb_create: B blocks per matrix, beta1,
     beta2, refresh_period (T, 0 = never automatic), scale_s (s in
     W <- W - lr s U), param_dtype of W / G and act_dtype of X ("f32" or
-    "bf16")."""
+    "bf16"), basis_dtype of the basis the update multiplies with ("f32", or
+    "bf16" as in the pages' principal setting)."""
 
     def __init__(self, shapes: Sequence[Tuple[int, int]], B: int, beta1: float = 0.95,
                  beta2: float = 0.99, refresh_period: int = 10, scale_s: float = 1.0,
                  param_dtype: str = "f32", act_dtype: str = "f32",
-                 device: Optional[torch.device] = None, stream: Optional[torch.cuda.Stream] = None):
+                 device: Optional[torch.device] = None, stream: Optional[torch.cuda.Stream] = None,
+                 basis_dtype: str = "f32"):
         self.lib = load_library()
         self.shapes = [(int(m), int(n)) for m, n in shapes]
         self.B = int(B)
@@ -54,6 +56,9 @@ class Dobb:
                                        ctypes.c_size_t(nbytes), _stream_ptr(stream)))
         self.handle = h
         self.num_blocks = int(self.lib.dobb_num_blocks(h))
+        self.basis_dtype = basis_dtype
+        if basis_dtype != "f32":
+            check(self.lib.dobb_set_basis_dtype(h, DTYPES[basis_dtype], _stream_ptr(stream)))
 
     # -- phases --------------------------------------------------------------
     def accumulate(self, X: Sequence[Optional[torch.Tensor]], stream=None) -> None:

@@ -134,6 +134,16 @@ dobb_status dobb_step_with_signs(dobb_handle h, void* const* W, const void* cons
 dobb_status dobb_get_step(dobb_handle h, int64_t* t);
 dobb_status dobb_set_step(dobb_handle h, int64_t t);
 
+/* Precision of the basis the update multiplies with ("Dobb", Table 18:
+ * fp32 moment accumulation with a bf16 basis is the principal setting).
+ * DOBB_F32 (default): C_b = M_b Q_b and U_b = S_b Q_b^T with the fp32 basis.
+ * DOBB_BF16: every entry of Q_b is rounded once to bf16 (nearest, ties to
+ * even) and the products use that basis at fp32 accuracy.  The eigensolver
+ * keeps the fp32 basis as its warm start either way.  Re-packs the
+ * tensor-core operand images on `stream`; DOBB_ERR_INVALID_ARG for another
+ * dtype. */
+dobb_status dobb_set_basis_dtype(dobb_handle h, dobb_dtype basis_dtype, void* stream);
+
 /* Eigensolver controls: sweep cap (default 40) and the convergence
  * threshold, the relative off-diagonal norm ||off(B)||_F / ||B||_F that the
  * last sweep of B = V^T A V may leave (0 = default 2e-6). */

@@ -95,9 +95,12 @@ def check_bases(opt, A_ref_list, matrices=None):
     return worst
 
 
-def check_update(W_prev, M_prev, G, Q_gpu, S_gpu, W_gpu, M_gpu, beta1, lr, s, param_dtype, k):
-    """Score one matrix's update against the oracle run with the GPU basis."""
-    ref = O.update_from_bases(W_prev, M_prev, G, Q_gpu, beta1, lr, s, param_dtype)
+def check_update(W_prev, M_prev, G, Q_gpu, S_gpu, W_gpu, M_gpu, beta1, lr, s, param_dtype, k,
+                 basis_dtype="f32"):
+    """Score one matrix's update against the oracle run with the GPU basis
+    (rounded by the oracle itself when the basis is stored in bf16)."""
+    ref = O.update_from_bases(W_prev, M_prev, G, Q_gpu, beta1, lr, s, param_dtype,
+                              basis_dtype=basis_dtype)
     # momentum
     dm = np.abs(M_gpu - ref["M"]).max() / max(np.abs(ref["M"]).max(), 1e-30)
     assert dm <= 1e-6, f"momentum relative error {dm:.3e}"
@@ -106,7 +109,8 @@ def check_update(W_prev, M_prev, G, Q_gpu, S_gpu, W_gpu, M_gpu, beta1, lr, s, pa
     assert sa["outside_band"] == 0, f"{sa['outside_band']} sign flips outside the band"
     assert sa["fraction"] < TOL_SIGN_FRAC, f"sign disagreement fraction {sa['fraction']:.2e}"
     # parameters, scored with the GPU's signs at the tolerated entries
-    ref2 = O.update_from_bases(W_prev, M_prev, G, Q_gpu, beta1, lr, s, "f32", S_override=S_gpu)
+    ref2 = O.update_from_bases(W_prev, M_prev, G, Q_gpu, beta1, lr, s, "f32", S_override=S_gpu,
+                               basis_dtype=basis_dtype)
     if param_dtype == "f32":
         e = MX.w_rel_error(W_gpu, ref2["W"])
         assert e <= TOL_W, f"W max relative error {e:.3e}"

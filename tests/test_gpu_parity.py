@@ -162,6 +162,39 @@ def test_update_matches_oracle_with_gpu_basis(pdt, shapes, B):
             assert abs(st[opt.block_offset(i) + b, 0] - nnz) <= 1e-4 * max(nnz, 1)
 
 
+@pytest.mark.parametrize("pdt", ["f32", "bf16"])
+@pytest.mark.parametrize("shapes,B", [
+    ([(37, 96)], 2),            # k = 48, tensor cores
+    ([(130, 200)], 2),          # k = 100, tensor cores
+    ([(200, 400)], 1),          # k = 400, tensor cores
+    ([(9, 15)], 5),             # k = 3, FP32 path
+])
+def test_update_with_bf16_basis_matches_oracle(pdt, shapes, B):
+    """[Dobb, Table 18] bf16 basis storage: the update multiplies with the
+    basis rounded once to bf16; scored against the oracle with the GPU's
+    basis, rounded by the oracle."""
+    N = max(256, 4 * max(n // B for _, n in shapes))
+    Xs, Gs, Ws = make_problem(shapes, N, 0.2, seed=14, param_dtype=pdt)
+    opt = _dobb(shapes, B, beta1=0.9, beta2=0.95, refresh_period=1, scale_s=1.5, param_dtype=pdt,
+                basis_dtype="bf16")
+    Wd = [to_dev(w, pdt) for w in Ws]
+    Gd = [to_dev(g, pdt) for g in Gs]
+    Sd = [torch.zeros(w.shape, dtype=torch.int8, device="cuda") for w in Ws]
+    W_prev = [to_np(w) for w in Wd]
+    opt.accumulate([to_dev(x, "f32") for x in Xs])
+    opt.step(Wd, Gd, 0.02, signs=Sd)
+    torch.cuda.synchronize()
+    for i, (m, n) in enumerate(shapes):
+        Q = to_np(opt.tensor("bases", i))
+        check_update(W_prev[i], np.zeros((m, n)), to_np(Gd[i]), Q, to_np(Sd[i]), to_np(Wd[i]),
+                     to_np(opt.tensor("momentum", i)), 0.9, 0.02, 1.5, pdt, n // B, basis_dtype="bf16")
+    # the rounding acts: the fp32-basis update differs somewhere
+    Q = to_np(opt.tensor("bases", 0))
+    m, n = shapes[0]
+    r32 = O.update_from_bases(W_prev[0], np.zeros((m, n)), to_np(Gd[0]), Q, 0.9, 0.02, 1.5, "f32")
+    assert np.abs(r32["W"] - to_np(Wd[0])).max() > 0
+
+
 def test_identity_basis_gives_sign_of_momentum():
     shapes = [(33, 40)]
     _, Gs, Ws = make_problem(shapes, 8, 0.5, seed=5)
