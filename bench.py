@@ -198,7 +198,7 @@ def _traffic_for(kernel_key):
             t = json.load(f)
         e = t.get(kernel_key)
         if e and e.get("source_sha") == _kernel_source_sha(e.get("source")):
-            return e.get("bytes_per_launch")
+            return e.get("bytes_per_step")
     except Exception:
         pass
     return None
