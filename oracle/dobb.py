@@ -61,6 +61,8 @@ __all__ = [
     "lapack_eigh",
     "canonicalize",
     "refresh_bases",
+    "cholesky_qr",
+    "orthogonal_iteration",
     "momentum",
     "project",
     "sign",
@@ -197,6 +199,35 @@ def refresh_bases(A: np.ndarray, method: str = "auto", jacobi_max_k: int = 48):
     return Q, lam
 
 
+def cholesky_qr(T: np.ndarray):
+    """QR factorisation through the Gram matrix ([Dobb, Table 16]: the
+    "Cholesky" QR routine): R = chol(T^T T) upper triangular with positive
+    diagonal, Q = T R^{-1}.  Mathematically the QR factorisation of T whose R
+    has a positive diagonal."""
+    T = _f64(T)
+    L = np.linalg.cholesky(T.T @ T)          # T^T T = L L^T, L lower
+    Q = np.linalg.solve(L, T.T).T            # Q^T = L^{-1} T^T
+    return Q, L.T
+
+
+def orthogonal_iteration(A: np.ndarray, Q0: np.ndarray, steps: int = 1):
+    """Refresh by orthogonal (subspace) iteration started from the current
+    basis ([Dobb, Table 15]: "k = 1" orthogonal-iteration steps per refresh is
+    the principal setting; Table 16: Cholesky QR).  For every block,
+    `steps` times: T = A_b Q_b, Q_b = T R^{-1} with R = chol(T^T T).
+    Returns Q (B, k, k) and the Rayleigh quotients diag(Q_b^T A_b Q_b)."""
+    A = _f64(A)
+    Q = _f64(Q0).copy()
+    Bn, k, _ = A.shape
+    lam = np.empty((Bn, k))
+    for b in range(Bn):
+        Ab = 0.5 * (A[b] + A[b].T)
+        for _ in range(steps):
+            Q[b], _ = cholesky_qr(Ab @ Q[b])
+        lam[b] = np.einsum("ij,ij->j", Q[b], Ab @ Q[b])
+    return Q, lam
+
+
 # ---------------------------------------------------------------------------
 # (3) momentum, project, sign, reconstruct, apply   [Dobb, Abstract; Table 9]
 # ---------------------------------------------------------------------------
@@ -309,6 +340,8 @@ class DobbOracle:
     param_dtype: str = "f32"
     eig_method: str = "auto"
     basis_dtype: str = "f32"
+    refresh_method: str = "eigh"   # "eigh" (exact) or "orth" (orthogonal iteration)
+    orth_steps: int = 1
 
     def __post_init__(self):
         self.t = 0
@@ -331,7 +364,10 @@ class DobbOracle:
 
     def refresh(self) -> None:
         for i in range(len(self.shapes)):
-            self.Q[i], self.lam[i] = refresh_bases(self.A[i], self.eig_method)
+            if self.refresh_method == "orth":
+                self.Q[i], self.lam[i] = orthogonal_iteration(self.A[i], self.Q[i], self.orth_steps)
+            else:
+                self.Q[i], self.lam[i] = refresh_bases(self.A[i], self.eig_method)
 
     def step(self, W_list, G_list, lr: float, keep_parts: bool = False):
         """Refresh if due, then update every matrix.  Returns the new W list

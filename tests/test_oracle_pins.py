@@ -225,6 +225,55 @@ def test_invariances():
 
 
 # --------------------------------------------------------------------------
+# orthogonal-iteration refresh ([Dobb, Table 15] principal, Table 16 Cholesky QR)
+# --------------------------------------------------------------------------
+
+def test_cholesky_qr_is_the_positive_diagonal_householder_qr():
+    rng = np.random.default_rng(31)
+    for k in (2, 5, 40):
+        T = rng.standard_normal((k, k)) + 3 * np.eye(k)
+        Q, R = O.cholesky_qr(T)
+        Qh, Rh = np.linalg.qr(T)                    # Householder (LAPACK geqrf)
+        d = np.sign(np.diag(Rh))
+        Qh, Rh = Qh * d[None, :], Rh * d[:, None]
+        assert np.abs(Q - Qh).max() < 1e-10 and np.abs(R - Rh).max() < 1e-10
+        assert np.all(np.diag(R) > 0) and np.allclose(np.tril(R, -1), 0)
+
+
+def test_cholesky_qr_two_by_two_by_hand():
+    a, b, c, d = 3.0, 1.0, -2.0, 4.0
+    T = np.array([[a, b], [c, d]])
+    r11 = math.hypot(a, c)
+    q1 = np.array([a, c]) / r11
+    r12 = q1 @ np.array([b, d])
+    w = np.array([b, d]) - r12 * q1
+    r22 = np.linalg.norm(w)
+    Q, R = O.cholesky_qr(T)
+    assert np.allclose(Q[:, 0], q1, atol=1e-14) and np.allclose(Q[:, 1], w / r22, atol=1e-14)
+    assert np.allclose(R, [[r11, r12], [0.0, r22]], atol=1e-14)
+
+
+def test_orthogonal_iteration_fixed_point_and_convergence():
+    rng = np.random.default_rng(32)
+    k = 12
+    A = np.stack([I.spd_with_gap(k, rng, cond=50.0)[0] for _ in range(2)])
+    Qe, le = O.refresh_bases(A, "lapack")
+    # exact eigenvectors (descending, PSD) are a fixed point, eigenvalues the quotients
+    Q1, l1 = O.orthogonal_iteration(A, Qe, 1)
+    assert np.abs(Q1 - Qe).max() < 1e-10 and np.abs(l1 - le).max() < 1e-10 * le.max()
+    # from a generic start, many steps converge to the eigenvectors (up to sign)
+    Q0 = np.stack([I.haar_orthogonal(k, rng) for _ in range(2)])
+    Qn, ln = O.orthogonal_iteration(A, Q0, 3000)
+    for b in range(2):
+        assert np.abs(np.abs(Qn[b].T @ Qe[b]) - np.eye(k)).max() < 1e-8
+        assert np.abs(ln[b] - le[b]).max() < 1e-10 * le[b].max()
+    # one step is one QR of A Q0
+    Qs, _ = O.orthogonal_iteration(A, Q0, 1)
+    Qr, _ = O.cholesky_qr(0.5 * (A[0] + A[0].T) @ Q0[0])
+    assert np.abs(Qs[0] - Qr).max() < 1e-14
+
+
+# --------------------------------------------------------------------------
 # bf16 basis storage ([Dobb, Table 18]: the principal precision setting)
 # --------------------------------------------------------------------------
 
