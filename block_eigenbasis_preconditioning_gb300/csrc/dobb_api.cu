@@ -285,6 +285,8 @@ struct dobb_ctx {
   int max_sweeps = 40;
   float tol = 0.f;
   bool basis_bf16 = false;  // the update multiplies with bf16(Q)
+  int refresh_method = DOBB_REFRESH_EIGH;
+  int orth_steps = 1;
   int sm_count = 1;
   size_t smem_limit = 0;
   size_t smem_per_sm = 0;
@@ -335,7 +337,29 @@ dobb_status do_pack(dobb_handle h, cudaStream_t s) {
   return DOBB_OK;
 }
 
+dobb_status do_refresh_orth(dobb_handle h, cudaStream_t s) {
+  for (const Chunk& ch : h->wl.chunks) {
+    if (ch.eig_n == 0) continue;
+    EigArgs a{};
+    a.info = h->dinfo();
+    a.tiles = h->dtiles() + ch.eig_off;
+    a.num_tiles = ch.eig_n;
+    a.A = h->A();
+    a.Q = h->Q();
+    a.lam = h->lam();
+    a.scratch = h->scratch();
+    a.flags = h->flags();
+    a.stats = h->stats();
+    const int g = std::max(1, std::min(ch.eig_n, h->sm_count));
+    cudaError_t e = launch_orth(a, h->orth_steps, g, s);
+    if (e != cudaSuccess) return fail(DOBB_ERR_CUDA, "orthogonal-iteration launch: %s", cudaGetErrorString(e));
+    ++h->launches;
+  }
+  return do_pack(h, s);
+}
+
 dobb_status do_refresh(dobb_handle h, cudaStream_t s) {
+  if (h->refresh_method == DOBB_REFRESH_ORTH) return do_refresh_orth(h, s);
   // blocks whose solver fits in half of an SM's shared memory run two CTAs per SM
   const size_t half = h->smem_per_sm / 2 > 2048 ? h->smem_per_sm / 2 - 2048 : 0;
   for (const Chunk& ch : h->wl.chunks) {
@@ -524,7 +548,7 @@ dobb_status dobb_create(dobb_handle* out, int num_matrices, const int64_t* m, co
     return fail(DOBB_ERR_CUDA, "device query: %s", cudaGetErrorString(e));
   }
   h->smem_limit = (size_t)optin - 2048;  // room for static shared memory
-  if ((e = configure_jacobi(h->smem_limit)) != cudaSuccess ||
+  if ((e = configure_jacobi(h->smem_limit)) != cudaSuccess || (e = configure_orth()) != cudaSuccess ||
       (e = configure_step(h->smem_limit)) != cudaSuccess ||
       (e = configure_step_tc(h->smem_limit)) != cudaSuccess ||
       (e = configure_syrk_tc(h->smem_limit)) != cudaSuccess) {
@@ -769,6 +793,16 @@ dobb_status dobb_set_basis_dtype(dobb_handle h, dobb_dtype basis_dtype, void* st
   h->basis_bf16 = basis_dtype == DOBB_BF16;
   // the tensor-core operand images hold the basis in the chosen precision
   return do_pack(h, static_cast<cudaStream_t>(stream));
+}
+
+dobb_status dobb_set_refresh(dobb_handle h, int method, int steps) {
+  if (!h) return fail(DOBB_ERR_INVALID_ARG, "NULL handle");
+  if (method != DOBB_REFRESH_EIGH && method != DOBB_REFRESH_ORTH)
+    return fail(DOBB_ERR_INVALID_ARG, "refresh method must be DOBB_REFRESH_EIGH or DOBB_REFRESH_ORTH");
+  if (steps < 1) return fail(DOBB_ERR_INVALID_ARG, "orthogonal-iteration steps must be >= 1");
+  h->refresh_method = method;
+  h->orth_steps = steps;
+  return DOBB_OK;
 }
 
 dobb_status dobb_set_jacobi(dobb_handle h, int max_sweeps, float tol) {

@@ -143,6 +143,10 @@ size_t jacobi_smem_for(int k, size_t budget);
 int jacobi_ctas_per_sm();
 size_t step_smem_for(int k);
 cudaError_t configure_jacobi(size_t smem_limit);
+// orthogonal-iteration refresh (steps Cholesky-QR iterations per block)
+cudaError_t launch_orth(const EigArgs& a, int steps, int grid, cudaStream_t s);
+size_t orth_smem_bytes();
+cudaError_t configure_orth();
 cudaError_t configure_step(size_t smem_limit);
 size_t step_tc_smem(int max_k, int nbstage);
 size_t step_tc_bstage(int max_k);

@@ -134,6 +134,22 @@ dobb_status dobb_step_with_signs(dobb_handle h, void* const* W, const void* cons
 dobb_status dobb_get_step(dobb_handle h, int64_t* t);
 dobb_status dobb_set_step(dobb_handle h, int64_t t);
 
+/* Refresh method ("Dobb", Table 15).
+ * DOBB_REFRESH_EIGH (default): complete eigendecomposition of every block,
+ *   Q_b with A_b = Q_b Lambda_b Q_b^T (two-sided Jacobi), columns by
+ *   descending eigenvalue.
+ * DOBB_REFRESH_ORTH: `steps` orthogonal-iteration steps from the current
+ *   basis (one step is the pages' principal setting): Q_b <- T R^{-1} with
+ *   T = A_b Q_b and R = chol(T^T T) (Table 16: Cholesky QR; computed as
+ *   CholeskyQR2 in fp32, with a shifted first pass when T^T T is not
+ *   numerically positive definite); Lambda_b holds the Rayleigh quotients
+ *   diag(Q_b^T A_b Q_b).  A block whose QR fails keeps its basis and gets
+ *   DOBB_FLAG_NOT_CONVERGED.
+ * DOBB_ERR_INVALID_ARG for another method or steps < 1.  Takes effect at the
+ * next refresh. */
+enum { DOBB_REFRESH_EIGH = 0, DOBB_REFRESH_ORTH = 1 };
+dobb_status dobb_set_refresh(dobb_handle h, int method, int steps);
+
 /* Precision of the basis the update multiplies with ("Dobb", Table 18:
  * fp32 moment accumulation with a bf16 basis is the principal setting).
  * DOBB_F32 (default): C_b = M_b Q_b and U_b = S_b Q_b^T with the fp32 basis.

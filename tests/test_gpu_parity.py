@@ -343,3 +343,113 @@ def test_tensor_core_update_matches_oracle_multi_step():
     each scored against the oracle run with the GPU basis and GPU signs."""
     shapes = [(256, 1600), (160, 6400)]
     _run(shapes, 16, 1024, 0.2, steps=3, T=2, pdt="bf16", adt="bf16", seed=22)
+
+
+# --------------------------------------------------------------------------
+# (f1) orthogonal-iteration refresh ([Dobb, Table 15] principal, Table 16)
+# --------------------------------------------------------------------------
+
+def _orth_case(k, B, cond, seed):
+    rng = np.random.default_rng(seed)
+    A = np.stack([I.spd_with_gap(k, rng, cond=cond)[0] if k > 1 else np.array([[0.7]])
+                  for _ in range(B)]).astype(np.float32).astype(np.float64)
+    Q0 = np.stack([I.haar_orthogonal(k, rng) for _ in range(B)]).astype(np.float32).astype(np.float64)
+    return A, Q0
+
+
+def _load(opt, A, Q0, k, B):
+    opt.tensor("moments", 0).copy_(torch.from_numpy(A.astype(np.float32)).view(B, k, k))
+    opt.tensor("bases", 0).copy_(torch.from_numpy(Q0.astype(np.float32)).view(B, k, k))
+
+
+@pytest.mark.parametrize("k", [1, 3, 31, 48, 65, 100, 130, 400])
+def test_orth_refresh_is_one_cholesky_qr_step(k):
+    """One step: Q = T R^{-1}, T = A Q0.  Scored by what fixes the QR factor of
+    T: orthonormal columns, Q^T T upper triangular with a positive diagonal
+    (backward stable, independent of kappa(T)), and the forward error against
+    the fp64 oracle within the fp32 perturbation bound ~ kappa k eps."""
+    B, cond = 2, 50.0
+    A, Q0 = _orth_case(k, B, cond, seed=100 + k)
+    opt = _dobb([(4, B * k)], B, refresh_period=0, refresh="orth", orth_steps=1)
+    _load(opt, A, Q0, k, B)
+    opt.refresh()
+    torch.cuda.synchronize()
+    Q = to_np(opt.tensor("bases", 0))
+    lam = to_np(opt.tensor("eigvals", 0))
+    Qr, lr = O.orthogonal_iteration(A, Q0, 1)
+    assert np.all(opt.block_flags() == 0)
+    for b in range(B):
+        T = A[b] @ Q0[b]
+        R = Q[b].T @ T
+        assert np.linalg.norm(Q[b].T @ Q[b] - np.eye(k)) <= 1e-5 * max(1.0, np.sqrt(k))
+        assert np.linalg.norm(np.tril(R, -1)) <= 1e-5 * np.linalg.norm(T)
+        assert np.all(np.diag(R) > 0)
+        assert np.linalg.norm(Q[b] - Qr[b]) <= 20 * cond * k * 2.0 ** -24
+        assert np.abs(lam[b] - lr[b]).max() <= 1e-5 * np.abs(lr[b]).max()
+
+
+def test_orth_refresh_converges_to_the_eigenbasis():
+    k, B = 48, 2
+    A, Q0 = _orth_case(k, B, 20.0, seed=7)
+    opt = _dobb([(4, B * k)], B, refresh_period=0, refresh="orth", orth_steps=400)
+    _load(opt, A, Q0, k, B)
+    opt.refresh()
+    torch.cuda.synchronize()
+    Q = to_np(opt.tensor("bases", 0))
+    lam = to_np(opt.tensor("eigvals", 0))
+    Qe, le = O.refresh_bases(A, "lapack")
+    for b in range(B):
+        assert np.abs(np.abs(Q[b].T @ Qe[b]) - np.eye(k)).max() <= 1e-4
+        assert np.abs(lam[b] - le[b]).max() <= 1e-5 * le[b].max()
+
+
+def test_orth_refresh_shifted_pass_on_ill_conditioned_blocks():
+    """kappa(A) = 1e6: the fp32 Gram matrix of T = A Q0 is not positive
+    definite, so shifted passes come first (each lowers kappa by ~0.1 at
+    k = 100); the factor is still orthonormal and Q^T T upper triangular to
+    fp32 level."""
+    k, B = 100, 2
+    A, Q0 = _orth_case(k, B, 1e6, seed=8)
+    opt = _dobb([(4, B * k)], B, refresh_period=0, refresh="orth", orth_steps=1)
+    _load(opt, A, Q0, k, B)
+    opt.refresh()
+    torch.cuda.synchronize()
+    Q = to_np(opt.tensor("bases", 0))
+    assert np.all(opt.block_flags() == 0)
+    st = opt.block_stats()
+    assert np.all(st[:, 3] >= 1.0)  # shifted passes were taken
+    for b in range(B):
+        T = A[b] @ Q0[b]
+        assert np.linalg.norm(Q[b].T @ Q[b] - np.eye(k)) <= 1e-5 * np.sqrt(k)
+        assert np.linalg.norm(np.tril(Q[b].T @ T, -1)) <= 1e-4 * np.linalg.norm(T)
+
+
+@pytest.mark.parametrize("pdt", ["f32", "bf16"])
+def test_run_with_orth_refresh_matches_oracle_updates(pdt):
+    """A short run refreshing by one orthogonal-iteration step every 2 steps:
+    moments against the oracle, every update against the oracle with the
+    GPU's basis."""
+    shapes, B = [(96, 200), (64, 128)], 2
+    rng = np.random.default_rng(21)
+    opt = _dobb(shapes, B, beta1=0.9, beta2=0.9, refresh_period=2, scale_s=1.0, param_dtype=pdt,
+                refresh="orth", orth_steps=1)
+    orc = O.DobbOracle(shapes, B, beta1=0.9, beta2=0.9, refresh_period=0, param_dtype=pdt)
+    Wd = [to_dev(I.weights(m, n, rng, dtype=pdt), pdt) for m, n in shapes]
+    for t in range(5):
+        Xs = [I.activations(512, n, 0.3, rng) for _, n in shapes]
+        Gs = [I.gradients(m, X, rng, dtype=pdt) for (m, _), X in zip(shapes, Xs)]
+        Gd = [to_dev(g, pdt) for g in Gs]
+        Sd = [torch.zeros(w.shape, dtype=torch.int8, device="cuda") for w in Wd]
+        W_prev = [to_np(w) for w in Wd]
+        M_prev = [m.copy() for m in orc.M]
+        opt.accumulate([to_dev(x, "f32") for x in Xs])
+        orc.accumulate(Xs)
+        opt.step(Wd, Gd, 0.02, signs=Sd)
+        torch.cuda.synchronize()
+        check_moments(opt, orc)
+        for i, (m, n) in enumerate(shapes):
+            Q = to_np(opt.tensor("bases", i))
+            r = check_update(W_prev[i], M_prev[i], to_np(Gd[i]), Q, to_np(Sd[i]), to_np(Wd[i]),
+                             to_np(opt.tensor("momentum", i)), 0.9, 0.02, 1.0, pdt, n // B)
+            orc.M[i] = O.momentum(M_prev[i], to_np(Gd[i]), 0.9)
+            assert np.linalg.norm(Q[0].T @ Q[0] - np.eye(n // B)) <= 1e-5 * np.sqrt(n // B)
