@@ -75,6 +75,7 @@ struct Chunk {
 
 struct SyrkChunk {
   int mat_base = 0, mat_end = 0, off = 0, n = 0, max_k = 8;
+  int small = 0;  // index (within the chunk) of the first tile with k <= kTcSmallK
 };
 
 // Work lists of all phases, in the order they are stored on the device.
@@ -213,6 +214,9 @@ WorkLists build_work(int num, const int64_t* m, const int64_t* n, int B) {
       std::stable_sort(v.begin(), v.end(), [](auto& x, auto& y) { return x.first > y.first; });
       sc.off = (int)wl.tiles.size();
       sc.n = (int)v.size();
+      sc.small = sc.n;
+      for (int j = 0; j < sc.n; ++j)
+        if (v[j].first <= kTcSmallK) { sc.small = j; break; }
       for (auto& e : v) wl.tiles.push_back(e.second);
       wl.syrk_tc.push_back(sc);
       c0 = c1;
@@ -699,16 +703,29 @@ dobb_status dobb_accumulate_moments(dobb_handle h, const void* const* X, const i
         }
         a->maps[slot] = h->xmaps[i];
       }
-      a->stages = syrk_tc_stages(sc.max_k, h->smem_limit - 1024);
-      a->stage_bytes = (int32_t)syrk_tc_stage_bytes(sc.max_k);
-      const size_t smem = syrk_tc_smem(sc.max_k, a->stages);
-      const int g = std::max(1, std::min(sc.n, h->sm_count));
-      cudaError_t e = launch_syrk_tc(*a, g, smem, s);
-      if (e != cudaSuccess) {
-        delete a;
-        return fail(DOBB_ERR_CUDA, "tensor-core accumulate launch: %s", cudaGetErrorString(e));
+      // two launches: blocks wider than kTcSmallK, then the narrow ones with
+      // stages sized for them (more tokens in flight)
+      for (int part = 0; part < 2; ++part) {
+        const int lo = part == 0 ? 0 : sc.small, hi = part == 0 ? sc.small : sc.n;
+        if (hi <= lo) continue;
+        int kmax = 8;
+        for (int j = lo; j < hi; ++j) {
+          const Tile& tl = h->wl.tiles[sc.off + j];
+          kmax = std::max(kmax, (int)(h->n[tl.mat] / h->B));
+        }
+        a->tiles = h->dtiles() + sc.off + lo;
+        a->num_tiles = hi - lo;
+        a->stages = syrk_tc_stages(kmax, h->smem_limit - 1024);
+        a->stage_bytes = (int32_t)syrk_tc_stage_bytes(kmax);
+        const size_t smem = syrk_tc_smem(kmax, a->stages);
+        const int g = std::max(1, std::min(hi - lo, h->sm_count));
+        cudaError_t e = launch_syrk_tc(*a, g, smem, s);
+        if (e != cudaSuccess) {
+          delete a;
+          return fail(DOBB_ERR_CUDA, "tensor-core accumulate launch: %s", cudaGetErrorString(e));
+        }
+        ++h->launches;
       }
-      ++h->launches;
     }
     delete a;
     if (h->wl.syrk_rest_n == 0) return DOBB_OK;

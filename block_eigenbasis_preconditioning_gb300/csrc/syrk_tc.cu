@@ -32,8 +32,10 @@ constexpr int kTok = 64;            // tokens per stage
 constexpr int kBoxBytes = kTok * 128;  // 64 tokens x 64 bf16 features
 constexpr uint32_t kTmemCols = 512;
 
+constexpr int kMaxSyStages = 16;
+
 struct SySmem {
-  uint64_t full[8], empty[8];
+  uint64_t full[kMaxSyStages], empty[kMaxSyStages];
   uint64_t d_full, d_free;
   uint32_t tmem_base;
   int abort;
@@ -225,7 +227,7 @@ size_t syrk_tc_stage_bytes(int max_k) {
 int syrk_tc_stages(int max_k, size_t smem_limit) {
   const size_t sb = syrk_tc_stage_bytes(max_k);
   int st = (int)((smem_limit - 2048) / sb);
-  return std::max(2, std::min(8, st));
+  return std::max(2, std::min(kMaxSyStages, st));
 }
 
 size_t syrk_tc_smem(int max_k, int stages) {
