@@ -67,6 +67,8 @@ __all__ = [
     "project",
     "sign",
     "reconstruct",
+    "l2_normalize_columns",
+    "normalize",
     "apply_update",
     "round_to_bf16",
     "basis_for_update",
@@ -253,6 +255,28 @@ def sign(C: np.ndarray) -> np.ndarray:
     return np.sign(_f64(C))
 
 
+def l2_normalize_columns(C: np.ndarray) -> np.ndarray:
+    """Column l2 normalisation of the coefficients, "Dobb-l2" ([Dobb, Table 11];
+    Table 9 gives its raw update the same ||O||_F^2 = n as Dobb's sign).  Each
+    column of C (over all m rows) is scaled to l2 norm sqrt(m), so that with
+    O = U / sqrt(m) as for the sign update every nonzero column of O has unit
+    norm; a zero column stays zero."""
+    C = _f64(C)
+    m = C.shape[0]
+    nrm = np.sqrt((C ** 2).sum(axis=0))
+    scale = np.where(nrm > 0, math.sqrt(m) / np.where(nrm > 0, nrm, 1.0), 0.0)
+    return C * scale[None, :]
+
+
+def normalize(C: np.ndarray, norm: str = "sign") -> np.ndarray:
+    """The coefficient normalisation: "sign" (Dobb, l_inf) or "l2" (Dobb-l2)."""
+    if norm == "sign":
+        return sign(C)
+    if norm == "l2":
+        return l2_normalize_columns(C)
+    raise ValueError(f"norm {norm!r}")
+
+
 def reconstruct(S: np.ndarray, Q: np.ndarray) -> np.ndarray:
     """U_b = S_b Q_b^T: map the normalised coefficients back to the input
     axis; U = [U_1 ... U_B] along the columns."""
@@ -305,16 +329,17 @@ def basis_for_update(Q: np.ndarray, basis_dtype: str = "f32") -> np.ndarray:
 
 def update_from_bases(W, M, G, Q, beta1: float, lr: float, s: float,
                       param_dtype: str = "f32", S_override: Optional[np.ndarray] = None,
-                      basis_dtype: str = "f32"):
+                      basis_dtype: str = "f32", norm: str = "sign"):
     """One update of a single matrix with given block bases Q (B, k, k).
     Returns dict with the new M, C, S, U and W.  `S_override` substitutes a
     given sign matrix (used to score a second implementation's signs at the
     entries where the sign is numerically undetermined).  `basis_dtype`
-    selects the stored precision of the basis (see `basis_for_update`)."""
+    selects the stored precision of the basis (see `basis_for_update`), `norm`
+    the coefficient normalisation (see `normalize`)."""
     Qu = basis_for_update(Q, basis_dtype)
     Mn = momentum(M, G, beta1)
     C = project(Mn, Qu)
-    S = sign(C) if S_override is None else _f64(S_override)
+    S = normalize(C, norm) if S_override is None else _f64(S_override)
     U = reconstruct(S, Qu)
     Wn = apply_update(W, U, lr, s, param_dtype)
     return {"M": Mn, "C": C, "S": S, "U": U, "W": Wn}
@@ -342,6 +367,7 @@ class DobbOracle:
     basis_dtype: str = "f32"
     refresh_method: str = "eigh"   # "eigh" (exact) or "orth" (orthogonal iteration)
     orth_steps: int = 1
+    norm: str = "sign"             # "sign" (Dobb) or "l2" (Dobb-l2)
 
     def __post_init__(self):
         self.t = 0
@@ -377,7 +403,8 @@ class DobbOracle:
         out_W, parts = [], []
         for i, (W, G) in enumerate(zip(W_list, G_list)):
             r = update_from_bases(W, self.M[i], G, self.Q[i], self.beta1, lr,
-                                  self.scale_s, self.param_dtype, basis_dtype=self.basis_dtype)
+                                  self.scale_s, self.param_dtype, basis_dtype=self.basis_dtype,
+                                  norm=self.norm)
             self.M[i] = r["M"]
             out_W.append(r["W"])
             if keep_parts:

@@ -225,6 +225,63 @@ def test_invariances():
 
 
 # --------------------------------------------------------------------------
+# Dobb-l2: column l2 normalisation ([Dobb, Tables 9 and 11])
+# --------------------------------------------------------------------------
+
+def test_l2_table9_norm_and_nonzero_columns():
+    """[Dobb, Table 9]: Dobb-l2's raw update has ||O||_F^2 = n (O = U / sqrt(m));
+    with zero columns in C only the nonzero ones count."""
+    rng = np.random.default_rng(51)
+    for (m, n, B) in ((40, 24, 3), (16, 48, 4)):
+        M, G, W, Q = _rand_case(rng, m=m, n=n, B=B)
+        U = O.update_from_bases(W, M, G, Q, 0.95, 1.0, 1.0, norm="l2")["U"]
+        assert abs((U ** 2).sum() / m - n) < 1e-9 * n
+        # a zero column of C (zero momentum column and Q = I) stays zero
+        Q2 = np.broadcast_to(np.eye(n // B), (B, n // B, n // B)).copy()
+        M2, G2 = M.copy(), G.copy()
+        M2[:, 1] = 0.0
+        G2[:, 1] = 0.0
+        U2 = O.update_from_bases(W, M2, G2, Q2, 0.95, 1.0, 1.0, norm="l2")["U"]
+        assert np.all(U2[:, 1] == 0.0) and abs((U2 ** 2).sum() / m - (n - 1)) < 1e-9 * n
+
+
+def test_l2_identity_basis_closed_form_and_invariances():
+    rng = np.random.default_rng(52)
+    m, n, B = 20, 12, 3
+    M, G, W, Q = _rand_case(rng, m=m, n=n, B=B)
+    Mn = 0.9 * M + G
+    I4 = np.broadcast_to(np.eye(4), (B, 4, 4)).copy()
+    U = O.update_from_bases(W, M, G, I4, 0.9, 0.02, 1.0, norm="l2")["U"]
+    assert np.abs(U - math.sqrt(m) * Mn / np.linalg.norm(Mn, axis=0)[None, :]).max() < 1e-12
+    base = O.update_from_bases(W, M, G, Q, 0.9, 0.02, 1.0, norm="l2")["U"]
+    Q2 = Q.copy()
+    for b in range(B):
+        Q2[b] = (Q[b] * rng.choice([-1.0, 1.0], size=4)[None, :])[:, rng.permutation(4)]
+    assert np.abs(O.update_from_bases(W, M, G, Q2, 0.9, 0.02, 1.0, norm="l2")["U"] - base).max() < 1e-12
+    assert np.abs(O.update_from_bases(W, 2.5 * M, 2.5 * G, Q, 0.9, 0.02, 1.0, norm="l2")["U"]
+                  - base).max() < 1e-12
+
+
+def test_l2_brute_force_tiny_step():
+    rng = np.random.default_rng(53)
+    m, n, B = 3, 4, 2
+    k = n // B
+    M, G, W, Q = _rand_case(rng, m=m, n=n, B=B)
+    beta1, lr, s = 0.8, 0.1, 1.5
+    W_exp = W.copy()
+    for b in range(B):
+        C = [[sum((beta1 * M[i, b * k + l] + G[i, b * k + l]) * Q[b, l, j] for l in range(k))
+              for j in range(k)] for i in range(m)]
+        nrm = [math.sqrt(sum(C[i][j] ** 2 for i in range(m))) for j in range(k)]
+        for i in range(m):
+            for l in range(k):
+                u = sum(math.sqrt(m) * C[i][j] / nrm[j] * Q[b, l, j] for j in range(k))
+                W_exp[i, b * k + l] -= lr * s * u
+    r = O.update_from_bases(W, M, G, Q, beta1, lr, s, norm="l2")
+    assert np.abs(r["W"] - W_exp).max() < 1e-12
+
+
+# --------------------------------------------------------------------------
 # orthogonal-iteration refresh ([Dobb, Table 15] principal, Table 16 Cholesky QR)
 # --------------------------------------------------------------------------
 
