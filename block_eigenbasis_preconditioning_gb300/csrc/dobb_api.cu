@@ -48,6 +48,7 @@ size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 struct Layout {
   size_t a_floats = 0, lam_floats = 0, m_floats = 0, pack_bytes = 0;
   int64_t nblocks = 0;
+  size_t off_colsq = 0;  // column sums of squares (column-l2 normalisation), eigenvalue layout
   size_t off_A = 0, off_Q = 0, off_lam = 0, off_M = 0, off_flags = 0, off_stats = 0,
          off_check = 0, off_err = 0, off_info = 0, off_maps = 0, off_tiles = 0, off_pack = 0,
          off_scratch = 0, total = 0;
@@ -261,6 +262,7 @@ Layout compute_layout(int num, const int64_t* m, const int64_t* n, int B, size_t
   L.off_flags = off;  off = align_up(off + 4 * (size_t)L.nblocks);
   L.off_stats = off;  off = align_up(off + 16 * (size_t)L.nblocks);
   L.off_check = off;  off = align_up(off + 12 * (size_t)L.nblocks);
+  L.off_colsq = off;  off = align_up(off + 4 * L.lam_floats);
   L.off_err = off;    off = align_up(off + 4);
   L.off_info = off;   off = align_up(off + sizeof(MatInfo) * (size_t)num);
   L.off_maps = off;   off = align_up(off + sizeof(CUtensorMap) * (size_t)num);
@@ -290,6 +292,7 @@ struct dobb_ctx {
   float tol = 0.f;
   bool basis_bf16 = false;  // the update multiplies with bf16(Q)
   int refresh_method = DOBB_REFRESH_EIGH;
+  int norm = DOBB_NORM_SIGN;
   int orth_steps = 1;
   int sm_count = 1;
   size_t smem_limit = 0;
@@ -312,6 +315,7 @@ struct dobb_ctx {
   uint32_t* flags() const { return reinterpret_cast<uint32_t*>(base + L.off_flags); }
   float* stats() const { return reinterpret_cast<float*>(base + L.off_stats); }
   float* check() const { return reinterpret_cast<float*>(base + L.off_check); }
+  float* colsq() const { return reinterpret_cast<float*>(base + L.off_colsq); }
   MatInfo* dinfo() const { return reinterpret_cast<MatInfo*>(base + L.off_info); }
   Tile* dtiles() const { return reinterpret_cast<Tile*>(base + L.off_tiles); }
   float* scratch() const { return reinterpret_cast<float*>(base + L.off_scratch); }
@@ -420,7 +424,8 @@ dobb_status do_step(dobb_handle h, void* const* W, const void* const* G, float l
   bool aligned = true;
   for (int i = 0; i < h->num; ++i)
     if ((reinterpret_cast<uintptr_t>(W[i]) | reinterpret_cast<uintptr_t>(G[i])) % 16 != 0) aligned = false;
-  const bool use_tc = h->path == 0 && aligned;
+  const bool l2 = h->norm == DOBB_NORM_L2;
+  const bool use_tc = h->path == 0 && aligned && !l2;
   for (const Chunk& ch : h->wl.chunks) {
     if (ch.step_n == 0) continue;
     StepArgs a{};
@@ -435,6 +440,8 @@ dobb_status do_step(dobb_handle h, void* const* W, const void* const* G, float l
     a.beta1 = h->beta1;
     a.lr_s = lr * h->scale_s;
     a.basis_bf16 = h->basis_bf16 ? 1 : 0;
+    a.mode = kModeSign;
+    a.colsq = h->colsq();
     for (int i = ch.mat_base; i < ch.mat_end; ++i) {
       a.W[i - ch.mat_base] = W[i];
       a.G[i - ch.mat_base] = G[i];
@@ -468,6 +475,20 @@ dobb_status do_step(dobb_handle h, void* const* W, const void* const* G, float l
         if (e != cudaSuccess) return fail(DOBB_ERR_CUDA, "tensor-core step launch: %s", cudaGetErrorString(e));
         ++h->launches;
       }
+    }
+    if (l2) {
+      // column l2: pass 1 over every (matrix, block) of the chunk (momentum
+      // update and column sums of C^2), then the update with scaled coefficients
+      StepArgs an = a;
+      an.tiles = h->dtiles() + h->wl.blocks_off + h->info[ch.mat_base].blk0;
+      an.num_tiles = (ch.mat_end - ch.mat_base) * h->B;
+      const size_t smem = step_smem_for(ch.max_k);
+      const int by_smem = std::max(1, (int)(h->smem_per_sm / (smem + 1024)));
+      const int g = std::max(1, std::min(an.num_tiles, h->sm_count * std::min(4, by_smem)));
+      cudaError_t e = launch_l2_norms(an, h->pdt, g, smem, s);
+      if (e != cudaSuccess) return fail(DOBB_ERR_CUDA, "column-norm launch: %s", cudaGetErrorString(e));
+      ++h->launches;
+      a.mode = kModeL2Apply;
     }
     const bool rest_only = use_tc && ch.tc_n > 0;
     const int n_ffma = rest_only ? ch.rest_n : ch.step_n;
@@ -810,6 +831,21 @@ dobb_status dobb_set_basis_dtype(dobb_handle h, dobb_dtype basis_dtype, void* st
   h->basis_bf16 = basis_dtype == DOBB_BF16;
   // the tensor-core operand images hold the basis in the chosen precision
   return do_pack(h, static_cast<cudaStream_t>(stream));
+}
+
+dobb_status dobb_set_normalization(dobb_handle h, int norm) {
+  if (!h) return fail(DOBB_ERR_INVALID_ARG, "NULL handle");
+  if (norm != DOBB_NORM_SIGN && norm != DOBB_NORM_L2)
+    return fail(DOBB_ERR_INVALID_ARG, "normalisation must be DOBB_NORM_SIGN or DOBB_NORM_L2");
+  if (norm == DOBB_NORM_L2) {
+    for (int i = 0; i < h->num; ++i)
+      if (h->n[i] / h->B > l2_max_k())
+        return fail(DOBB_ERR_UNSUPPORTED, "column-l2 normalisation supports blocks up to %d wide", l2_max_k());
+    if (step_smem_for((int)(h->n[0] / h->B)) > h->smem_limit)
+      return fail(DOBB_ERR_UNSUPPORTED, "block too wide for the FP32 update kernel");
+  }
+  h->norm = norm;
+  return DOBB_OK;
 }
 
 dobb_status dobb_set_refresh(dobb_handle h, int method, int steps) {

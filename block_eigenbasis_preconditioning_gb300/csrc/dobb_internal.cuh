@@ -100,6 +100,10 @@ struct EigArgs {
   float tol;              // relative off-diagonal norm of the last sweep's B (0 = default)
 };
 
+// Coefficient normalisation of the FP32 update kernel.
+constexpr int32_t kModeSign = 0;
+constexpr int32_t kModeL2Apply = 2;
+
 struct StepArgs {
   const MatInfo* info;
   const Tile* tiles;
@@ -112,6 +116,8 @@ struct StepArgs {
   float beta1;
   float lr_s;             // lr * s
   int32_t basis_bf16;     // multiply with bf16(Q) (bf16 basis storage)
+  int32_t mode;           // kModeSign, or kModeL2Apply (column-l2 pass 2)
+  float* colsq;           // column sums of C^2 (column-l2), eigenvalue-region layout
   void* W[kMaxMatPerLaunch];
   const void* G[kMaxMatPerLaunch];
   int8_t* S[kMaxMatPerLaunch];
@@ -132,6 +138,10 @@ cudaError_t launch_syrk_ema(const AccArgs& a, int act_dtype, int grid, cudaStrea
 cudaError_t launch_jacobi(const EigArgs& a, int grid, size_t smem_bytes, cudaStream_t s);
 cudaError_t launch_step_ffma(const StepArgs& a, int param_dtype, int grid, size_t smem,
                              cudaStream_t s);
+// column-l2 pass 1 over (matrix, block) items; writes StepArgs::colsq
+cudaError_t launch_l2_norms(const StepArgs& a, int param_dtype, int grid, size_t smem,
+                            cudaStream_t s);
+int l2_max_k();
 cudaError_t launch_check(const CheckArgs& a, int grid, cudaStream_t s);
 
 // Kernel resource queries used by the scheduler at create time.

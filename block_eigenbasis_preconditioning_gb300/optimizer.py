@@ -11,7 +11,7 @@ from typing import List, Optional, Sequence, Tuple
 
 import torch
 
-from .binding import (DTYPES, REFRESH_METHODS, TENSORS, _i64, _ptrs, check, load_library)
+from .binding import (DTYPES, NORMS, REFRESH_METHODS, TENSORS, _i64, _ptrs, check, load_library)
 
 _TORCH_DTYPES = {"f32": torch.float32, "bf16": torch.bfloat16}
 
@@ -30,13 +30,15 @@ class Dobb:
     "bf16"), basis_dtype of the basis the update multiplies with ("f32", or
     "bf16" as in the pages' principal setting), and the refresh method:
     "eigh" (complete eigendecomposition) or "orth" (orth_steps steps of
-    orthogonal iteration with Cholesky QR, the pages' principal refresh)."""
+    orthogonal iteration with Cholesky QR, the pages' principal refresh), and
+    the coefficient normalisation norm: "sign" (Dobb) or "l2" (Dobb-l2)."""
 
     def __init__(self, shapes: Sequence[Tuple[int, int]], B: int, beta1: float = 0.95,
                  beta2: float = 0.99, refresh_period: int = 10, scale_s: float = 1.0,
                  param_dtype: str = "f32", act_dtype: str = "f32",
                  device: Optional[torch.device] = None, stream: Optional[torch.cuda.Stream] = None,
-                 basis_dtype: str = "f32", refresh: str = "eigh", orth_steps: int = 1):
+                 basis_dtype: str = "f32", refresh: str = "eigh", orth_steps: int = 1,
+                 norm: str = "sign"):
         self.lib = load_library()
         self.shapes = [(int(m), int(n)) for m, n in shapes]
         self.B = int(B)
@@ -64,6 +66,9 @@ class Dobb:
         self.refresh_method = refresh
         if refresh != "eigh" or orth_steps != 1:
             check(self.lib.dobb_set_refresh(h, REFRESH_METHODS[refresh], int(orth_steps)))
+        self.norm = norm
+        if norm != "sign":
+            check(self.lib.dobb_set_normalization(h, NORMS[norm]))
 
     # -- phases --------------------------------------------------------------
     def accumulate(self, X: Sequence[Optional[torch.Tensor]], stream=None) -> None:

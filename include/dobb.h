@@ -134,6 +134,19 @@ dobb_status dobb_step_with_signs(dobb_handle h, void* const* W, const void* cons
 dobb_status dobb_get_step(dobb_handle h, int64_t* t);
 dobb_status dobb_set_step(dobb_handle h, int64_t t);
 
+/* Coefficient normalisation of the update.
+ * DOBB_NORM_SIGN (default): S_b = sign(C_b) ("Dobb", Abstract; l_inf).
+ * DOBB_NORM_L2: "Dobb-l2" (Table 11), each column of C_b over all m rows
+ *   scaled to l2 norm sqrt(m): S_b[:, j] = sqrt(m) C_b[:, j] / ||C_b[:, j]||
+ *   (0 for a zero column), so U / sqrt(m) has Table 9's ||O||_F^2 = n as the
+ *   sign update does.  Runs on the FP32 kernels in two passes (momentum and
+ *   column norms over all rows, then the update); blocks up to 1024 wide.
+ *   dobb_step's optional sign output receives sign(C_b).
+ * DOBB_ERR_INVALID_ARG for another value, DOBB_ERR_UNSUPPORTED for wider
+ * blocks. */
+enum { DOBB_NORM_SIGN = 0, DOBB_NORM_L2 = 1 };
+dobb_status dobb_set_normalization(dobb_handle h, int norm);
+
 /* Refresh method ("Dobb", Table 15).
  * DOBB_REFRESH_EIGH (default): complete eigendecomposition of every block,
  *   Q_b with A_b = Q_b Lambda_b Q_b^T (two-sided Jacobi), columns by

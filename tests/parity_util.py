@@ -20,6 +20,8 @@ Tolerances (the bar every GPU test applies):
 """
 from __future__ import annotations
 
+import math
+
 import numpy as np
 import torch
 
@@ -118,3 +120,50 @@ def check_update(W_prev, M_prev, G, Q_gpu, S_gpu, W_gpu, M_gpu, beta1, lr, s, pa
     res = MX.bf16_parity(W_gpu, ref2["W"], TOL_W)
     assert res["violations"] == 0, f"bf16 W: {res}"
     return {"sign": sa, "bf16": res, "m_err": dm}
+
+
+def l2_update_error_bound(M_new, Q, k, m):
+    """Frobenius bound on the error of a Dobb-l2 U computed in fp32 (the
+    tolerance is derived from the arithmetic, not chosen).  The projection's
+    k-term fp32 dot products have |C~ - C|_ij <= g (|M| |Q|)_ij, g = k u /
+    (1 - k u), u = 2^-24; normalising column j to norm sqrt(m) moves it by at
+    most 2 sqrt(m) ||e_j|| / ||c_j||; with Q_b orthonormal ||dU_b||_F equals
+    ||dS_b||_F.  Columns with little momentum energy dominate, as tiny |C|
+    entries do for the sign."""
+    u = 2.0 ** -24
+    g = k * u / (1 - k * u)
+    Mn = np.abs(np.asarray(M_new, dtype=np.float64))
+    B = Q.shape[0]
+    tot = 0.0
+    for b in range(B):
+        sl = slice(b * k, (b + 1) * k)
+        C = np.asarray(M_new, dtype=np.float64)[:, sl] @ Q[b]
+        E = g * (Mn[:, sl] @ np.abs(Q[b]))
+        cn = np.linalg.norm(C, axis=0)
+        en = np.linalg.norm(E, axis=0)
+        ok = cn > 0
+        tot += float(((2 * math.sqrt(m) * en[ok] / cn[ok]) ** 2).sum())
+        # plus the rounding of the normalisation and the reconstruction
+        tot += (8 * k * u) ** 2 * m * k
+    return math.sqrt(tot)
+
+
+def check_update_l2(W_prev, M_prev, G, Q_gpu, W_gpu, M_gpu, beta1, lr, s, param_dtype,
+                    basis_dtype="f32"):
+    """Score a Dobb-l2 update (column l2 normalisation) against the oracle run
+    with the GPU basis.  The normalised coefficients are continuous, so W is
+    compared directly, in Frobenius norm, within lr s times the fp32 bound of
+    `l2_update_error_bound` (plus, for bf16 parameters, half a bf16 quantum per
+    entry, 2^-8 |W|)."""
+    ref = O.update_from_bases(W_prev, M_prev, G, Q_gpu, beta1, lr, s, "f32",
+                              basis_dtype=basis_dtype, norm="l2")
+    dm = np.abs(M_gpu - ref["M"]).max() / max(np.abs(ref["M"]).max(), 1e-30)
+    assert dm <= 1e-6, f"momentum relative error {dm:.3e}"
+    m, n = ref["W"].shape
+    k = Q_gpu.shape[1]
+    bound = lr * s * l2_update_error_bound(ref["M"], Q_gpu, k, m)
+    if param_dtype == "bf16":
+        bound += float(np.linalg.norm(2.0 ** -8 * np.abs(ref["W"])))
+    err = float(np.linalg.norm(np.asarray(W_gpu, dtype=np.float64) - ref["W"]))
+    assert err <= bound, f"W error {err:.3e} above the fp32 bound {bound:.3e}"
+    return err, bound

@@ -8,8 +8,8 @@ from block_eigenbasis_preconditioning_gb300 import inputs as I
 from oracle import dobb as O
 from oracle import metrics as MX
 
-from parity_util import (TOL_A, check_bases, check_moments, check_update, make_problem,
-                         to_dev, to_np)
+from parity_util import (TOL_A, check_bases, check_moments, check_update, check_update_l2,
+                         make_problem, to_dev, to_np)
 
 pytestmark = pytest.mark.gpu
 
@@ -453,3 +453,69 @@ def test_run_with_orth_refresh_matches_oracle_updates(pdt):
                              to_np(opt.tensor("momentum", i)), 0.9, 0.02, 1.0, pdt, n // B)
             orc.M[i] = O.momentum(M_prev[i], to_np(Gd[i]), 0.9)
             assert np.linalg.norm(Q[0].T @ Q[0] - np.eye(n // B)) <= 1e-5 * np.sqrt(n // B)
+
+
+# --------------------------------------------------------------------------
+# (f2) Dobb-l2: column l2 normalisation ([Dobb, Tables 9 and 11])
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("pdt", ["f32", "bf16"])
+@pytest.mark.parametrize("shapes,B", [
+    ([(37, 96)], 2),            # k = 48, ragged rows
+    ([(1, 24), (17, 24)], 3),   # m = 1 (l2 = sign there), k = 8
+    ([(130, 200)], 2),          # k = 100
+    ([(200, 400)], 1),          # k = 400
+    ([(9, 15)], 5),             # k = 3 (odd)
+])
+def test_update_with_l2_normalisation_matches_oracle(pdt, shapes, B):
+    N = max(256, 4 * max(n // B for _, n in shapes))
+    Xs, Gs, Ws = make_problem(shapes, N, 0.2, seed=24, param_dtype=pdt)
+    opt = _dobb(shapes, B, beta1=0.9, beta2=0.95, refresh_period=1, scale_s=1.5, param_dtype=pdt,
+                norm="l2")
+    Wd = [to_dev(w, pdt) for w in Ws]
+    Gd = [to_dev(g, pdt) for g in Gs]
+    Sd = [torch.zeros(w.shape, dtype=torch.int8, device="cuda") for w in Ws]
+    W_prev = [to_np(w) for w in Wd]
+    opt.accumulate([to_dev(x, "f32") for x in Xs])
+    opt.step(Wd, Gd, 0.02, signs=Sd)
+    torch.cuda.synchronize()
+    st = opt.block_stats()
+    for i, (m, n) in enumerate(shapes):
+        k = n // B
+        Q = to_np(opt.tensor("bases", i))
+        check_update_l2(W_prev[i], np.zeros((m, n)), to_np(Gd[i]), Q, to_np(Wd[i]),
+                        to_np(opt.tensor("momentum", i)), 0.9, 0.02, 1.5, pdt)
+        # the returned signs are those of C
+        ref = O.update_from_bases(W_prev[i], np.zeros((m, n)), to_np(Gd[i]), Q, 0.9, 0.02, 1.5, "f32")
+        sa = MX.sign_agreement(ref["C"], to_np(Sd[i]), k)
+        assert sa["outside_band"] == 0
+        # ||U_b||_F^2 = m k: every column of S has norm sqrt(m), Q_b orthonormal
+        for b in range(B):
+            assert abs(st[opt.block_offset(i) + b, 0] - m * k) <= 1e-4 * m * k
+
+
+def test_run_with_l2_normalisation_and_refresh():
+    """Several steps with refreshes: moments, bases and every Dobb-l2 update
+    against the oracle with the GPU's basis."""
+    shapes, B = [(64, 192), (96, 128)], 2
+    rng = np.random.default_rng(25)
+    opt = _dobb(shapes, B, beta1=0.95, beta2=0.9, refresh_period=2, scale_s=1.0, norm="l2")
+    orc = O.DobbOracle(shapes, B, beta1=0.95, beta2=0.9, refresh_period=0, norm="l2")
+    Wd = [to_dev(I.weights(m, n, rng), "f32") for m, n in shapes]
+    for t in range(5):
+        Xs = [I.activations(512, n, 0.3, rng) for _, n in shapes]
+        Gd = [to_dev(I.gradients(m, X, rng), "f32") for (m, _), X in zip(shapes, Xs)]
+        W_prev = [to_np(w) for w in Wd]
+        M_prev = [m.copy() for m in orc.M]
+        opt.accumulate([to_dev(x, "f32") for x in Xs])
+        orc.accumulate(Xs)
+        opt.step(Wd, Gd, 0.02)
+        torch.cuda.synchronize()
+        check_moments(opt, orc)
+        if t % 2 == 0:
+            check_bases(opt, [to_np(opt.tensor("moments", i)) for i in range(len(shapes))])
+        for i, (m, n) in enumerate(shapes):
+            Q = to_np(opt.tensor("bases", i))
+            check_update_l2(W_prev[i], M_prev[i], to_np(Gd[i]), Q, to_np(Wd[i]),
+                            to_np(opt.tensor("momentum", i)), 0.95, 0.02, 1.0, "f32")
+            orc.M[i] = O.momentum(M_prev[i], to_np(Gd[i]), 0.95)
