@@ -55,19 +55,25 @@ def _peaks():
 # algorithmic work per launch (units: bytes / flops), see the design notes
 # ---------------------------------------------------------------------------
 
-def work_model(shapes, B, N, pbytes=2, xbytes=2):
+def work_model(shapes, B, N, pbytes=2, xbytes=2, refresh="eigh", orth_steps=1, norm="sign"):
     upd_bytes = upd_flops = acc_bytes = acc_flops = ref_flops = ref_bytes = 0
     for (m, n) in shapes:
         k = n // B
         # update: G read, M read + write, W read + write, Q_b read once
         upd_bytes += m * n * (pbytes + 4 + 4 + 2 * pbytes) + 4 * B * k * k
+        if norm == "l2":
+            # the column norms run over all rows before any row is updated: the
+            # momentum is read a second time
+            upd_bytes += 4 * m * n
         upd_flops += 4 * k * m * n
         # accumulate: X read, A read + write (symmetric: N k (k+1) flops)
         acc_bytes += xbytes * N * n + 8 * B * k * k
         acc_flops += B * N * k * (k + 1)
         # refresh: 9 k^3 flops per block (symmetric eigendecomposition with
-        # vectors), A read, Q and Lambda written
-        ref_flops += 9 * B * k ** 3
+        # vectors), or per orthogonal-iteration step 2 k^3 (A Q) + k^3 (Gram,
+        # symmetric) + k^3 / 3 (Cholesky) + k^3 (triangular solve); A read,
+        # Q and Lambda written
+        ref_flops += B * k ** 3 * (9 if refresh == "eigh" else orth_steps * 13 / 3)
         ref_bytes += 8 * B * k * k + 4 * B * k
     return dict(update_bytes=upd_bytes, update_flops=upd_flops, acc_bytes=acc_bytes,
                 acc_flops=acc_flops, refresh_flops=ref_flops, refresh_bytes=ref_bytes)
@@ -191,8 +197,8 @@ def _kernel_source_sha(name):
 
 
 def _traffic_for(kernel_key):
-    """dram bytes per launch from a committed ncu summary, if it was taken on
-    the current source of that kernel."""
+    """dram bytes of that kernel per step (all its launches in one step) from a
+    committed ncu summary, if it was taken on the current source of the kernel."""
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             t = json.load(f)
@@ -208,7 +214,7 @@ def _traffic_for(kernel_key):
 # CPU baseline: the oracle on a bounded sample
 # ---------------------------------------------------------------------------
 
-def cpu_baseline(layers_sample=2, seed=0, basis="f32"):
+def cpu_baseline(layers_sample=2, seed=0, basis="f32", refresh="eigh", orth_steps=1, norm="sign"):
     import numpy as np
     from block_eigenbasis_preconditioning_gb300 import inputs as I
     from oracle import dobb as O
@@ -218,7 +224,8 @@ def cpu_baseline(layers_sample=2, seed=0, basis="f32"):
         shapes += [(1600, 1600)] * 4 + [(6400, 1600), (1600, 6400)]
     params = sum(m * n for m, n in shapes)
     orc = O.DobbOracle(shapes, B_BLOCKS, BETA1, BETA2, refresh_period=0, scale_s=SCALE,
-                       param_dtype="bf16", eig_method="lapack", basis_dtype=basis)
+                       param_dtype="bf16", eig_method="lapack", basis_dtype=basis,
+                       refresh_method=refresh, orth_steps=orth_steps, norm=norm)
     Xs = [I.round_bf16_np(rng.standard_normal((N_TOKENS, n)).astype(np.float32)) for _, n in shapes]
     Gs = [I.round_bf16_np((rng.standard_normal((m, n)) * 1e-3).astype(np.float32)) for m, n in shapes]
     Ws = [I.round_bf16_np((rng.standard_normal((m, n)) * 0.02).astype(np.float32)) for m, n in shapes]
@@ -233,7 +240,9 @@ def cpu_baseline(layers_sample=2, seed=0, basis="f32"):
     step_s = acc + upd + ref / REFRESH
     return {"value": params / step_s, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
             "sample": f"{layers_sample} GPT-2 XL layers ({params} params, 12 matrices), one "
-                      f"accumulate (N={N_TOKENS}) + one LAPACK refresh + one update in fp64 numpy; "
+                      f"accumulate (N={N_TOKENS}) + one "
+                      f"{'LAPACK' if refresh == 'eigh' else 'orthogonal-iteration'} refresh + one "
+                      f"update in fp64 numpy; "
                       f"amortized as accumulate + update + refresh/{REFRESH}",
             "seconds": {"accumulate": acc, "refresh": ref, "update": upd}}
 
@@ -248,7 +257,9 @@ def workload_config(args, n_matrices=None, params=None):
         name = (f"gpt2-xl shapes, first {args.layers} layers ({n_matrices} matrices, "
                 f"{params} params), B=16")
     return {"workload": name, "B": B_BLOCKS, "refresh_period": REFRESH, "tokens": N_TOKENS,
-            "basis": args.basis, "l2": "inputs larger than L2 (22 GB streamed per step)",
+            "basis": args.basis, "norm": args.norm,
+            "refresh": args.refresh if args.refresh == "eigh" else f"orth x{args.orth_steps}",
+            "l2": "inputs larger than L2 (22 GB streamed per step)",
             "parallelism": "single GPU"}
 
 
@@ -259,7 +270,8 @@ def run_reference(args):
     steps = []
     res = None
     for _ in range(max(1, args.steps)):
-        res = cpu_baseline(layers_sample=1, basis=args.basis)
+        res = cpu_baseline(layers_sample=1, basis=args.basis, refresh=args.refresh,
+                           orth_steps=args.orth_steps, norm=args.norm)
         steps.append(res["value"])
     v = sorted(steps)[len(steps) // 2]
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": 1,
@@ -297,7 +309,8 @@ def run_gpu(args):
     params = sum(m * n for m, n in shapes)
     Xsets, Gs, Ws = make_inputs(torch, shapes, layers, device, seed=1234 + rank)
     opt = Dobb(shapes, B_BLOCKS, BETA1, BETA2, refresh_period=REFRESH, scale_s=SCALE,
-               param_dtype="bf16", act_dtype="bf16", device=device, basis_dtype=args.basis)
+               param_dtype="bf16", act_dtype="bf16", device=device, basis_dtype=args.basis,
+               refresh=args.refresh, orth_steps=args.orth_steps, norm=args.norm)
     stream = torch.cuda.current_stream()
     moments = opt.tensor("moments")
 
@@ -367,16 +380,19 @@ def run_gpu(args):
         refresh_ms = e0.elapsed_time(e1)
 
     hbm, bf16, peak_kind = _peaks()
-    wm = work_model(shapes, B_BLOCKS, N_TOKENS)
+    wm = work_model(shapes, B_BLOCKS, N_TOKENS, refresh=args.refresh, orth_steps=args.orth_steps,
+                    norm=args.norm)
     alu_peak_tflops = 152 * 128 * 2 * 2.07e9 / 1e12  # FP32 lanes x FMA x max SM clock
     phases = {
-        "update": {"ms": upd_mean, "kernel": "step_tc_kernel", "bound": "hbm",
+        "update": {"ms": upd_mean, "kernel": "step_tc_kernel" if args.norm == "sign" else "step_ffma_kernel",
+                   "bound": "hbm",
                    "achieved": wm["update_bytes"] / (upd_mean * 1e-3) / 1e9 if upd_mean else None,
                    "peak": hbm, "unit": "GB/s", "flops": wm["update_flops"], "bytes": wm["update_bytes"]},
         "accumulate": {"ms": mean(acc_ms), "kernel": "syrk_tc_kernel", "bound": "hbm",
                        "achieved": wm["acc_bytes"] / (mean(acc_ms) * 1e-3) / 1e9,
                        "peak": hbm, "unit": "GB/s", "flops": wm["acc_flops"], "bytes": wm["acc_bytes"]},
-        "refresh": {"ms": refresh_ms, "kernel": "jacobi_kernel", "bound": "alu",
+        "refresh": {"ms": refresh_ms, "kernel": "jacobi_kernel" if args.refresh == "eigh" else "orth_kernel",
+                    "bound": "alu",
                     "achieved": wm["refresh_flops"] / (refresh_ms * 1e-3) / 1e12,
                     "peak": alu_peak_tflops, "unit": "TFLOP/s", "flops": wm["refresh_flops"]},
     }
@@ -399,7 +415,8 @@ def run_gpu(args):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
         try:
-            cpu = cpu_baseline(basis=args.basis)
+            cpu = cpu_baseline(basis=args.basis, refresh=args.refresh, orth_steps=args.orth_steps,
+                               norm=args.norm)
         except Exception as ex:  # pragma: no cover
             cpu = {"error": repr(ex)}
 
@@ -463,6 +480,12 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--refresh", default="eigh", choices=["eigh", "orth"],
+                    help="eigh: complete eigendecomposition; orth: orthogonal iteration with "
+                         "Cholesky QR (the pages' principal refresh)")
+    ap.add_argument("--orth-steps", type=int, default=1)
+    ap.add_argument("--norm", default="sign", choices=["sign", "l2"],
+                    help="coefficient normalisation: sign (Dobb) or l2 (Dobb-l2, FP32 kernels)")
     ap.add_argument("--basis", default="f32", choices=["f32", "bf16"],
                     help="precision of the basis the update multiplies with (bf16: the "
                          "pages' principal storage setting)")

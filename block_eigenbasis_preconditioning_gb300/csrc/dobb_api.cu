@@ -71,8 +71,13 @@ struct Chunk {
   int max_k_tc = 0, max_k_rest = 1;
   int syrk_off = 0, syrk_n = 0;
   int eig_off = 0, eig_n = 0;
+  int l2_off = 0, l2_n = 0;         // column-l2 norm items: (matrix, block, row chunk)
   int max_k = 1;
 };
+
+// rows per item of the column-l2 norm pass (one chunk's partial column sums
+// are added with one atomic per column)
+constexpr int64_t kL2Rows = 1024;
 
 struct SyrkChunk {
   int mat_base = 0, mat_end = 0, off = 0, n = 0, max_k = 8;
@@ -178,6 +183,13 @@ WorkLists build_work(int num, const int64_t* m, const int64_t* n, int B) {
     ch.syrk_off = (int)wl.tiles.size();
     ch.syrk_n = (int)v.size();
     for (auto& e : v) wl.tiles.push_back(e.second);
+    // column-l2 norm items: row chunks of every block, in matrix order
+    ch.l2_off = (int)wl.tiles.size();
+    for (int i = ch.mat_base; i < ch.mat_end; ++i)
+      for (int b = 0; b < B; ++b)
+        for (int64_t r = 0; r < m[i]; r += kL2Rows)
+          wl.tiles.push_back(Tile{i, b, (int)r, (int)std::min<int64_t>(kL2Rows, m[i] - r)});
+    ch.l2_n = (int)wl.tiles.size() - ch.l2_off;
     // eigen items: one per block, largest k first (cost ~ k^3)
     v.clear();
     for (int i = ch.mat_base; i < ch.mat_end; ++i) {
@@ -480,8 +492,12 @@ dobb_status do_step(dobb_handle h, void* const* W, const void* const* G, float l
       // column l2: pass 1 over every (matrix, block) of the chunk (momentum
       // update and column sums of C^2), then the update with scaled coefficients
       StepArgs an = a;
-      an.tiles = h->dtiles() + h->wl.blocks_off + h->info[ch.mat_base].blk0;
-      an.num_tiles = (ch.mat_end - ch.mat_base) * h->B;
+      an.tiles = h->dtiles() + ch.l2_off;
+      an.num_tiles = ch.l2_n;
+      const MatInfo& m0 = h->info[ch.mat_base];
+      const MatInfo& m1 = h->info[ch.mat_end - 1];
+      CUDA_TRY(cudaMemsetAsync(h->colsq() + m0.lam_off, 0,
+                               4 * (size_t)(m1.lam_off + (int64_t)m1.B * m1.k - m0.lam_off), s));
       const size_t smem = step_smem_for(ch.max_k);
       const int by_smem = std::max(1, (int)(h->smem_per_sm / (smem + 1024)));
       const int g = std::max(1, std::min(an.num_tiles, h->sm_count * std::min(4, by_smem)));

@@ -11,9 +11,9 @@
 // coefficients, reconstruct the update) and Table 9 (update scale s).
 // N is the sign (kModeSign), or for "Dobb-l2" (Table 11) the column l2
 // normalisation S[:, j] = sqrt(m) C[:, j] / ||C[:, j]||, whose column norms run
-// over all m rows: l2_norms_kernel first walks every (matrix, block) over all
-// its rows, updating M and summing C^2 per column, and the update kernel then
-// runs with kModeL2Apply (no momentum update, scaled coefficients).
+// over all m rows: l2_norms_kernel first walks every row chunk of every
+// (matrix, block), updating M and summing C^2 per column, and the update
+// kernel then runs with kModeL2Apply (no momentum update, scaled coefficients).
 #include "common.cuh"
 
 namespace dobb {
@@ -216,10 +216,11 @@ step_ffma_kernel(const __grid_constant__ StepArgs a) {
   }
 }
 
-// First pass of the column-l2 normalisation: one (matrix, block) per item,
-// over all its rows in tiles of kTM: M <- beta1 M + G, C = M Q, and the sum
-// of C^2 per column, kept per thread and written once per column into
-// colsq (the eigenvalue region's layout: lam_off + blk k + j).
+// First pass of the column-l2 normalisation: one (matrix, block, row chunk)
+// per item (Tile::a = first row, Tile::b = rows), over its rows in tiles of
+// kTM: M <- beta1 M + G, C = M Q, and the sum of C^2 per column, kept per
+// thread and added once per column and chunk into colsq (the eigenvalue
+// region's layout: lam_off + blk k + j; zeroed before the launch).
 template <typename PT>
 __global__ void __launch_bounds__(kThreads)
 l2_norms_kernel(const __grid_constant__ StepArgs a) {
@@ -245,8 +246,9 @@ l2_norms_kernel(const __grid_constant__ StepArgs a) {
 #pragma unroll
       for (int q = 0; q < 4; ++q) sq[p][q] = 0.f;
     int bad = 0;
-    for (int row0 = 0; row0 < mi.m; row0 += kTM) {
-      const int rows = (int)((mi.m - row0) < kTM ? (mi.m - row0) : kTM);
+    const int rend = (int)min((int64_t)t.a + t.b, mi.m);
+    for (int row0 = t.a; row0 < rend; row0 += kTM) {
+      const int rows = rend - row0 < kTM ? rend - row0 : kTM;
       bad |= momentum_tile(Mg, G, a.beta1, n, col0, row0, rows, k);
       __syncthreads();
 #pragma unroll
@@ -276,7 +278,7 @@ l2_norms_kernel(const __grid_constant__ StepArgs a) {
       float s = 0.f;
 #pragma unroll
       for (int r = 0; r < kRG; ++r) s += colbuf[r * kp + j];
-      a.colsq[mi.lam_off + (int64_t)t.blk * k + j] = s;
+      atomicAdd(a.colsq + mi.lam_off + (int64_t)t.blk * k + j, s);
     }
     const int any_bad = __syncthreads_or(bad);
     if (tid == 0 && any_bad) atomicOr(a.flags + mi.blk0 + t.blk, (uint32_t)DOBB_FLAG_NONFINITE_G);
