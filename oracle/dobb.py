@@ -68,6 +68,8 @@ __all__ = [
     "sign",
     "reconstruct",
     "l2_normalize_columns",
+    "project_left",
+    "reconstruct_left",
     "normalize",
     "apply_update",
     "round_to_bf16",
@@ -327,20 +329,54 @@ def basis_for_update(Q: np.ndarray, basis_dtype: str = "f32") -> np.ndarray:
     return _f64(Q)
 
 
+def project_left(M: np.ndarray, Q: np.ndarray) -> np.ndarray:
+    """Output-gradient side ("Dobb-G", [Dobb, Tables 12-13]): C_b = Q_b^T M_b
+    for every row block b (k = m / B rows): coefficients of the momentum
+    columns in the block eigenbasis of the output-gradient second moment."""
+    M = _f64(M)
+    Bn, k, _ = Q.shape
+    C = np.empty_like(M)
+    for b in range(Bn):
+        C[b * k:(b + 1) * k, :] = _f64(Q[b]).T @ M[b * k:(b + 1) * k, :]
+    return C
+
+
+def reconstruct_left(S: np.ndarray, Q: np.ndarray) -> np.ndarray:
+    """U_b = Q_b S_b for every row block b (the mirror of `reconstruct`)."""
+    S = _f64(S)
+    Bn, k, _ = Q.shape
+    U = np.empty_like(S)
+    for b in range(Bn):
+        U[b * k:(b + 1) * k, :] = _f64(Q[b]) @ S[b * k:(b + 1) * k, :]
+    return U
+
+
 def update_from_bases(W, M, G, Q, beta1: float, lr: float, s: float,
                       param_dtype: str = "f32", S_override: Optional[np.ndarray] = None,
-                      basis_dtype: str = "f32", norm: str = "sign"):
+                      basis_dtype: str = "f32", norm: str = "sign", side: str = "input"):
     """One update of a single matrix with given block bases Q (B, k, k).
     Returns dict with the new M, C, S, U and W.  `S_override` substitutes a
     given sign matrix (used to score a second implementation's signs at the
     entries where the sign is numerically undetermined).  `basis_dtype`
     selects the stored precision of the basis (see `basis_for_update`), `norm`
-    the coefficient normalisation (see `normalize`)."""
+    the coefficient normalisation (see `normalize`), `side` the axis the
+    blocks and bases live on: "input" (Dobb: column blocks, bases of the
+    activation second moment) or "output" (Dobb-G: row blocks, bases of the
+    output-gradient second moment, applied from the left; the normalisation
+    then runs over the rows of C^T, i.e. the columns of the transposed
+    problem)."""
     Qu = basis_for_update(Q, basis_dtype)
     Mn = momentum(M, G, beta1)
-    C = project(Mn, Qu)
-    S = normalize(C, norm) if S_override is None else _f64(S_override)
-    U = reconstruct(S, Qu)
+    if side == "output":
+        C = project_left(Mn, Qu)
+        S = normalize(C.T, norm).T if S_override is None else _f64(S_override)
+        U = reconstruct_left(S, Qu)
+    elif side == "input":
+        C = project(Mn, Qu)
+        S = normalize(C, norm) if S_override is None else _f64(S_override)
+        U = reconstruct(S, Qu)
+    else:
+        raise ValueError(f"side {side!r}")
     Wn = apply_update(W, U, lr, s, param_dtype)
     return {"M": Mn, "C": C, "S": S, "U": U, "W": Wn}
 
@@ -368,6 +404,7 @@ class DobbOracle:
     refresh_method: str = "eigh"   # "eigh" (exact) or "orth" (orthogonal iteration)
     orth_steps: int = 1
     norm: str = "sign"             # "sign" (Dobb) or "l2" (Dobb-l2)
+    side: str = "input"            # "input" (Dobb) or "output" (Dobb-G)
 
     def __post_init__(self):
         self.t = 0
@@ -376,13 +413,15 @@ class DobbOracle:
         self.lam: List[np.ndarray] = []
         self.M: List[np.ndarray] = []
         for (m, n) in self.shapes:
-            k = block_width(n, self.B)
+            k = block_width(m if self.side == "output" else n, self.B)
             self.A.append(np.zeros((self.B, k, k)))
             self.Q.append(np.broadcast_to(np.eye(k), (self.B, k, k)).copy())
             self.lam.append(np.zeros((self.B, k)))
             self.M.append(np.zeros((m, n)))
 
     def accumulate(self, X_list: Sequence[np.ndarray]) -> None:
+        """X: input activations (N x n), or for side "output" the output
+        gradients (N x m)."""
         for i, X in enumerate(X_list):
             if X is None:
                 continue
@@ -404,7 +443,7 @@ class DobbOracle:
         for i, (W, G) in enumerate(zip(W_list, G_list)):
             r = update_from_bases(W, self.M[i], G, self.Q[i], self.beta1, lr,
                                   self.scale_s, self.param_dtype, basis_dtype=self.basis_dtype,
-                                  norm=self.norm)
+                                  norm=self.norm, side=self.side)
             self.M[i] = r["M"]
             out_W.append(r["W"])
             if keep_parts:

@@ -225,6 +225,57 @@ def test_invariances():
 
 
 # --------------------------------------------------------------------------
+# Dobb-G: output-gradient basis ([Dobb, Tables 9, 12, 13])
+# --------------------------------------------------------------------------
+
+def test_dobb_g_table9_norm():
+    """[Dobb, Table 9]: Dobb-G's raw update has ||O||_F^2 = m with RMS
+    tau sqrt(max(m, n) / n) at s = tau sqrt(max(m, n)): O = U / sqrt(n)."""
+    rng = np.random.default_rng(61)
+    for (m, n, B) in ((24, 40, 3), (48, 16, 4)):
+        k = m // B
+        M, G, W = rng.standard_normal((3, m, n))
+        Q = np.stack([I.haar_orthogonal(k, rng) for _ in range(B)])
+        U = O.update_from_bases(W, M, G, Q, 0.95, 1.0, 1.0, side="output")["U"]
+        Ob = U / math.sqrt(n)
+        assert abs((Ob ** 2).sum() - m) < 1e-9 * m
+        tau = 0.2
+        rms = math.sqrt(((tau * math.sqrt(max(m, n)) * Ob) ** 2).mean())
+        assert abs(rms - tau * math.sqrt(max(m, n) / n)) < 1e-12
+
+
+@pytest.mark.parametrize("norm", ["sign", "l2"])
+def test_dobb_g_is_dobb_on_the_transpose(norm):
+    """Row blocks of W with bases applied from the left are the column blocks
+    of W^T: Dobb-G(W, M, G) = Dobb(W^T, M^T, G^T)^T with the same bases."""
+    rng = np.random.default_rng(62)
+    m, n, B = 18, 10, 3
+    k = m // B
+    M, G, W = rng.standard_normal((3, m, n))
+    Q = np.stack([I.haar_orthogonal(k, rng) for _ in range(B)])
+    rg = O.update_from_bases(W, M, G, Q, 0.9, 0.05, 1.3, side="output", norm=norm)
+    rd = O.update_from_bases(W.T, M.T, G.T, Q, 0.9, 0.05, 1.3, side="input", norm=norm)
+    for key in ("M", "C", "S", "U", "W"):
+        assert np.abs(rg[key] - rd[key].T).max() < 1e-12, key
+
+
+def test_dobb_g_identity_basis_and_moments():
+    rng = np.random.default_rng(63)
+    m, n, B, N = 12, 7, 3, 50
+    M, G, W = rng.standard_normal((3, m, n))
+    I4 = np.broadcast_to(np.eye(4), (B, 4, 4)).copy()
+    r = O.update_from_bases(W, M, G, I4, 0.5, 0.1, 1.0, side="output")
+    assert np.array_equal(r["U"], np.sign(0.5 * M + G))
+    # moments of the output gradients: blocks along m
+    orc = O.DobbOracle([(m, n)], B, beta2=0.0, refresh_period=0, side="output")
+    D = rng.standard_normal((N, m))
+    orc.accumulate([D])
+    for b in range(B):
+        Db = D[:, b * 4:(b + 1) * 4]
+        assert np.abs(orc.A[0][b] - Db.T @ Db / N).max() < 1e-12
+
+
+# --------------------------------------------------------------------------
 # Dobb-l2: column l2 normalisation ([Dobb, Tables 9 and 11])
 # --------------------------------------------------------------------------
 
