@@ -55,9 +55,12 @@ def _peaks():
 # algorithmic work per launch (units: bytes / flops), see the design notes
 # ---------------------------------------------------------------------------
 
-def work_model(shapes, B, N, pbytes=2, xbytes=2, refresh="eigh", orth_steps=1, norm="sign"):
+def work_model(shapes, B, N, pbytes=2, xbytes=2, refresh="eigh", orth_steps=1, norm="sign",
+               sides=None):
     upd_bytes = upd_flops = acc_bytes = acc_flops = ref_flops = ref_bytes = 0
-    for (m, n) in shapes:
+    for i, (m, n) in enumerate(shapes):
+        if sides is not None and sides[i] == "output":
+            m, n = n, m   # Dobb-G: the same work on the transposed problem
         k = n // B
         # update: G read, M read + write, W read + write, Q_b read once
         upd_bytes += m * n * (pbytes + 4 + 4 + 2 * pbytes) + 4 * B * k * k
@@ -141,11 +144,12 @@ class ClockSampler:
 # synthetic inputs on the device (seeded)
 # ---------------------------------------------------------------------------
 
-def make_inputs(torch, shapes, layers, device, seed, n_xsets=2):
+def make_inputs(torch, shapes, layers, device, seed, n_xsets=2, sides=None):
     """X_i (N x n, bf16) per matrix with layer-dependent effective rank,
-    G_i = D X_i / N (bf16), W_i ~ N(0, 0.02^2) (bf16).  Generated on the
-    device with torch's seeded generator; the spectra come from the shared
-    input module."""
+    G_i = D X_i / N (bf16), W_i ~ N(0, 0.02^2) (bf16).  For an output-side
+    (Dobb-G) matrix X_i are output gradients (N x m) of the same recipe and
+    G_i = X_i^T D / N.  Generated on the device with torch's seeded
+    generator; the spectra come from the shared input module."""
     from block_eigenbasis_preconditioning_gb300 import inputs as I
     g = torch.Generator(device=device)
     g.manual_seed(seed)
@@ -155,7 +159,10 @@ def make_inputs(torch, shapes, layers, device, seed, n_xsets=2):
     haar_cache = {}
     Xsets = [[] for _ in range(n_xsets)]
     Gs, Ws = [], []
-    for (m, n), li in zip(shapes, layers):
+    for i, ((m, n), li) in enumerate(zip(shapes, layers)):
+        out = sides is not None and sides[i] == "output"
+        if out:
+            m, n = n, m   # X spans the output axis; G is built transposed below
         eff = I.layer_rank_schedule(min(li, nl - 1), nl) if li < nl else 0.10
         key = (n, round(eff, 6))
         if key not in lam_cache:
@@ -177,9 +184,10 @@ def make_inputs(torch, shapes, layers, device, seed, n_xsets=2):
             del Z, X
         D = torch.randn(m, N_TOKENS, generator=g, device=device)
         G = (D @ Xsets[0][-1].float()) / N_TOKENS
-        Gs.append(G.to(torch.bfloat16))
+        Gs.append((G.T if out else G).contiguous().to(torch.bfloat16))
         del D, G
-        Ws.append((torch.randn(m, n, generator=g, device=device) * 0.02).to(torch.bfloat16))
+        W = torch.randn(m, n, generator=g, device=device) * 0.02
+        Ws.append((W.T if out else W).contiguous().to(torch.bfloat16))
     return Xsets, Gs, Ws
 
 
@@ -214,7 +222,8 @@ def _traffic_for(kernel_key):
 # CPU baseline: the oracle on a bounded sample
 # ---------------------------------------------------------------------------
 
-def cpu_baseline(layers_sample=2, seed=0, basis="f32", refresh="eigh", orth_steps=1, norm="sign"):
+def cpu_baseline(layers_sample=2, seed=0, basis="f32", refresh="eigh", orth_steps=1, norm="sign",
+                 side="input"):
     import numpy as np
     from block_eigenbasis_preconditioning_gb300 import inputs as I
     from oracle import dobb as O
@@ -225,8 +234,9 @@ def cpu_baseline(layers_sample=2, seed=0, basis="f32", refresh="eigh", orth_step
     params = sum(m * n for m, n in shapes)
     orc = O.DobbOracle(shapes, B_BLOCKS, BETA1, BETA2, refresh_period=0, scale_s=SCALE,
                        param_dtype="bf16", eig_method="lapack", basis_dtype=basis,
-                       refresh_method=refresh, orth_steps=orth_steps, norm=norm)
-    Xs = [I.round_bf16_np(rng.standard_normal((N_TOKENS, n)).astype(np.float32)) for _, n in shapes]
+                       refresh_method=refresh, orth_steps=orth_steps, norm=norm, side=side)
+    Xs = [I.round_bf16_np(rng.standard_normal((N_TOKENS, m if side == "output" else n))
+                          .astype(np.float32)) for m, n in shapes]
     Gs = [I.round_bf16_np((rng.standard_normal((m, n)) * 1e-3).astype(np.float32)) for m, n in shapes]
     Ws = [I.round_bf16_np((rng.standard_normal((m, n)) * 0.02).astype(np.float32)) for m, n in shapes]
     t0 = time.perf_counter()
@@ -257,7 +267,7 @@ def workload_config(args, n_matrices=None, params=None):
         name = (f"gpt2-xl shapes, first {args.layers} layers ({n_matrices} matrices, "
                 f"{params} params), B=16")
     return {"workload": name, "B": B_BLOCKS, "refresh_period": REFRESH, "tokens": N_TOKENS,
-            "basis": args.basis, "norm": args.norm,
+            "basis": args.basis, "norm": args.norm, "side": args.side,
             "refresh": args.refresh if args.refresh == "eigh" else f"orth x{args.orth_steps}",
             "l2": "inputs larger than L2 (22 GB streamed per step)",
             "parallelism": "single GPU"}
@@ -271,7 +281,7 @@ def run_reference(args):
     res = None
     for _ in range(max(1, args.steps)):
         res = cpu_baseline(layers_sample=1, basis=args.basis, refresh=args.refresh,
-                           orth_steps=args.orth_steps, norm=args.norm)
+                           orth_steps=args.orth_steps, norm=args.norm, side=args.side)
         steps.append(res["value"])
     v = sorted(steps)[len(steps) // 2]
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": 1,
@@ -307,10 +317,14 @@ def run_gpu(args):
         shapes = [shapes[i] for i in keep]
         layers = [layers[i] for i in keep]
     params = sum(m * n for m, n in shapes)
-    Xsets, Gs, Ws = make_inputs(torch, shapes, layers, device, seed=1234 + rank)
+    # Dobb-G blocks the output axis of every layer matrix; the token
+    # embedding (50257 rows: no 16 equal blocks) stays on the input side
+    sides = [("output" if args.side == "output" and m % B_BLOCKS == 0 and m // B_BLOCKS <= 1024
+              else "input") for m, n in shapes]
+    Xsets, Gs, Ws = make_inputs(torch, shapes, layers, device, seed=1234 + rank, sides=sides)
     opt = Dobb(shapes, B_BLOCKS, BETA1, BETA2, refresh_period=REFRESH, scale_s=SCALE,
                param_dtype="bf16", act_dtype="bf16", device=device, basis_dtype=args.basis,
-               refresh=args.refresh, orth_steps=args.orth_steps, norm=args.norm)
+               refresh=args.refresh, orth_steps=args.orth_steps, norm=args.norm, side=sides)
     stream = torch.cuda.current_stream()
     moments = opt.tensor("moments")
 
@@ -381,10 +395,11 @@ def run_gpu(args):
 
     hbm, bf16, peak_kind = _peaks()
     wm = work_model(shapes, B_BLOCKS, N_TOKENS, refresh=args.refresh, orth_steps=args.orth_steps,
-                    norm=args.norm)
+                    norm=args.norm, sides=sides)
+    ffma_update = args.norm != "sign" or "output" in sides
     alu_peak_tflops = 152 * 128 * 2 * 2.07e9 / 1e12  # FP32 lanes x FMA x max SM clock
     phases = {
-        "update": {"ms": upd_mean, "kernel": "step_tc_kernel" if args.norm == "sign" else "step_ffma_kernel",
+        "update": {"ms": upd_mean, "kernel": "step_ffma_kernel" if ffma_update else "step_tc_kernel",
                    "bound": "hbm",
                    "achieved": wm["update_bytes"] / (upd_mean * 1e-3) / 1e9 if upd_mean else None,
                    "peak": hbm, "unit": "GB/s", "flops": wm["update_flops"], "bytes": wm["update_bytes"]},
@@ -416,7 +431,7 @@ def run_gpu(args):
     if rank == 0 and world == 1 and not args.no_cpu:
         try:
             cpu = cpu_baseline(basis=args.basis, refresh=args.refresh, orth_steps=args.orth_steps,
-                               norm=args.norm)
+                               norm=args.norm, side=args.side)
         except Exception as ex:  # pragma: no cover
             cpu = {"error": repr(ex)}
 
@@ -486,6 +501,10 @@ def main():
     ap.add_argument("--orth-steps", type=int, default=1)
     ap.add_argument("--norm", default="sign", choices=["sign", "l2"],
                     help="coefficient normalisation: sign (Dobb) or l2 (Dobb-l2, FP32 kernels)")
+    ap.add_argument("--side", default="input", choices=["input", "output"],
+                    help="input: Dobb (blocks of the input axis, activation moments); output: "
+                         "Dobb-G (blocks of the output axis, output-gradient moments; FP32 "
+                         "update kernel)")
     ap.add_argument("--basis", default="f32", choices=["f32", "bf16"],
                     help="precision of the basis the update multiplies with (bf16: the "
                          "pages' principal storage setting)")

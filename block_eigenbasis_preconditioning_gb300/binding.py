@@ -22,6 +22,7 @@ STATUS_NAMES = {0: "DOBB_OK", 1: "DOBB_ERR_INVALID_ARG", 2: "DOBB_ERR_CUDA",
 DTYPES = {"f32": 0, "bf16": 1}
 REFRESH_METHODS = {"eigh": 0, "orth": 1}
 NORMS = {"sign": 0, "l2": 1}
+SIDES = {"input": 0, "output": 1}
 TENSORS = {"moments": 0, "bases": 1, "eigvals": 2, "momentum": 3, "flags": 4, "stats": 5,
            "error": 6}
 FLAG_NONFINITE_X = 1
@@ -50,6 +51,7 @@ SIGNATURES = [
     ("dobb_set_basis_dtype", _c.c_int, [_VP, _c.c_int, _VP]),
     ("dobb_set_refresh", _c.c_int, [_VP, _c.c_int, _c.c_int]),
     ("dobb_set_normalization", _c.c_int, [_VP, _c.c_int]),
+    ("dobb_set_side", _c.c_int, [_VP, _c.c_int, _c.c_int, _VP]),
     ("dobb_set_jacobi", _c.c_int, [_VP, _c.c_int, _c.c_float]),
     ("dobb_state_tensor", _c.c_int, [_VP, _c.c_int, _c.c_int, _c.POINTER(_VP),
                                      _c.POINTER(_c.c_size_t)]),

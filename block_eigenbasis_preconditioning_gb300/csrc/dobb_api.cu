@@ -317,6 +317,7 @@ struct dobb_ctx {
   std::vector<int64_t> xmap_N;
   PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   bool any_tc = false;
+  bool any_wt = false;     // some matrix is registered output-side (DOBB_SIDE_OUTPUT)
   std::vector<float> check_host;
   std::vector<CUtensorMap> maps;
 
@@ -437,7 +438,7 @@ dobb_status do_step(dobb_handle h, void* const* W, const void* const* G, float l
   for (int i = 0; i < h->num; ++i)
     if ((reinterpret_cast<uintptr_t>(W[i]) | reinterpret_cast<uintptr_t>(G[i])) % 16 != 0) aligned = false;
   const bool l2 = h->norm == DOBB_NORM_L2;
-  const bool use_tc = h->path == 0 && aligned && !l2;
+  const bool use_tc = h->path == 0 && aligned && !l2 && !h->any_wt;
   for (const Chunk& ch : h->wl.chunks) {
     if (ch.step_n == 0) continue;
     StepArgs a{};
@@ -861,6 +862,26 @@ dobb_status dobb_set_normalization(dobb_handle h, int norm) {
       return fail(DOBB_ERR_UNSUPPORTED, "block too wide for the FP32 update kernel");
   }
   h->norm = norm;
+  return DOBB_OK;
+}
+
+dobb_status dobb_set_side(dobb_handle h, int matrix, int side, void* stream) {
+  if (!h) return fail(DOBB_ERR_INVALID_ARG, "NULL handle");
+  if (matrix < -1 || matrix >= h->num) return fail(DOBB_ERR_INVALID_ARG, "matrix %d out of range", matrix);
+  if (side != DOBB_SIDE_INPUT && side != DOBB_SIDE_OUTPUT)
+    return fail(DOBB_ERR_INVALID_ARG, "side must be DOBB_SIDE_INPUT or DOBB_SIDE_OUTPUT");
+  const int lo = matrix < 0 ? 0 : matrix, hi = matrix < 0 ? h->num : matrix + 1;
+  for (int i = lo; i < hi; ++i) {
+    if (side == DOBB_SIDE_OUTPUT && step_smem_for(h->info[i].k) > h->smem_limit)
+      return fail(DOBB_ERR_UNSUPPORTED, "block too wide for the FP32 update kernel");
+  }
+  for (int i = lo; i < hi; ++i) h->info[i].wt = side == DOBB_SIDE_OUTPUT ? 1 : 0;
+  h->any_wt = false;
+  for (const MatInfo& mi : h->info) h->any_wt = h->any_wt || mi.wt;
+  CUDA_TRY(cudaMemcpyAsync(h->dinfo() + lo, h->info.data() + lo, sizeof(MatInfo) * (size_t)(hi - lo),
+                           cudaMemcpyHostToDevice, static_cast<cudaStream_t>(stream)));
+  // the host copy is the source of an asynchronous transfer: finish it here
+  CUDA_TRY(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)));
   return DOBB_OK;
 }
 

@@ -34,7 +34,8 @@ struct MatInfo {
   int64_t qp_off;    // byte offset of block 0's packed operand images
   int64_t qblk_bytes;  // bytes of one block's packed images
   int32_t tc;        // 1 if the tensor-core update kernel handles this matrix
-  int32_t pad1;
+  int32_t wt;        // 1: the caller's W, G (and signs) are stored transposed
+                     //    (m_orig x n_orig row-major = this n x m problem's transpose)
 };
 
 // Extra arguments of the tensor-core update kernel.

@@ -82,15 +82,22 @@ __device__ __forceinline__ void project_pass(const float* Mg, const float* Qb, i
   }
 }
 
+// Offset of element (r, c) of the problem in the caller's W / G / sign
+// buffers: row-major m x n, or for an output-side ("Dobb-G") matrix the
+// caller's n x m buffer seen transposed.
+__device__ __forceinline__ int64_t pidx(const MatInfo& mi, int64_t r, int64_t c) {
+  return mi.wt ? c * mi.m + r : r * mi.n + c;
+}
+
 // M <- beta1 M + G on the rows of one tile; returns this thread's non-finite flag.
 template <typename PT>
-__device__ __forceinline__ int momentum_tile(float* Mg, const PT* G, float beta1, int64_t n,
+__device__ __forceinline__ int momentum_tile(float* Mg, const PT* G, float beta1, const MatInfo& mi,
                                              int64_t col0, int row0, int rows, int k) {
   int bad = 0;
   for (int e = threadIdx.x; e < rows * k; e += kThreads) {
     const int r = e / k, c = e % k;
-    const int64_t idx = (int64_t)(row0 + r) * n + col0 + c;
-    const float mn = fmaf(beta1, Mg[idx], load_f32(G + idx));
+    const int64_t idx = (int64_t)(row0 + r) * mi.n + col0 + c;
+    const float mn = fmaf(beta1, Mg[idx], load_f32(G + pidx(mi, row0 + r, col0 + c)));
     bad |= !isfinite(mn);
     Mg[idx] = mn;
   }
@@ -123,7 +130,7 @@ step_ffma_kernel(const __grid_constant__ StepArgs a) {
     float* Mc = Qs + kKC * kQS;
 
     // momentum (the l2 apply pass finds it updated by the norm pass)
-    const int bad = l2 ? 0 : momentum_tile(Mg, G, a.beta1, n, col0, row0, rows, k);
+    const int bad = l2 ? 0 : momentum_tile(Mg, G, a.beta1, mi, col0, row0, rows, k);
     __syncthreads();
 
     // project + normalise
@@ -149,7 +156,7 @@ step_ffma_kernel(const __grid_constant__ StepArgs a) {
           Ss[r * kp + j] = r < rows ? sv : 0.f;
           if (r < rows) {
             c2 = fmaf(acc[p][q], acc[p][q], c2);
-            if (Sout) Sout[(int64_t)(row0 + r) * n + col0 + j] = (int8_t)sign_of(acc[p][q]);
+            if (Sout) Sout[pidx(mi, row0 + r, col0 + j)] = (int8_t)sign_of(acc[p][q]);
           }
         }
       }
@@ -196,7 +203,7 @@ step_ffma_kernel(const __grid_constant__ StepArgs a) {
         for (int q = 0; q < 4; ++q) {
           const int r = rg * 4 + p, l = lc + cg * 4 + q;
           if (r < rows && l < k) {
-            const int64_t idx = (int64_t)(row0 + r) * n + col0 + l;
+            const int64_t idx = pidx(mi, row0 + r, col0 + l);
             store_f32(W + idx, fmaf(-a.lr_s, acc[p][q], load_f32(W + idx)));
             u2 = fmaf(acc[p][q], acc[p][q], u2);
           }
@@ -249,7 +256,7 @@ l2_norms_kernel(const __grid_constant__ StepArgs a) {
     const int rend = (int)min((int64_t)t.a + t.b, mi.m);
     for (int row0 = t.a; row0 < rend; row0 += kTM) {
       const int rows = rend - row0 < kTM ? rend - row0 : kTM;
-      bad |= momentum_tile(Mg, G, a.beta1, n, col0, row0, rows, k);
+      bad |= momentum_tile(Mg, G, a.beta1, mi, col0, row0, rows, k);
       __syncthreads();
 #pragma unroll
       for (int pass = 0; pass < kMaxPass; ++pass) {

@@ -11,7 +11,8 @@ from typing import List, Optional, Sequence, Tuple
 
 import torch
 
-from .binding import (DTYPES, NORMS, REFRESH_METHODS, TENSORS, _i64, _ptrs, check, load_library)
+from .binding import (DTYPES, NORMS, REFRESH_METHODS, SIDES, TENSORS, _i64, _ptrs, check,
+                      load_library)
 
 _TORCH_DTYPES = {"f32": torch.float32, "bf16": torch.bfloat16}
 
@@ -31,22 +32,36 @@ class Dobb:
     "bf16" as in the pages' principal setting), and the refresh method:
     "eigh" (complete eigendecomposition) or "orth" (orth_steps steps of
     orthogonal iteration with Cholesky QR, the pages' principal refresh), and
-    the coefficient normalisation norm: "sign" (Dobb) or "l2" (Dobb-l2)."""
+    the coefficient normalisation norm: "sign" (Dobb) or "l2" (Dobb-l2).
+
+    side ("input", "output", or one of them per matrix) picks the axis the
+    blocks cover: "input" is Dobb (blocks of W's n columns, accumulate takes
+    input activations N x n), "output" is Dobb-G (blocks of W's m rows,
+    accumulate takes output gradients N x m).  W, G and signs always keep
+    the caller's (m, n) layout; the library registers an output-side matrix
+    as its transpose, so its moments, bases and momentum views are those of
+    W^T (blocks of width m / B, momentum n x m)."""
 
     def __init__(self, shapes: Sequence[Tuple[int, int]], B: int, beta1: float = 0.95,
                  beta2: float = 0.99, refresh_period: int = 10, scale_s: float = 1.0,
                  param_dtype: str = "f32", act_dtype: str = "f32",
                  device: Optional[torch.device] = None, stream: Optional[torch.cuda.Stream] = None,
                  basis_dtype: str = "f32", refresh: str = "eigh", orth_steps: int = 1,
-                 norm: str = "sign"):
+                 norm: str = "sign", side="input"):
         self.lib = load_library()
         self.shapes = [(int(m), int(n)) for m, n in shapes]
+        self.sides = [side] * len(self.shapes) if isinstance(side, str) else list(side)
+        if len(self.sides) != len(self.shapes) or any(sd not in SIDES for sd in self.sides):
+            raise ValueError(f"side must be 'input', 'output' or one per matrix, got {side!r}")
+        # the problem the library sees: an output-side matrix is registered transposed
+        self.reg_shapes = [(n, m) if sd == "output" else (m, n)
+                           for (m, n), sd in zip(self.shapes, self.sides)]
         self.B = int(B)
         self.param_dtype = param_dtype
         self.act_dtype = act_dtype
         self.device = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
-        ms = _i64([s[0] for s in self.shapes])
-        ns = _i64([s[1] for s in self.shapes])
+        ms = _i64([s[0] for s in self.reg_shapes])
+        ns = _i64([s[1] for s in self.reg_shapes])
         nbytes = self.lib.dobb_state_bytes(len(self.shapes), ms, ns, self.B)
         if nbytes == 0:
             check(1)
@@ -69,6 +84,9 @@ class Dobb:
         self.norm = norm
         if norm != "sign":
             check(self.lib.dobb_set_normalization(h, NORMS[norm]))
+        for i, sd in enumerate(self.sides):
+            if sd != "input":
+                check(self.lib.dobb_set_side(h, i, SIDES[sd], _stream_ptr(stream)))
 
     # -- phases --------------------------------------------------------------
     def accumulate(self, X: Sequence[Optional[torch.Tensor]], stream=None) -> None:
@@ -93,7 +111,9 @@ class Dobb:
     # -- state access ----------------------------------------------------------
     def tensor(self, which: str, matrix: int = -1) -> torch.Tensor:
         """A view into the state buffer: moments / bases (B, k, k), eigvals
-        (B, k), momentum (m, n), flags (int32 per block), stats (blocks, 4)."""
+        (B, k), momentum (m, n), flags (int32 per block), stats (blocks, 4).
+        Shapes are those of the registered problem (W^T for an output-side
+        matrix)."""
         ptr = ctypes.c_void_p()
         nbytes = ctypes.c_size_t()
         check(self.lib.dobb_state_tensor(self.handle, TENSORS[which], int(matrix),
@@ -105,7 +125,7 @@ class Dobb:
         t = raw.view(torch.float32)
         if matrix < 0:
             return t
-        m, n = self.shapes[matrix]
+        m, n = self.reg_shapes[matrix]
         k = n // self.B
         if which in ("moments", "bases"):
             return t.view(self.B, k, k)

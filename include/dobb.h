@@ -147,6 +147,27 @@ dobb_status dobb_set_step(dobb_handle h, int64_t t);
 enum { DOBB_NORM_SIGN = 0, DOBB_NORM_L2 = 1 };
 dobb_status dobb_set_normalization(dobb_handle h, int norm);
 
+/* Which axis of a weight the blocks and moments cover ("Dobb", Tables
+ * 12-13).  `matrix` is an index, or -1 for every matrix.
+ * DOBB_SIDE_INPUT (default): Dobb.  The matrix registered as (m, n) is the
+ *   caller's W (m x n, row-major); blocks split its n input columns and
+ *   dobb_accumulate_moments takes input activations X (N x n).
+ * DOBB_SIDE_OUTPUT: "Dobb-G".  The matrix registered as (m, n) is the
+ *   TRANSPOSE of the caller's weight: W, G (and the optional sign output)
+ *   are n x m row-major buffers, i.e. a weight with n output rows and m
+ *   input columns; blocks split its n output rows, dobb_accumulate_moments
+ *   takes output gradients (N x n), and the update is C_b = Q_b^T M_b,
+ *   U_b = S_b' Q_b applied from the left (S_b' the normalised C_b, a sign
+ *   or, with DOBB_NORM_L2, each ROW of C_b scaled to l2 norm sqrt(m)).  The
+ *   momentum buffer (dobb_state_tensor) keeps the registered m x n layout,
+ *   i.e. the transpose of the caller's momentum.  Steps of a handle with any
+ *   output-side matrix run on the FP32 update kernel.
+ * Copies the per-matrix table on `stream` and waits for it.
+ * DOBB_ERR_INVALID_ARG for another side or a matrix out of range;
+ * DOBB_ERR_UNSUPPORTED for a block too wide for the FP32 update kernel. */
+enum { DOBB_SIDE_INPUT = 0, DOBB_SIDE_OUTPUT = 1 };
+dobb_status dobb_set_side(dobb_handle h, int matrix, int side, void* stream);
+
 /* Refresh method ("Dobb", Table 15).
  * DOBB_REFRESH_EIGH (default): complete eigendecomposition of every block,
  *   Q_b with A_b = Q_b Lambda_b Q_b^T (two-sided Jacobi), columns by

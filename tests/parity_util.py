@@ -59,6 +59,23 @@ def make_problem(shapes, N, eff, seed, param_dtype="f32", act_dtype="f32"):
     return Xs, Gs, Ws
 
 
+def make_output_side_problem(shapes, N, eff, seed, param_dtype="f32", act_dtype="f32"):
+    """Seeded inputs of the output-gradient side for a list of (m, n):
+    output gradients D (N x m) with a geometric-spectrum covariance, input
+    activations X (N x n), G = D^T X / N (a linear layer's weight gradient)
+    and W."""
+    rng = np.random.default_rng(seed)
+    Ds, Gs, Ws = [], [], []
+    for (m, n) in shapes:
+        D = I.activations(N, m, eff, rng, dtype=act_dtype)
+        X = I.activations(N, n, 0.5, rng)
+        g = (D.astype(np.float64).T @ X.astype(np.float64) / N).astype(np.float32)
+        Ds.append(D)
+        Gs.append(I.round_bf16_np(g) if param_dtype == "bf16" else g)
+        Ws.append(I.weights(m, n, rng, dtype=param_dtype))
+    return Ds, Gs, Ws
+
+
 def check_moments(opt, orc, matrices=None):
     worst = 0.0
     for i in (matrices if matrices is not None else range(len(orc.shapes))):
@@ -98,21 +115,26 @@ def check_bases(opt, A_ref_list, matrices=None):
 
 
 def check_update(W_prev, M_prev, G, Q_gpu, S_gpu, W_gpu, M_gpu, beta1, lr, s, param_dtype, k,
-                 basis_dtype="f32"):
+                 basis_dtype="f32", side="input"):
     """Score one matrix's update against the oracle run with the GPU basis
-    (rounded by the oracle itself when the basis is stored in bf16)."""
+    (rounded by the oracle itself when the basis is stored in bf16).  All
+    matrices in the caller's (m, n) layout; side "output" scores Dobb-G (row
+    blocks: the sign band is taken per row block of C)."""
     ref = O.update_from_bases(W_prev, M_prev, G, Q_gpu, beta1, lr, s, param_dtype,
-                              basis_dtype=basis_dtype)
+                              basis_dtype=basis_dtype, side=side)
     # momentum
     dm = np.abs(M_gpu - ref["M"]).max() / max(np.abs(ref["M"]).max(), 1e-30)
     assert dm <= 1e-6, f"momentum relative error {dm:.3e}"
     # signs
-    sa = MX.sign_agreement(ref["C"], S_gpu, k, TOL_SIGN_BAND)
+    if side == "output":
+        sa = MX.sign_agreement(ref["C"].T, np.asarray(S_gpu).T, k, TOL_SIGN_BAND)
+    else:
+        sa = MX.sign_agreement(ref["C"], S_gpu, k, TOL_SIGN_BAND)
     assert sa["outside_band"] == 0, f"{sa['outside_band']} sign flips outside the band"
     assert sa["fraction"] < TOL_SIGN_FRAC, f"sign disagreement fraction {sa['fraction']:.2e}"
     # parameters, scored with the GPU's signs at the tolerated entries
     ref2 = O.update_from_bases(W_prev, M_prev, G, Q_gpu, beta1, lr, s, "f32", S_override=S_gpu,
-                               basis_dtype=basis_dtype)
+                               basis_dtype=basis_dtype, side=side)
     if param_dtype == "f32":
         e = MX.w_rel_error(W_gpu, ref2["W"])
         assert e <= TOL_W, f"W max relative error {e:.3e}"
@@ -149,19 +171,21 @@ def l2_update_error_bound(M_new, Q, k, m):
 
 
 def check_update_l2(W_prev, M_prev, G, Q_gpu, W_gpu, M_gpu, beta1, lr, s, param_dtype,
-                    basis_dtype="f32"):
+                    basis_dtype="f32", side="input"):
     """Score a Dobb-l2 update (column l2 normalisation) against the oracle run
     with the GPU basis.  The normalised coefficients are continuous, so W is
     compared directly, in Frobenius norm, within lr s times the fp32 bound of
     `l2_update_error_bound` (plus, for bf16 parameters, half a bf16 quantum per
-    entry, 2^-8 |W|)."""
+    entry, 2^-8 |W|).  Side "output" (Dobb-G) normalises the rows of C: the
+    bound is that of the transposed problem."""
     ref = O.update_from_bases(W_prev, M_prev, G, Q_gpu, beta1, lr, s, "f32",
-                              basis_dtype=basis_dtype, norm="l2")
+                              basis_dtype=basis_dtype, norm="l2", side=side)
     dm = np.abs(M_gpu - ref["M"]).max() / max(np.abs(ref["M"]).max(), 1e-30)
     assert dm <= 1e-6, f"momentum relative error {dm:.3e}"
-    m, n = ref["W"].shape
+    Mt = ref["M"].T if side == "output" else ref["M"]
+    m = Mt.shape[0]
     k = Q_gpu.shape[1]
-    bound = lr * s * l2_update_error_bound(ref["M"], Q_gpu, k, m)
+    bound = lr * s * l2_update_error_bound(Mt, Q_gpu, k, m)
     if param_dtype == "bf16":
         bound += float(np.linalg.norm(2.0 ** -8 * np.abs(ref["W"])))
     err = float(np.linalg.norm(np.asarray(W_gpu, dtype=np.float64) - ref["W"]))

@@ -9,7 +9,7 @@ from oracle import dobb as O
 from oracle import metrics as MX
 
 from parity_util import (TOL_A, check_bases, check_moments, check_update, check_update_l2,
-                         make_problem, to_dev, to_np)
+                         make_output_side_problem, make_problem, to_dev, to_np)
 
 pytestmark = pytest.mark.gpu
 
@@ -519,3 +519,132 @@ def test_run_with_l2_normalisation_and_refresh():
             check_update_l2(W_prev[i], M_prev[i], to_np(Gd[i]), Q, to_np(Wd[i]),
                             to_np(opt.tensor("momentum", i)), 0.95, 0.02, 1.0, "f32")
             orc.M[i] = O.momentum(M_prev[i], to_np(Gd[i]), 0.95)
+
+
+# --------------------------------------------------------------------------
+# (f4) Dobb-G: bases of the output-gradient second moment, row blocks
+# ([Dobb, Tables 12-13]); W, G and signs in the caller's (m, n) layout
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("act", ["f32", "bf16"])
+def test_output_side_moments_match_oracle(act):
+    shapes, B = [(96, 24), (64, 33)], 2
+    Ds, _, _ = make_output_side_problem(shapes, 77, 0.3, seed=30, act_dtype=act)
+    opt = _dobb(shapes, B, beta2=0.9, refresh_period=0, act_dtype=act, side="output")
+    orc = O.DobbOracle(shapes, B, beta2=0.9, refresh_period=0, side="output")
+    for _ in range(2):
+        opt.accumulate([to_dev(d, act) for d in Ds])
+        orc.accumulate(Ds)
+    torch.cuda.synchronize()
+    for i, (m, n) in enumerate(shapes):
+        assert tuple(opt.tensor("moments", i).shape) == (B, m // B, m // B)
+    check_moments(opt, orc)
+
+
+@pytest.mark.parametrize("pdt", ["f32", "bf16"])
+@pytest.mark.parametrize("norm", ["sign", "l2"])
+@pytest.mark.parametrize("shapes,B", [
+    ([(96, 37)], 2),            # k = 48, ragged columns
+    ([(24, 1), (24, 17)], 3),   # n = 1, k = 8
+    ([(200, 130)], 2),          # k = 100
+    ([(400, 200)], 1),          # k = 400
+    ([(15, 9)], 5),             # k = 3 (odd)
+])
+def test_output_side_update_matches_oracle(pdt, norm, shapes, B):
+    N = max(256, 4 * max(m // B for m, _ in shapes))
+    Ds, Gs, Ws = make_output_side_problem(shapes, N, 0.2, seed=31, param_dtype=pdt)
+    opt = _dobb(shapes, B, beta1=0.9, beta2=0.95, refresh_period=1, scale_s=1.5, param_dtype=pdt,
+                norm=norm, side="output")
+    Wd = [to_dev(w, pdt) for w in Ws]
+    Gd = [to_dev(g, pdt) for g in Gs]
+    Sd = [torch.zeros(w.shape, dtype=torch.int8, device="cuda") for w in Ws]
+    W_prev = [to_np(w) for w in Wd]
+    opt.accumulate([to_dev(d, "f32") for d in Ds])
+    opt.step(Wd, Gd, 0.02, signs=Sd)
+    torch.cuda.synchronize()
+    st = opt.block_stats()
+    for i, (m, n) in enumerate(shapes):
+        k = m // B
+        Q = to_np(opt.tensor("bases", i))
+        M_gpu = to_np(opt.tensor("momentum", i)).T    # registered as W^T
+        if norm == "sign":
+            check_update(W_prev[i], np.zeros((m, n)), to_np(Gd[i]), Q, to_np(Sd[i]), to_np(Wd[i]),
+                         M_gpu, 0.9, 0.02, 1.5, pdt, k, side="output")
+        else:
+            check_update_l2(W_prev[i], np.zeros((m, n)), to_np(Gd[i]), Q, to_np(Wd[i]), M_gpu,
+                            0.9, 0.02, 1.5, pdt, side="output")
+            # sign output: the signs of C = Q_b^T M_b
+            ref = O.update_from_bases(W_prev[i], np.zeros((m, n)), to_np(Gd[i]), Q, 0.9, 0.02,
+                                      1.5, "f32", side="output")
+            sa = MX.sign_agreement(ref["C"].T, to_np(Sd[i]).T, k)
+            assert sa["outside_band"] == 0
+        # ||U_b||_F^2: number of nonzero signs, or k n for the row-l2 update
+        S = to_np(Sd[i])
+        for b in range(B):
+            want = np.count_nonzero(S[b * k:(b + 1) * k, :]) if norm == "sign" else n * k
+            assert abs(st[opt.block_offset(i) + b, 0] - want) <= 1e-4 * max(want, 1)
+
+
+def test_output_side_is_input_side_on_the_transpose():
+    """Dobb-G on W with output gradients D is Dobb on W^T with D as the
+    activations: both runs of the same registered problem agree bit for bit
+    (the FP32 update kernel in both)."""
+    m, n, B = 192, 80, 3
+    rng = np.random.default_rng(32)
+    W = I.weights(m, n, rng)
+    kw = dict(beta1=0.9, beta2=0.95, refresh_period=2, scale_s=1.0)
+    opt_g = _dobb([(m, n)], B, side="output", **kw)
+    opt_t = _dobb([(n, m)], B, **kw)
+    opt_t.set_step_path("ffma")
+    Wg, Wt = to_dev(W, "f32"), to_dev(W.T, "f32")
+    for _ in range(4):
+        D = I.activations(300, m, 0.25, rng)
+        X = I.activations(300, n, 0.5, rng)
+        G = (D.astype(np.float64).T @ X / 300).astype(np.float32)
+        opt_g.accumulate([to_dev(D, "f32")])
+        opt_t.accumulate([to_dev(D, "f32")])
+        opt_g.step([Wg], [to_dev(G, "f32")], 0.01)
+        opt_t.step([Wt], [to_dev(G.T, "f32")], 0.01)
+    torch.cuda.synchronize()
+    assert torch.equal(opt_g.tensor("bases", 0), opt_t.tensor("bases", 0))
+    assert torch.equal(opt_g.tensor("momentum", 0), opt_t.tensor("momentum", 0))
+    assert torch.equal(Wg, Wt.T)
+
+
+def test_mixed_sides_run_matches_oracle():
+    """One input-side and one output-side matrix in one handle, several steps
+    with refreshes; each scored against the oracle of its side."""
+    shapes, B = [(64, 96), (96, 64)], 2
+    sides = ["input", "output"]
+    rng = np.random.default_rng(33)
+    opt = _dobb(shapes, B, beta1=0.95, beta2=0.9, refresh_period=2, side=sides)
+    orcs = [O.DobbOracle([s], B, beta1=0.95, beta2=0.9, refresh_period=0, side=sd)
+            for s, sd in zip(shapes, sides)]
+    Wd = [to_dev(I.weights(m, n, rng), "f32") for m, n in shapes]
+    for t in range(5):
+        Xs = [I.activations(400, n if sd == "input" else m, 0.3, rng)
+              for (m, n), sd in zip(shapes, sides)]
+        Gs = [I.gradients(shapes[0][0], Xs[0], rng),
+              (Xs[1].astype(np.float64).T @ I.activations(400, shapes[1][1], 0.5, rng) / 400
+               ).astype(np.float32)]
+        Gd = [to_dev(g, "f32") for g in Gs]
+        Sd = [torch.zeros(w.shape, dtype=torch.int8, device="cuda") for w in Wd]
+        W_prev = [to_np(w) for w in Wd]
+        M_prev = [o.M[0].copy() for o in orcs]
+        opt.accumulate([to_dev(x, "f32") for x in Xs])
+        for o, X in zip(orcs, Xs):
+            o.accumulate([X])
+        opt.step(Wd, Gd, 0.02, signs=Sd)
+        torch.cuda.synchronize()
+        for i, ((m, n), sd) in enumerate(zip(shapes, sides)):
+            Ag = to_np(opt.tensor("moments", i))
+            rel = np.linalg.norm(Ag - orcs[i].A[0]) / np.linalg.norm(orcs[i].A[0])
+            assert rel <= TOL_A
+            if t % 2 == 0:
+                check_bases(opt, {i: Ag}, matrices=[i])
+            Q = to_np(opt.tensor("bases", i))
+            M_gpu = to_np(opt.tensor("momentum", i))
+            check_update(W_prev[i], M_prev[i], to_np(Gd[i]), Q, to_np(Sd[i]), to_np(Wd[i]),
+                         M_gpu.T if sd == "output" else M_gpu, 0.95, 0.02, 1.0, "f32",
+                         (m if sd == "output" else n) // B, side=sd)
+            orcs[i].M[0] = O.momentum(M_prev[i], to_np(Gd[i]), 0.95)
