@@ -415,7 +415,7 @@ step_tc_kernel(const __grid_constant__ StepArgs a, const __grid_constant__ TcArg
       for (int cc = 0; cc * 32 < kpN; ++cc) {
         float v[32];
         tmem_ld32(tc_row + 32 * cc, v);
-        tmem_wait_ld();
+        tmem_wait_ld(v);
         uint32_t pk[16];
 #pragma unroll
         for (int q = 0; q < 16; ++q) {
@@ -462,7 +462,7 @@ step_tc_kernel(const __grid_constant__ StepArgs a, const __grid_constant__ TcArg
           }
           float u[32];
           tmem_ld32(trow + 256 + kUCols * b + 32 * q, u);
-          tmem_wait_ld();
+          tmem_wait_ld(u);
           if (any) {
 #pragma unroll
             for (int e = 0; e < 8; ++e) {

@@ -186,7 +186,7 @@ syrk_tc_kernel(const __grid_constant__ SyrkTcArgs a) {
       for (int c0 = 0; c0 < Np; c0 += 32) {
         float v[32];
         tmem_ld32(trow + c0, v);
-        tmem_wait_ld();
+        tmem_wait_ld(v);
         if (rvalid) {
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
