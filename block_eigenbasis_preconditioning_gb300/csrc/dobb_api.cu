@@ -755,6 +755,7 @@ dobb_status dobb_accumulate_moments(dobb_handle h, const void* const* X, const i
         a->num_tiles = hi - lo;
         a->stages = syrk_tc_stages(kmax, h->smem_limit - 1024);
         a->stage_bytes = (int32_t)syrk_tc_stage_bytes(kmax);
+        a->dbuf = syrk_tc_double_buffer(kmax) ? 1 : 0;
         const size_t smem = syrk_tc_smem(kmax, a->stages);
         const int g = std::max(1, std::min(hi - lo, h->sm_count));
         cudaError_t e = launch_syrk_tc(*a, g, smem, s);

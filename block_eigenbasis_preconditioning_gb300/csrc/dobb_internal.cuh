@@ -82,6 +82,8 @@ struct SyrkTcArgs {
   float beta2;
   int32_t stages;
   int32_t stage_bytes;
+  int32_t dbuf;           // 1: every block fits 256 TMEM columns, two accumulators alternate
+  int32_t pad;
   const void* X[kMaxSyrkTcMat];
   int64_t N[kMaxSyrkTcMat];
   CUtensorMap maps[kMaxSyrkTcMat];
@@ -176,6 +178,7 @@ size_t syrk_tc_smem(int max_k, int stages);
 bool syrk_tc_eligible(int64_t n, int k);
 cudaError_t configure_syrk_tc(size_t smem_limit);
 cudaError_t launch_syrk_tc(const SyrkTcArgs& a, int grid, size_t smem, cudaStream_t s);
+bool syrk_tc_double_buffer(int max_k);  // two accumulators fit TMEM
 cudaError_t launch_init_bases(float* Q, float* lam, const MatInfo* info, const Tile* items,
                               int num_items, int grid, cudaStream_t s);
 

@@ -11,7 +11,9 @@
 //
 // Work unit: (matrix, block, 128-row slice of the block).  The epilogue
 // warps read D row by row from TMEM and write the EMA of the upper triangle
-// to both A[i][j] and A[j][i], so A stays exactly symmetric.
+// to both A[i][j] and A[j][i], so A stays exactly symmetric.  When every
+// block of a launch spans at most 256 columns, two accumulators alternate in
+// TMEM, so the next unit's products run while the epilogue drains the last.
 //
 // TMA needs a 16-byte aligned start column: a block starting at column b k
 // is loaded from column x0 = (b k) & ~7 and all indices shift by
@@ -36,7 +38,7 @@ constexpr int kMaxSyStages = 16;
 
 struct SySmem {
   uint64_t full[kMaxSyStages], empty[kMaxSyStages];
-  uint64_t d_full, d_free;
+  uint64_t d_full[2], d_free[2];
   uint32_t tmem_base;
   int abort;
 };
@@ -84,8 +86,10 @@ syrk_tc_kernel(const __grid_constant__ SyrkTcArgs a) {
       mbar_init(&sh->full[i], 1);
       mbar_init(&sh->empty[i], 1);
     }
-    mbar_init(&sh->d_full, 1);
-    mbar_init(&sh->d_free, 4);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sh->d_full[i], 1);
+      mbar_init(&sh->d_free[i], 4);
+    }
     sh->abort = 0;
     fence_mbar_init();
   }
@@ -122,13 +126,16 @@ syrk_tc_kernel(const __grid_constant__ SyrkTcArgs a) {
       const Tile tl = a.tiles[w];
       const SyTile s = sy_tile(a, tl);
       if (a.X[tl.mat - a.mat_base] == nullptr || s.N <= 0) continue;
-      // the accumulator must have been drained by the epilogue
-      if (tile_i > 0 && !warp_wait(&sh->d_free, (tile_i - 1) & 1)) {
+      // this unit's accumulator must have been drained by the epilogue
+      const uint32_t b = a.dbuf ? (tile_i & 1) : 0u;       // accumulator
+      const uint32_t use = a.dbuf ? (tile_i >> 1) : tile_i;  // earlier uses of it
+      if (use > 0 && !warp_wait(&sh->d_free[b], (use - 1) & 1)) {
         sh->abort = 1;
         atomicOr(a.err, 32u);
         break;
       }
       tc_fence_after();
+      const uint32_t dacc = tmem + 256 * b;
       const int Np = (s.ext + 15) & ~15;
       const int n0 = min(256, Np), n1 = Np - n0;
       // MN-major operands: transpose bits for A and B
@@ -146,7 +153,7 @@ syrk_tc_kernel(const __grid_constant__ SyrkTcArgs a) {
             const uint32_t koff = kk * 2048;  // 16 tokens x 128 B
             const uint64_t da = smem_desc(sb + (uint32_t)(2 * tl.a) * kBoxBytes + koff, lbo, 1024, kSw128);
             const uint64_t db0 = smem_desc(sb + koff, lbo, 1024, kSw128);
-            mma_f16_ss(tmem, da, db0, id0, first ? 0u : 1u);
+            mma_f16_ss(dacc, da, db0, id0, first ? 0u : 1u);
             if (n1 > 0) {
               const uint64_t db1 = smem_desc(sb + 4 * kBoxBytes + koff, lbo, 1024, kSw128);
               mma_f16_ss(tmem + 256, da, db1, id1, first ? 0u : 1u);
@@ -159,12 +166,15 @@ syrk_tc_kernel(const __grid_constant__ SyrkTcArgs a) {
         if (++st == (uint32_t)nst) { st = 0; ph ^= 1; }
       }
       if (!ok) { sh->abort = 1; atomicOr(a.err, 64u); break; }
-      if (lane == 0) tc_commit(&sh->d_full);
+      if (lane == 0) tc_commit(&sh->d_full[b]);
       __syncwarp();
       ++tile_i;
     }
-    // drain before TMEM is released
-    if (tile_i > 0) warp_wait(&sh->d_free, (tile_i - 1) & 1);
+    // drain before TMEM is released: the last use of each accumulator
+    for (uint32_t b = 0; b < 2; ++b) {
+      const uint32_t uses = a.dbuf ? (tile_i + 1 - b) / 2 : (b == 0 ? tile_i : 0u);
+      if (uses > 0) warp_wait(&sh->d_free[b], (uses - 1) & 1);
+    }
   } else {
     const int g = warp & 3;
     const int r = 32 * g + lane;  // row of the 128-row slice
@@ -175,7 +185,9 @@ syrk_tc_kernel(const __grid_constant__ SyrkTcArgs a) {
       const SyTile s = sy_tile(a, tl);
       if (a.X[tl.mat - a.mat_base] == nullptr || s.N <= 0) continue;
       const MatInfo mi = a.info[tl.mat];
-      if (!warp_wait(&sh->d_full, tile_i & 1)) { sh->abort = 1; atomicOr(a.err, 128u); break; }
+      const uint32_t b = a.dbuf ? (tile_i & 1) : 0u;
+      const uint32_t use = a.dbuf ? (tile_i >> 1) : tile_i;
+      if (!warp_wait(&sh->d_full[b], use & 1)) { sh->abort = 1; atomicOr(a.err, 128u); break; }
       tc_fence_after();
       const int i = 128 * tl.a + r - s.delta;  // row within the block
       const bool rvalid = i >= 0 && i < s.k;
@@ -185,7 +197,7 @@ syrk_tc_kernel(const __grid_constant__ SyrkTcArgs a) {
       const int Np = (s.ext + 15) & ~15;
       for (int c0 = 0; c0 < Np; c0 += 32) {
         float v[32];
-        tmem_ld32(trow + c0, v);
+        tmem_ld32(trow + 256 * b + c0, v);
         tmem_wait_ld(v);
         if (rvalid) {
 #pragma unroll
@@ -204,7 +216,7 @@ syrk_tc_kernel(const __grid_constant__ SyrkTcArgs a) {
         atomicOr(a.flags + mi.blk0 + tl.blk, (uint32_t)DOBB_FLAG_NONFINITE_X);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sh->d_free);
+      if (lane == 0) mbar_arrive(&sh->d_free[b]);
       ++tile_i;
     }
   }
@@ -233,6 +245,8 @@ int syrk_tc_stages(int max_k, size_t smem_limit) {
 size_t syrk_tc_smem(int max_k, int stages) {
   return 1024 + (size_t)stages * syrk_tc_stage_bytes(max_k) + sizeof(SySmem) + 64;
 }
+
+bool syrk_tc_double_buffer(int max_k) { return ((max_k + 7 + 15) & ~15) <= 256; }
 
 bool syrk_tc_eligible(int64_t n, int k) { return n % 8 == 0 && k <= kMaxTcK && k >= 8; }
 
