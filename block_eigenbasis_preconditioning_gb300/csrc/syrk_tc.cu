@@ -5,8 +5,9 @@
 //
 // D = X_b^T X_b is a contraction over tokens.  One TMA tile of X (64 tokens x
 // 64 features per box, 128-byte swizzle) is both MMA operands: A = X_b^T
-// (M = features of a 128-row slice, MN-major) and B = X_b (N = all features
-// of the block, MN-major).  bf16 x bf16 products are exact in fp32; the
+// (M = features of a 128-row slice, MN-major) and B = X_b (N = the block's
+// features from the slice's first one on: only the upper triangle of D is
+// needed, so later slices read fewer features), MN-major.  bf16 x bf16 products are exact in fp32; the
 // tensor core accumulates them in fp32 in TMEM.
 //
 // Work unit: (matrix, block, 128-row slice of the block).  The epilogue
@@ -56,6 +57,7 @@ struct SyTile {
   int64_t N, n;
   int k, delta, nbox, ext;  // ext = k + delta (features spanned)
   int x0;
+  int wbox, nboxw, Nw;      // the unit's feature window: first box, boxes, columns
 };
 
 __device__ __forceinline__ SyTile sy_tile(const SyrkTcArgs& a, const Tile& tl) {
@@ -69,6 +71,12 @@ __device__ __forceinline__ SyTile sy_tile(const SyrkTcArgs& a, const Tile& tl) {
   s.delta = (int)(c0 - s.x0);
   s.ext = s.k + s.delta;
   s.nbox = ((s.ext + 127) / 128) * 2;  // whole 128-feature slices
+  // slice a holds rows [128 a, 128 a + 128) of the extended block and needs
+  // only the columns at or right of them (the upper triangle): its window
+  // starts at its own first feature
+  s.wbox = 2 * tl.a;
+  s.nboxw = s.nbox - s.wbox;
+  s.Nw = ((s.ext + 15) & ~15) - 128 * tl.a;
   return s;
 }
 
@@ -112,10 +120,10 @@ syrk_tc_kernel(const __grid_constant__ SyrkTcArgs a) {
         const CUtensorMap* map = &a.maps[tl.mat - a.mat_base];
         for (int64_t t0 = 0; t0 < s.N; t0 += kTok) {
           if (!mbar_wait(&sh->empty[st], ph ^ 1)) { sh->abort = 1; atomicOr(a.err, 16u); break; }
-          mbar_arrive_expect_tx(&sh->full[st], (uint32_t)(s.nbox * kBoxBytes));
-          for (int q = 0; q < s.nbox; ++q)
-            tma_load_2d(base + (size_t)st * stage_bytes + q * kBoxBytes, map, s.x0 + 64 * q,
-                        (int)t0, &sh->full[st]);
+          mbar_arrive_expect_tx(&sh->full[st], (uint32_t)(s.nboxw * kBoxBytes));
+          for (int q = 0; q < s.nboxw; ++q)
+            tma_load_2d(base + (size_t)st * stage_bytes + q * kBoxBytes, map,
+                        s.x0 + 64 * (s.wbox + q), (int)t0, &sh->full[st]);
           if (++st == (uint32_t)nst) { st = 0; ph ^= 1; }
         }
       }
@@ -136,8 +144,7 @@ syrk_tc_kernel(const __grid_constant__ SyrkTcArgs a) {
       }
       tc_fence_after();
       const uint32_t dacc = tmem + 256 * b;
-      const int Np = (s.ext + 15) & ~15;
-      const int n0 = min(256, Np), n1 = Np - n0;
+      const int n0 = min(256, s.Nw), n1 = s.Nw - n0;
       // MN-major operands: transpose bits for A and B
       const uint32_t id0 = instr_desc(1, 128, n0) | (1u << 15) | (1u << 16);
       const uint32_t id1 = n1 > 0 ? (instr_desc(1, 128, n1) | (1u << 15) | (1u << 16)) : 0u;
@@ -151,7 +158,7 @@ syrk_tc_kernel(const __grid_constant__ SyrkTcArgs a) {
           const uint32_t lbo = kBoxBytes;  // next 64-feature box
           for (int kk = 0; kk < kTok / 16; ++kk) {
             const uint32_t koff = kk * 2048;  // 16 tokens x 128 B
-            const uint64_t da = smem_desc(sb + (uint32_t)(2 * tl.a) * kBoxBytes + koff, lbo, 1024, kSw128);
+            const uint64_t da = smem_desc(sb + koff, lbo, 1024, kSw128);  // the slice's own features
             const uint64_t db0 = smem_desc(sb + koff, lbo, 1024, kSw128);
             mma_f16_ss(dacc, da, db0, id0, first ? 0u : 1u);
             if (n1 > 0) {
@@ -194,15 +201,14 @@ syrk_tc_kernel(const __grid_constant__ SyrkTcArgs a) {
       float* Ab = a.A + mi.a_off + (int64_t)tl.blk * s.k * s.k;
       const float c1 = (1.f - a.beta2) / (float)s.N;
       int bad = 0;
-      const int Np = (s.ext + 15) & ~15;
-      for (int c0 = 0; c0 < Np; c0 += 32) {
+      for (int c0 = 0; c0 < s.Nw; c0 += 32) {
         float v[32];
         tmem_ld32(trow + 256 * b + c0, v);
         tmem_wait_ld(v);
         if (rvalid) {
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
-            const int j = c0 + e - s.delta;
+            const int j = 128 * tl.a + c0 + e - s.delta;
             if (j >= i && j < s.k) {
               bad |= !isfinite(v[e]);
               const float nv = fmaf(a.beta2, Ab[(int64_t)i * s.k + j], c1 * v[e]);
