@@ -202,8 +202,9 @@ WorkLists build_work(int num, const int64_t* m, const int64_t* n, int B) {
     for (auto& e : v) wl.tiles.push_back(e.second);
     wl.chunks.push_back(ch);
   }
-  // tensor-core accumulate: chunks of eligible matrices, tiles of 128 rows
-  // (the slice count depends on each block's misalignment to 8 columns)
+  // tensor-core accumulate: chunks of eligible matrices; a unit is a run of
+  // 128-row slices [a, b) of one block whose accumulators share TMEM (the
+  // slice count depends on each block's misalignment to 8 columns)
   {
     std::vector<int> elig;
     for (int i = 0; i < num; ++i)
@@ -213,15 +214,30 @@ WorkLists build_work(int num, const int64_t* m, const int64_t* n, int B) {
       sc.mat_base = elig[c0];
       std::vector<std::pair<int64_t, Tile>> v;
       size_t c1 = c0;
+      int kmax_wide = 0;
       while (c1 < elig.size() && elig[c1] - sc.mat_base < kMaxSyrkTcMat) {
-        const int i = elig[c1];
+        const int k = (int)(n[elig[c1]] / B);
+        if (k > kTcSmallK) kmax_wide = std::max(kmax_wide, k);
+        ++c1;
+      }
+      for (size_t c = c0; c < c1; ++c) {
+        const int i = elig[c];
         const int k = (int)(n[i] / B);
         sc.max_k = std::max(sc.max_k, k);
+        // TMEM columns a unit may use: one of two alternating accumulators,
+        // or all of TMEM (as in the kernel's launch of these blocks)
+        const int budget = syrk_tc_double_buffer(k > kTcSmallK ? kmax_wide : kTcSmallK) ? 256 : 512;
         for (int b = 0; b < B; ++b) {
           const int d = (int)(((int64_t)b * k) & 7);
-          for (int t = 0; 128 * t < k + d; ++t) v.push_back({(int64_t)k, Tile{i, b, t, 0}});
+          const int np = (k + d + 15) & ~15, ns = (k + d + 127) / 128;
+          for (int t0 = 0; t0 < ns;) {
+            int t1 = t0, cols = 0;
+            while (t1 < ns && cols + syrk_tc_slice_cols(np, t1) <= budget) cols += syrk_tc_slice_cols(np, t1++);
+            if (t1 == t0) t1 = t0 + 1;  // a first slice always fits its launch
+            v.push_back({(int64_t)k, Tile{i, b, t0, t1}});
+            t0 = t1;
+          }
         }
-        ++c1;
       }
       sc.mat_end = elig[c1 - 1] + 1;
       std::stable_sort(v.begin(), v.end(), [](auto& x, auto& y) { return x.first > y.first; });

@@ -73,7 +73,7 @@ constexpr int kMaxSyrkTcMat = 200;
 
 struct SyrkTcArgs {
   const MatInfo* info;
-  const Tile* tiles;      // (matrix, block, 128-row slice, 0)
+  const Tile* tiles;      // (matrix, block, first slice, end slice) of 128 rows
   int32_t num_tiles;
   int32_t mat_base;       // slot i of X / N / maps is matrix mat_base + i
   float* A;
@@ -179,6 +179,8 @@ bool syrk_tc_eligible(int64_t n, int k);
 cudaError_t configure_syrk_tc(size_t smem_limit);
 cudaError_t launch_syrk_tc(const SyrkTcArgs& a, int grid, size_t smem, cudaStream_t s);
 bool syrk_tc_double_buffer(int max_k);  // two accumulators fit TMEM
+// TMEM columns of slice t's accumulator (np: padded extended block width)
+__host__ __device__ inline int syrk_tc_slice_cols(int np, int t) { return (np - 128 * t + 31) & ~31; }
 cudaError_t launch_init_bases(float* Q, float* lam, const MatInfo* info, const Tile* items,
                               int num_items, int grid, cudaStream_t s);
 

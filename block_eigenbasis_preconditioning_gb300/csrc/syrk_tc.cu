@@ -56,8 +56,9 @@ __device__ __forceinline__ bool sy_aborted(const SySmem* sh) {
 struct SyTile {
   int64_t N, n;
   int k, delta, nbox, ext;  // ext = k + delta (features spanned)
-  int x0;
-  int wbox, nboxw, Nw;      // the unit's feature window: first box, boxes, columns
+  int x0, np;               // np: ext padded to 16
+  int t0, t1;               // the unit's slices [t0, t1)
+  int wbox, nboxw;          // the unit's feature window: first box, boxes
 };
 
 __device__ __forceinline__ SyTile sy_tile(const SyrkTcArgs& a, const Tile& tl) {
@@ -71,12 +72,14 @@ __device__ __forceinline__ SyTile sy_tile(const SyrkTcArgs& a, const Tile& tl) {
   s.delta = (int)(c0 - s.x0);
   s.ext = s.k + s.delta;
   s.nbox = ((s.ext + 127) / 128) * 2;  // whole 128-feature slices
-  // slice a holds rows [128 a, 128 a + 128) of the extended block and needs
-  // only the columns at or right of them (the upper triangle): its window
-  // starts at its own first feature
+  s.np = (s.ext + 15) & ~15;
+  // slice t holds rows [128 t, 128 t + 128) of the extended block and needs
+  // only the columns at or right of them (the upper triangle); a unit of
+  // slices [t0, t1) reads the window from its first slice's first feature
+  s.t0 = tl.a;
+  s.t1 = tl.b;
   s.wbox = 2 * tl.a;
   s.nboxw = s.nbox - s.wbox;
-  s.Nw = ((s.ext + 15) & ~15) - 128 * tl.a;
   return s;
 }
 
@@ -144,10 +147,6 @@ syrk_tc_kernel(const __grid_constant__ SyrkTcArgs a) {
       }
       tc_fence_after();
       const uint32_t dacc = tmem + 256 * b;
-      const int n0 = min(256, s.Nw), n1 = s.Nw - n0;
-      // MN-major operands: transpose bits for A and B
-      const uint32_t id0 = instr_desc(1, 128, n0) | (1u << 15) | (1u << 16);
-      const uint32_t id1 = n1 > 0 ? (instr_desc(1, 128, n1) | (1u << 15) | (1u << 16)) : 0u;
       bool ok = true;
       uint32_t first = 1;
       for (int64_t t0 = 0; t0 < s.N; t0 += kTok) {
@@ -156,17 +155,29 @@ syrk_tc_kernel(const __grid_constant__ SyrkTcArgs a) {
         if (lane == 0) {
           const uint32_t sb = smem_u32(base + (size_t)st * stage_bytes);
           const uint32_t lbo = kBoxBytes;  // next 64-feature box
-          for (int kk = 0; kk < kTok / 16; ++kk) {
-            const uint32_t koff = kk * 2048;  // 16 tokens x 128 B
-            const uint64_t da = smem_desc(sb + koff, lbo, 1024, kSw128);  // the slice's own features
-            const uint64_t db0 = smem_desc(sb + koff, lbo, 1024, kSw128);
-            mma_f16_ss(dacc, da, db0, id0, first ? 0u : 1u);
-            if (n1 > 0) {
-              const uint64_t db1 = smem_desc(sb + 4 * kBoxBytes + koff, lbo, 1024, kSw128);
-              mma_f16_ss(tmem + 256, da, db1, id1, first ? 0u : 1u);
+          // slice t: A = its own 128 features, B = the features from them
+          // on; accumulators side by side from column 0 of this unit's TMEM
+          uint32_t col = 0;
+          for (int t = s.t0; t < s.t1; ++t) {
+            const int nt = s.np - 128 * t;
+            const int n0 = min(256, nt), n1 = nt - n0;
+            // MN-major operands: transpose bits for A and B
+            const uint32_t id0 = instr_desc(1, 128, n0) | (1u << 15) | (1u << 16);
+            const uint32_t id1 = n1 > 0 ? (instr_desc(1, 128, n1) | (1u << 15) | (1u << 16)) : 0u;
+            const uint32_t sbt = sb + (uint32_t)(2 * (t - s.t0)) * kBoxBytes;
+            for (int kk = 0; kk < kTok / 16; ++kk) {
+              const uint32_t koff = kk * 2048;  // 16 tokens x 128 B
+              const uint64_t da = smem_desc(sbt + koff, lbo, 1024, kSw128);
+              const uint32_t acc = (first && kk == 0) ? 0u : 1u;  // the unit's first product
+              mma_f16_ss(dacc + col, da, da, id0, acc);
+              if (n1 > 0) {
+                const uint64_t db1 = smem_desc(sbt + 4 * kBoxBytes + koff, lbo, 1024, kSw128);
+                mma_f16_ss(dacc + col + 256, da, db1, id1, acc);
+              }
             }
-            first = 0;
+            col += (uint32_t)syrk_tc_slice_cols(s.np, t);
           }
+          first = 0;
           tc_commit(&sh->empty[st]);
         }
         __syncwarp();
@@ -196,27 +207,32 @@ syrk_tc_kernel(const __grid_constant__ SyrkTcArgs a) {
       const uint32_t use = a.dbuf ? (tile_i >> 1) : tile_i;
       if (!warp_wait(&sh->d_full[b], use & 1)) { sh->abort = 1; atomicOr(a.err, 128u); break; }
       tc_fence_after();
-      const int i = 128 * tl.a + r - s.delta;  // row within the block
-      const bool rvalid = i >= 0 && i < s.k;
       float* Ab = a.A + mi.a_off + (int64_t)tl.blk * s.k * s.k;
       const float c1 = (1.f - a.beta2) / (float)s.N;
       int bad = 0;
-      for (int c0 = 0; c0 < s.Nw; c0 += 32) {
-        float v[32];
-        tmem_ld32(trow + 256 * b + c0, v);
-        tmem_wait_ld(v);
-        if (rvalid) {
+      uint32_t col = 0;
+      for (int t = s.t0; t < s.t1; ++t) {
+        const int i = 128 * t + r - s.delta;  // row within the block
+        const bool rvalid = i >= 0 && i < s.k;
+        const int nt = s.np - 128 * t;
+        for (int c0 = 0; c0 < nt; c0 += 32) {
+          float v[32];
+          tmem_ld32(trow + 256 * b + col + c0, v);
+          tmem_wait_ld(v);
+          if (rvalid) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int j = 128 * tl.a + c0 + e - s.delta;
-            if (j >= i && j < s.k) {
-              bad |= !isfinite(v[e]);
-              const float nv = fmaf(a.beta2, Ab[(int64_t)i * s.k + j], c1 * v[e]);
-              Ab[(int64_t)i * s.k + j] = nv;
-              if (j != i) Ab[(int64_t)j * s.k + i] = nv;
+            for (int e = 0; e < 32; ++e) {
+              const int j = 128 * t + c0 + e - s.delta;
+              if (j >= i && j < s.k) {
+                bad |= !isfinite(v[e]);
+                const float nv = fmaf(a.beta2, Ab[(int64_t)i * s.k + j], c1 * v[e]);
+                Ab[(int64_t)i * s.k + j] = nv;
+                if (j != i) Ab[(int64_t)j * s.k + i] = nv;
+              }
             }
           }
         }
+        col += (uint32_t)syrk_tc_slice_cols(s.np, t);
       }
       if (__any_sync(0xffffffffu, bad) && lane == 0)
         atomicOr(a.flags + mi.blk0 + tl.blk, (uint32_t)DOBB_FLAG_NONFINITE_X);
