@@ -46,6 +46,7 @@ struct TcArgs {
   int32_t bstage;          // bytes of one B stage
   int32_t nbstage;         // B stages (2 ... 16)
   int32_t npieces;         // basis operand pieces: 2 (fp32 basis: hi, lo) or 1 (bf16 basis)
+  int32_t defer;           // 1: every block of the launch has kpN <= 128 (reconstructs deferred)
 };
 
 // One unit of grouped work: matrix, block and two phase-specific indices.

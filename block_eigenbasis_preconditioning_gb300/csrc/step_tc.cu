@@ -46,7 +46,7 @@ constexpr uint32_t kTmemCols = 512;
 struct TcSmem {
   uint64_t a_full[kAStages], a_conv[kAStages], a_empty[kAStages];
   uint64_t b_full[kMaxBStages], b_empty[kMaxBStages];
-  uint64_t c_full, s_full;
+  uint64_t c_full[2], s_full;   // c_full per C region (tile parity)
   uint64_t u_full[2], u_empty[2];
   uint64_t r_done, fin;
   uint32_t tmem_base;
@@ -135,7 +135,8 @@ step_tc_kernel(const __grid_constant__ StepArgs a, const __grid_constant__ TcArg
       mbar_init(&sh->b_full[i], 1);
       mbar_init(&sh->b_empty[i], 1);
     }
-    mbar_init(&sh->c_full, 1);
+    mbar_init(&sh->c_full[0], 1);
+    mbar_init(&sh->c_full[1], 1);
     mbar_init(&sh->s_full, 4);
     mbar_init(&sh->r_done, 1);
     mbar_init(&sh->fin, 1);
@@ -155,10 +156,33 @@ step_tc_kernel(const __grid_constant__ StepArgs a, const __grid_constant__ TcArg
   tc_fence_after();
   const uint32_t tmem = sh->tmem_base;
 
+  // Narrow blocks (C of two tiles fits the two halves of TMEM columns
+  // [0, 256)) defer each tile's reconstruct until the next tile's projection
+  // has been issued: the MMA warp then projects while the epilogue signs.
+  const bool defer = t.defer != 0;
   if (warp == 0) {
     // ------------------------------------------------------------ producer
+    // momentum chunks and basis images, the images in the order the MMA
+    // warp consumes them
     if (lane == 0) {
       uint32_t as = 0, ap = 0, bs = 0, bp = 0;
+      const unsigned char* pend_qr = nullptr;  // deferred reconstruct images
+      int pend_kpN = 0;
+      auto load_recon = [&](const unsigned char* qr, int kpN) {
+        // reconstruct operands: chunks of 128 output columns, 16-wide K steps
+        int64_t off = 0;
+        for (int c0 = 0; c0 < kpN && !aborted(sh); c0 += kUCols) {
+          const int nn = min(kUCols, kpN - c0);
+          const uint32_t bytes = (uint32_t)t.npieces * nn * 32u;
+          for (int s = 0; s < kpN / 16; ++s) {
+            if (!mbar_wait(&sh->b_empty[bs], bp ^ 1)) { raise(sh, t.err, 3); return; }
+            mbar_arrive_expect_tx(&sh->b_full[bs], bytes);
+            bulk_load(b_buf + bs * t.bstage, qr + off, bytes, &sh->b_full[bs]);
+            off += bytes;
+            if (++bs == nbs) { bs = 0; bp ^= 1; }
+          }
+        }
+      };
       for (int w = blockIdx.x; w < a.num_tiles && !aborted(sh); w += gridDim.x) {
         const Tile tl = a.tiles[w];
         const MatInfo mi = a.info[tl.mat];
@@ -183,27 +207,72 @@ step_tc_kernel(const __grid_constant__ StepArgs a, const __grid_constant__ TcArg
             if (++bs == nbs) { bs = 0; bp ^= 1; }
           }
         }
-        // reconstruct operands: chunks of 128 output columns, 16-wide K steps
-        int64_t off = 0;
-        for (int c0 = 0; c0 < kpN && !aborted(sh); c0 += kUCols) {
-          const int nn = min(kUCols, kpN - c0);
-          const uint32_t bytes = (uint32_t)t.npieces * nn * 32u;
-          for (int s = 0; s < kpN / 16; ++s) {
-            if (!mbar_wait(&sh->b_empty[bs], bp ^ 1)) { raise(sh, t.err, 3); break; }
-            mbar_arrive_expect_tx(&sh->b_full[bs], bytes);
-            bulk_load(b_buf + bs * t.bstage, qr + off, bytes, &sh->b_full[bs]);
-            off += bytes;
-            if (++bs == nbs) { bs = 0; bp ^= 1; }
-          }
+        if (defer) {
+          if (pend_qr) load_recon(pend_qr, pend_kpN);
+          pend_qr = qr;
+          pend_kpN = kpN;
+        } else {
+          load_recon(qr, kpN);
         }
       }
+      if (pend_qr && !aborted(sh)) load_recon(pend_qr, pend_kpN);
     }
   } else if (warp == 1) {
     // ----------------------------------------------------------------- MMA
     uint32_t as = 0, ap = 0, bs = 0, bp = 0, tile_i = 0;
     uint32_t uses[2] = {0, 0}, waited[2] = {0, 0}, ucount = 0;
     uint32_t r_issued = 0, r_waited = 0;     // reconstruct completions
-    uint32_t prev_lo = 0, prev_hi = 0;       // S columns of the previous tile
+    uint32_t prev_lo = 0, prev_hi = 0;       // S columns of the last reconstructed tile
+    // U = S Q^T for the tile whose signs are at columns [cb, cb + kpN / 2)
+    auto reconstruct = [&](uint32_t ti, uint32_t cb, int kpN) -> bool {
+      // wait for the signs in TMEM, then reconstruct U chunk by chunk
+      if (!warp_wait(&sh->s_full, ti & 1)) { raise(sh, t.err, 6); return false; }
+      tc_fence_after();
+      for (int c0 = 0; c0 < kpN; c0 += kUCols) {
+        const int nn = min(kUCols, kpN - c0);
+        const int b = ucount & 1;
+        while (waited[b] < uses[b]) {
+          if (!warp_wait(&sh->u_empty[b], waited[b] & 1)) { raise(sh, t.err, 7); return false; }
+          ++waited[b];
+        }
+        tc_fence_after();
+        const uint32_t idr = instr_desc(1, kTM, nn);
+        const uint32_t d = tmem + 256 + kUCols * b;
+        for (int s = 0; s < kpN / 16; ++s) {
+          if (!warp_wait(&sh->b_full[bs], bp)) { raise(sh, t.err, 7); return false; }
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t b_hi = smem_u32(b_buf + bs * t.bstage);
+            const uint32_t b_lo = b_hi + nn * 32;
+            mma_f16_ts(d, tmem + cb + 8 * s, smem_desc(b_hi, 16, 256, kSw32), idr, s == 0 ? 0u : 1u);
+            if (two) mma_f16_ts(d, tmem + cb + 8 * s, smem_desc(b_lo, 16, 256, kSw32), idr, 1u);
+            tc_commit(&sh->b_empty[bs]);
+          }
+          __syncwarp();
+          if (++bs == nbs) { bs = 0; bp ^= 1; }
+        }
+        if (lane == 0) tc_commit(&sh->u_full[b]);
+        __syncwarp();
+        ++uses[b];
+        ++ucount;
+      }
+      // completion of this tile's reconstruct MMAs (they read the signs).
+      // At most one phase of r_done is ever pending: retire the previous one
+      // before committing the next, so a parity wait cannot skip a phase.
+      if (r_issued > r_waited) {
+        if (!warp_wait(&sh->r_done, r_waited & 1)) { raise(sh, t.err, 12); return false; }
+        ++r_waited;
+      }
+      if (lane == 0) tc_commit(&sh->r_done);
+      __syncwarp();
+      ++r_issued;
+      prev_lo = cb;
+      prev_hi = cb + (uint32_t)(kpN / 2);
+      return true;
+    };
+    bool pending = false;                    // a projected tile awaits its reconstruct
+    uint32_t pend_ti = 0, pend_cb = 0;
+    int pend_kpN = 0;
     for (int w = blockIdx.x; w < a.num_tiles && !aborted(sh); w += gridDim.x, ++tile_i) {
       const Tile tl = a.tiles[w];
       const MatInfo mi = a.info[tl.mat];
@@ -222,7 +291,7 @@ step_tc_kernel(const __grid_constant__ StepArgs a, const __grid_constant__ TcArg
       if (!ok) { raise(sh, t.err, 4); break; }
       const uint32_t cb = c_base(kpN, tile_i);
       if (r_waited < r_issued && cb < prev_hi && prev_lo < cb + (uint32_t)kpN) {
-        // this tile's C would overwrite signs the previous reconstruct reads
+        // this tile's C would overwrite signs the last reconstruct reads
         if (!warp_wait(&sh->r_done, r_waited & 1)) { raise(sh, t.err, 11); break; }
         ++r_waited;
         tc_fence_after();
@@ -269,55 +338,19 @@ step_tc_kernel(const __grid_constant__ StepArgs a, const __grid_constant__ TcArg
         if (++as == kAStages) { as = 0; ap ^= 1; }
       }
       if (!ok) { raise(sh, t.err, 5); break; }
-      if (lane == 0) tc_commit(&sh->c_full);
+      if (lane == 0) tc_commit(&sh->c_full[tile_i & 1]);
       __syncwarp();
-      // wait for the signs in TMEM, then reconstruct U chunk by chunk
-      if (!warp_wait(&sh->s_full, tile_i & 1)) { raise(sh, t.err, 6); break; }
-      tc_fence_after();
-      for (int c0 = 0; c0 < kpN && ok; c0 += kUCols) {
-        const int nn = min(kUCols, kpN - c0);
-        const int b = ucount & 1;
-        while (waited[b] < uses[b]) {
-          if (!warp_wait(&sh->u_empty[b], waited[b] & 1)) { ok = false; break; }
-          ++waited[b];
-        }
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t idr = instr_desc(1, kTM, nn);
-        const uint32_t d = tmem + 256 + kUCols * b;
-        for (int s = 0; s < kpN / 16; ++s) {
-          if (!warp_wait(&sh->b_full[bs], bp)) { ok = false; break; }
-          tc_fence_after();
-          if (lane == 0) {
-            const uint32_t b_hi = smem_u32(b_buf + bs * t.bstage);
-            const uint32_t b_lo = b_hi + nn * 32;
-            mma_f16_ts(d, tmem + cb + 8 * s, smem_desc(b_hi, 16, 256, kSw32), idr, s == 0 ? 0u : 1u);
-            if (two) mma_f16_ts(d, tmem + cb + 8 * s, smem_desc(b_lo, 16, 256, kSw32), idr, 1u);
-            tc_commit(&sh->b_empty[bs]);
-          }
-          __syncwarp();
-          if (++bs == nbs) { bs = 0; bp ^= 1; }
-        }
-        if (!ok) break;
-        if (lane == 0) tc_commit(&sh->u_full[b]);
-        __syncwarp();
-        ++uses[b];
-        ++ucount;
+      if (defer) {
+        if (pending && !reconstruct(pend_ti, pend_cb, pend_kpN)) break;
+        pending = true;
+        pend_ti = tile_i;
+        pend_cb = cb;
+        pend_kpN = kpN;
+      } else if (!reconstruct(tile_i, cb, kpN)) {
+        break;
       }
-      if (!ok) { raise(sh, t.err, 7); break; }
-      // completion of this tile's reconstruct MMAs (they read the signs).
-      // At most one phase of r_done is ever pending: retire the previous one
-      // before committing the next, so a parity wait cannot skip a phase.
-      if (r_issued > r_waited) {
-        if (!warp_wait(&sh->r_done, r_waited & 1)) { raise(sh, t.err, 12); break; }
-        ++r_waited;
-      }
-      if (lane == 0) tc_commit(&sh->r_done);
-      __syncwarp();
-      ++r_issued;
-      prev_lo = cb;
-      prev_hi = cb + (uint32_t)(kpN / 2);
     }
+    if (pending && !aborted(sh)) reconstruct(pend_ti, pend_cb, pend_kpN);
     // let every issued MMA finish before TMEM is released
     if (lane == 0) tc_commit(&sh->fin);
     __syncwarp();
@@ -409,7 +442,7 @@ step_tc_kernel(const __grid_constant__ StepArgs a, const __grid_constant__ TcArg
       PT* W = static_cast<PT*>(a.W[slot]);
       int8_t* Sout = a.S[slot];
       float c2 = 0.f, u2 = 0.f;
-      if (!warp_wait(&sh->c_full, tile_i & 1)) { raise(sh, t.err, 9); break; }
+      if (!warp_wait(&sh->c_full[tile_i & 1], (tile_i >> 1) & 1)) { raise(sh, t.err, 9); break; }
       tc_fence_after();
       const uint32_t tc_row = trow + c_base(kpN, tile_i);
       for (int cc = 0; cc * 32 < kpN; ++cc) {
