@@ -494,12 +494,13 @@ dobb_status do_step(dobb_handle h, void* const* W, const void* const* G, float l
         t.qpack = h->pack();
         t.err = h->err();
         t.bstage = (int32_t)step_tc_bstage(kmax);
-        t.nbstage = step_tc_bstages(kmax, h->smem_limit);
+        t.nastage = step_tc_astages(kmax);
+        t.nbstage = step_tc_bstages(kmax, t.nastage, h->smem_limit);
         t.npieces = h->basis_bf16 ? 1 : 2;
         t.defer = ((kmax + 15) & ~15) <= 128 ? 1 : 0;
         if (t.nbstage < 2)
           return fail(DOBB_ERR_UNSUPPORTED, "block width %d leaves no room for operand stages", kmax);
-        const size_t smem = step_tc_smem(kmax, t.nbstage);
+        const size_t smem = step_tc_smem(kmax, t.nastage, t.nbstage);
         const int g = std::max(1, std::min(hi - lo, h->sm_count));
         cudaError_t e = launch_step_tc(at, t, h->pdt, g, smem, s);
         if (e != cudaSuccess) return fail(DOBB_ERR_CUDA, "tensor-core step launch: %s", cudaGetErrorString(e));

@@ -47,6 +47,8 @@ struct TcArgs {
   int32_t nbstage;         // B stages (2 ... 16)
   int32_t npieces;         // basis operand pieces: 2 (fp32 basis: hi, lo) or 1 (bf16 basis)
   int32_t defer;           // 1: every block of the launch has kpN <= 128 (reconstructs deferred)
+  int32_t nastage;         // momentum (A operand) stages (2 ... 4)
+  int32_t pad;
 };
 
 // One unit of grouped work: matrix, block and two phase-specific indices.
@@ -162,9 +164,10 @@ cudaError_t launch_orth(const EigArgs& a, int steps, int grid, cudaStream_t s);
 size_t orth_smem_bytes();
 cudaError_t configure_orth();
 cudaError_t configure_step(size_t smem_limit);
-size_t step_tc_smem(int max_k, int nbstage);
+size_t step_tc_smem(int max_k, int nastage, int nbstage);
 size_t step_tc_bstage(int max_k);
-int step_tc_bstages(int max_k, size_t smem_limit);  // B stages that fit (0: none)
+int step_tc_astages(int max_k);                                  // momentum stages for a launch
+int step_tc_bstages(int max_k, int nastage, size_t smem_limit);  // B stages that fit (0: none)
 int64_t tc_block_image_bytes(int k);
 bool tc_eligible(int64_t m, int64_t n, int k);
 cudaError_t configure_step_tc(size_t smem_limit);

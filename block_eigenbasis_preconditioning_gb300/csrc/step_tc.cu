@@ -37,14 +37,14 @@ using namespace ptx;
 
 constexpr int kThreads = 320;
 constexpr int kTM = 128;
-constexpr int kAStages = 2;
+constexpr int kMaxAStages = 4;   // momentum stages: the launch picks 2 ... 4
 constexpr int kMaxBStages = 16;  // the launch picks how many fit (small blocks: many)
 constexpr int kAChunkBytes = kTM * 32 * 4;  // 32 fp32 columns, 128B swizzle
 constexpr int kUCols = 128;
 constexpr uint32_t kTmemCols = 512;
 
 struct TcSmem {
-  uint64_t a_full[kAStages], a_conv[kAStages], a_empty[kAStages];
+  uint64_t a_full[kMaxAStages], a_conv[kMaxAStages], a_empty[kMaxAStages];
   uint64_t b_full[kMaxBStages], b_empty[kMaxBStages];
   uint64_t c_full[2], s_full;   // c_full per C region (tile parity)
   uint64_t u_full[2], u_empty[2];
@@ -118,15 +118,16 @@ step_tc_kernel(const __grid_constant__ StepArgs a, const __grid_constant__ TcArg
   // 1024-byte aligned operand region
   unsigned char* base = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
+  const int nas = t.nastage;                                     // momentum stages
   unsigned char* a_buf = base;                                   // [stage][hi|lo]
-  unsigned char* b_buf = base + kAStages * 2 * kAChunkBytes;     // [stage] t.bstage bytes
+  unsigned char* b_buf = base + nas * 2 * kAChunkBytes;          // [stage] t.bstage bytes
   TcSmem* sh = reinterpret_cast<TcSmem*>(b_buf + t.nbstage * t.bstage);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t nbs = (uint32_t)t.nbstage;  // B stages of this launch
   const bool two = t.npieces == 2;           // fp32 basis: hi and lo operand pieces
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kAStages; ++i) {
+    for (int i = 0; i < nas; ++i) {
       mbar_init(&sh->a_full[i], 1);
       mbar_init(&sh->a_conv[i], 4);
       mbar_init(&sh->a_empty[i], 1);
@@ -196,7 +197,7 @@ step_tc_kernel(const __grid_constant__ StepArgs a, const __grid_constant__ TcArg
           mbar_arrive_expect_tx(&sh->a_full[as], kAChunkBytes);
           tma_load_2d(a_buf + as * 2 * kAChunkBytes, map, tl.blk * k + kc * 32, tl.a,
                       &sh->a_full[as]);
-          if (++as == kAStages) { as = 0; ap ^= 1; }
+          if (++as == (uint32_t)nas) { as = 0; ap ^= 1; }
           for (int s4 = 0; s4 < 4; ++s4) {
             const int sub = kc * 4 + s4;
             if (sub >= nsub) break;
@@ -335,7 +336,7 @@ step_tc_kernel(const __grid_constant__ StepArgs a, const __grid_constant__ TcArg
         }
         if (lane == 0) tc_commit(&sh->a_empty[as]);
         __syncwarp();
-        if (++as == kAStages) { as = 0; ap ^= 1; }
+        if (++as == (uint32_t)nas) { as = 0; ap ^= 1; }
       }
       if (!ok) { raise(sh, t.err, 5); break; }
       if (lane == 0) tc_commit(&sh->c_full[tile_i & 1]);
@@ -419,7 +420,7 @@ step_tc_kernel(const __grid_constant__ StepArgs a, const __grid_constant__ TcArg
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sh->a_conv[as]);
-        if (++as == kAStages) { as = 0; ap ^= 1; }
+        if (++as == (uint32_t)nas) { as = 0; ap ^= 1; }
       }
       if (!ok) { raise(sh, t.err, 8); break; }
       if (__any_sync(0xffffffffu, bad) && lane == 0)
@@ -593,15 +594,23 @@ size_t step_tc_bstage(int max_k) {
   return (size_t)std::max(2 * kpN * 32, 2 * kUCols * 32);
 }
 
-size_t step_tc_smem(int max_k, int nbstage) {
-  return 1024 + (size_t)kAStages * 2 * kAChunkBytes + nbstage * step_tc_bstage(max_k) + sizeof(TcSmem) + 64;
+size_t step_tc_smem(int max_k, int nastage, int nbstage) {
+  return 1024 + (size_t)nastage * 2 * kAChunkBytes + nbstage * step_tc_bstage(max_k) + sizeof(TcSmem) + 64;
 }
 
-int step_tc_bstages(int max_k, size_t smem_limit) {
-  const size_t fixed = step_tc_smem(max_k, 0);
+// Momentum stages of a launch.
+int step_tc_astages(int max_k) { (void)max_k; return 2; }
+
+// Basis stages a launch uses at most.  Shared memory left unused stays L1
+// cache, which the per-row gradient and parameter accesses of the converter
+// and epilogue warps rely on.
+static int step_tc_bstage_cap(int max_k) { return max_k <= 128 ? 12 : 6; }
+
+int step_tc_bstages(int max_k, int nastage, size_t smem_limit) {
+  const size_t fixed = step_tc_smem(max_k, nastage, 0);
   const size_t per = step_tc_bstage(max_k);
   const int nb = smem_limit > fixed ? (int)((smem_limit - fixed) / per) : 0;
-  return std::min(kMaxBStages, nb);
+  return std::min(std::min(kMaxBStages, step_tc_bstage_cap(max_k)), nb);
 }
 
 int64_t tc_block_image_bytes(int k) {
