@@ -30,6 +30,7 @@ def _dobb(*a, **k):
     ([(5, 7)], 7, 3),                    # k = 1
     ([(40, 400)], 1, 70),                # k = 400: 7 x 7 tiles
     ([(16, 392), (12, 600)], 2, 300),    # k = 196 / 300, odd blocks 4 columns off: 2-3 slices
+    ([(24, 384)], 2, 200),               # k = 192 alone: two slices in one unit, two accumulators
 ])
 def test_moments_match_oracle(act, shapes, B, N):
     Xs, _, _ = make_problem(shapes, N, 0.3, seed=1, act_dtype=act)
