@@ -474,7 +474,20 @@ step_tc_kernel(const __grid_constant__ StepArgs a, const __grid_constant__ TcArg
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh->s_full);
+      // drain U piece by piece; the parameters of the next 32-column piece
+      // load while this one is applied
       bool ok = true;
+      float wn[32];
+      auto loadw = [&](int l0, float (&dst)[32]) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          float t4[4];
+          if (rvalid && l0 + 4 * e < k) load4(W + rowoff + l0 + 4 * e, t4);
+          else t4[0] = t4[1] = t4[2] = t4[3] = 0.f;
+          dst[4 * e] = t4[0]; dst[4 * e + 1] = t4[1]; dst[4 * e + 2] = t4[2]; dst[4 * e + 3] = t4[3];
+        }
+      };
+      loadw(0, wn);
       for (int c0 = 0; c0 < kpN; c0 += kUCols) {
         const int nn = min(kUCols, kpN - c0);
         const int b = ucount & 1;
@@ -484,16 +497,10 @@ step_tc_kernel(const __grid_constant__ StepArgs a, const __grid_constant__ TcArg
         for (int q = 0; q * 32 < nn; ++q) {
           const int l0 = c0 + 32 * q;
           float wv[32];
-          const bool any = rvalid && l0 < k;
-          if (any) {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              float t4[4];
-              if (l0 + 4 * e < k) load4(W + rowoff + l0 + 4 * e, t4);
-              else t4[0] = t4[1] = t4[2] = t4[3] = 0.f;
-              wv[4 * e] = t4[0]; wv[4 * e + 1] = t4[1]; wv[4 * e + 2] = t4[2]; wv[4 * e + 3] = t4[3];
-            }
-          }
+          for (int i = 0; i < 32; ++i) wv[i] = wn[i];
+          if (l0 + 32 < kpN) loadw(l0 + 32, wn);
+          const bool any = rvalid && l0 < k;
           float u[32];
           tmem_ld32(trow + 256 + kUCols * b + 32 * q, u);
           tmem_wait_ld(u);
