@@ -14,7 +14,7 @@
 //       by default), or the sweep rotated nothing, or off <= 1e-5 has
 //       stopped shrinking (the fp32 floor): after a sweep on a fresh B, off
 //       is the residual that the result will have
-//     while off > 1e-3 keep sweeping the same B (far from diagonal the
+//     while off > 3e-4 keep sweeping the same B (far from diagonal the
 //       rotations are large and a restart buys nothing); otherwise restart:
 //       V <- V + V (I - V^T V) / 2 (Newton-Schulz), B = V^T (A V); a B
 //       that has been swept twice is never trusted to end the iteration,
@@ -54,7 +54,7 @@ constexpr int kThreads = 256;
 #include "fp32_tiles.cuh"
 static_assert(kThreads == kTileThreads, "the tile products assume 256 threads");
 constexpr float kEps = 5.9604645e-8f;  // 2^-24, fp32 unit roundoff
-constexpr float kColdOff = 1e-3f;      // sweep the same B again while off(B) stays above this
+constexpr float kColdOff = 3e-4f;      // sweep the same B again while off(B) stays above this
 constexpr float kStopOff = 2e-6f;      // default: done when a fresh B's sweep leaves off(B) below this
 constexpr float kStallOff = 1e-5f;     // ... or leaves it below this without shrinking (fp32 floor)
 

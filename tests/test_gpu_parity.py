@@ -89,6 +89,22 @@ def test_refresh_on_spd_blocks_with_gaps(k):
     assert chk[:, 0].max() <= 1e-5 and chk[:, 2].max() <= 1e-5
 
 
+def test_refresh_on_a_1600_wide_stress_block():
+    """Refresh-stress shape at B = 4 / B = 1 (k = 1600): one SPD block with
+    every relative eigenvalue gap >= 1e-3 and condition number 1e6, solved
+    from the identity by one CTA."""
+    k = 1600
+    rng = np.random.default_rng(1600)
+    opt = _dobb([(4, k)], 1, refresh_period=0)
+    A = I.spd_with_gap(k, rng, cond=1e6)[0]
+    opt.tensor("moments", 0).copy_(torch.from_numpy(A.astype(np.float32)).view(1, k, k))
+    A32 = A.astype(np.float32).astype(np.float64)
+    opt.refresh()
+    torch.cuda.synchronize()
+    check_bases(opt, [A32[None]])
+    assert np.all(opt.block_flags() == 0)
+
+
 @pytest.mark.parametrize("k,eff", [(192, 0.15), (100, 0.10), (64, 0.40)])
 def test_refresh_on_accumulated_moments(k, eff):
     """Blocks of a low-effective-rank activation moment (ill-conditioned)."""
