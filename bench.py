@@ -454,6 +454,27 @@ def run_gpu(args):
     return 0
 
 
+def _bind_to_gpu_local_cpus(torch):
+    """Run this process on the host cores attached to the current GPU while the
+    pinned input buffers are allocated, so that their pages land in that
+    socket's memory (host buffers on the other socket cross the CPU-CPU link
+    on every copy).  Best effort: a system that does not expose the GPU's
+    local CPUs is left as is."""
+    try:
+        props = torch.cuda.get_device_properties(torch.cuda.current_device())
+        bus = "%04x:%02x:%02x.0" % (props.pci_domain_id, props.pci_bus_id, props.pci_device_id)
+        with open(f"/sys/bus/pci/devices/{bus}/local_cpulist") as f:
+            spec = f.read().strip()
+        cpus = set()
+        for part in spec.split(","):
+            lo, _, hi = part.partition("-")
+            cpus.update(range(int(lo), int(hi or lo) + 1))
+        if cpus:
+            os.sched_setaffinity(0, cpus)
+    except Exception:
+        pass
+
+
 def run_e2e(torch, opt, X, G, W, K, stream, params, world):
     """Each step copies that step's activations and gradients from pinned
     host memory, runs accumulate (+ refresh) + step through the public API,
@@ -461,8 +482,11 @@ def run_e2e(torch, opt, X, G, W, K, stream, params, world):
     step i+1 run on two copy streams into a second set of device buffers
     while step i computes (double buffering); a step's compute waits for its
     own inputs, and a buffer set is refilled only after the step that read it."""
+    prev_cpus = os.sched_getaffinity(0)
+    _bind_to_gpu_local_cpus(torch)
     Xh = [x.cpu().pin_memory() for x in X]
     Gh = [g.cpu().pin_memory() for g in G]
+    os.sched_setaffinity(0, prev_cpus)   # the pages are placed; the rest may use every core
     Xd = [[torch.empty_like(x) for x in X] for _ in range(2)]
     Gd = [[torch.empty_like(g) for g in G] for _ in range(2)]
     h2d = sum(x.numel() * x.element_size() for x in Xh) + sum(g.numel() * g.element_size() for g in Gh)
