@@ -93,6 +93,23 @@ def test_create_rejects_bad_arguments_without_device():
     assert lib.dobb_refresh_bases(None, None) == 5
     assert lib.dobb_num_blocks(None) == -1
     assert lib.dobb_checkpoint_bytes(None) == 0
+    # the variant setters validate the handle before anything else
+    assert lib.dobb_set_side(None, 0, 1, None) == 1
+    assert lib.dobb_set_normalization(None, 1) == 1
+    assert lib.dobb_set_refresh(None, 1, 1) == 1
+    assert lib.dobb_set_basis_dtype(None, 1, None) == 1
+    assert lib.dobb_last_error()
+
+
+def test_variant_names_match_the_header():
+    """The binding's variant tables carry the enum values the header declares."""
+    import re
+    hdr = open(os.path.join(ROOT, "include", "dobb.h")).read()
+    enums = dict((n, int(v)) for n, v in re.findall(r"(DOBB_[A-Z0-9_]+)\s*=\s*(\d+)", hdr))
+    assert binding.SIDES == {"input": enums["DOBB_SIDE_INPUT"], "output": enums["DOBB_SIDE_OUTPUT"]}
+    assert binding.NORMS == {"sign": enums["DOBB_NORM_SIGN"], "l2": enums["DOBB_NORM_L2"]}
+    assert binding.REFRESH_METHODS == {"eigh": enums["DOBB_REFRESH_EIGH"],
+                                       "orth": enums["DOBB_REFRESH_ORTH"]}
 
 
 def test_work_lists_cover_every_unit():
