@@ -162,7 +162,9 @@ dobb_status dobb_set_normalization(dobb_handle h, int norm);
  *   momentum buffer (dobb_state_tensor) keeps the registered m x n layout,
  *   i.e. the transpose of the caller's momentum.  Steps of a handle with any
  *   output-side matrix run on the FP32 update kernel.
- * Copies the per-matrix table on `stream` and waits for it.
+ * Copies the per-matrix table on `stream` and waits for it.  The side is
+ * configuration, like the normalisation and the refresh method: the state
+ * that dobb_get_state / dobb_set_state carry does not include it.
  * DOBB_ERR_INVALID_ARG for another side or a matrix out of range;
  * DOBB_ERR_UNSUPPORTED for a block too wide for the FP32 update kernel. */
 enum { DOBB_SIDE_INPUT = 0, DOBB_SIDE_OUTPUT = 1 };
