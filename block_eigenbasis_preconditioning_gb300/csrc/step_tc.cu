@@ -24,7 +24,8 @@
 //
 // TMEM columns: C at [0, kpN) during the projection, S (bf16 pairs) at
 // [0, kpN/2) afterwards, U chunks of 128 columns double-buffered at 256 and
-// 384.
+// 384.  Blocks with kpN <= 128 alternate C between [0, 128) and [128, 256),
+// which lets the MMA warp project tile t+1 before it reconstructs tile t.
 #include <cuda.h>
 
 #include "common.cuh"
