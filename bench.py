@@ -396,7 +396,7 @@ def run_gpu(args):
     hbm, bf16, peak_kind = _peaks()
     wm = work_model(shapes, B_BLOCKS, N_TOKENS, refresh=args.refresh, orth_steps=args.orth_steps,
                     norm=args.norm, sides=sides)
-    ffma_update = args.norm != "sign" or "output" in sides
+    ffma_update = args.norm != "sign"
     alu_peak_tflops = 152 * 128 * 2 * 2.07e9 / 1e12  # FP32 lanes x FMA x max SM clock
     phases = {
         "update": {"ms": upd_mean, "kernel": "step_ffma_kernel" if ffma_update else "step_tc_kernel",
@@ -553,8 +553,7 @@ def main():
                     help="coefficient normalisation: sign (Dobb) or l2 (Dobb-l2, FP32 kernels)")
     ap.add_argument("--side", default="input", choices=["input", "output"],
                     help="input: Dobb (blocks of the input axis, activation moments); output: "
-                         "Dobb-G (blocks of the output axis, output-gradient moments; FP32 "
-                         "update kernel)")
+                         "Dobb-G (blocks of the output axis, output-gradient moments)")
     ap.add_argument("--basis", default="f32", choices=["f32", "bf16"],
                     help="precision of the basis the update multiplies with (bf16: the "
                          "pages' principal storage setting)")

@@ -333,7 +333,6 @@ struct dobb_ctx {
   std::vector<int64_t> xmap_N;
   PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   bool any_tc = false;
-  bool any_wt = false;     // some matrix is registered output-side (DOBB_SIDE_OUTPUT)
   std::vector<float> check_host;
   std::vector<CUtensorMap> maps;
 
@@ -454,7 +453,7 @@ dobb_status do_step(dobb_handle h, void* const* W, const void* const* G, float l
   for (int i = 0; i < h->num; ++i)
     if ((reinterpret_cast<uintptr_t>(W[i]) | reinterpret_cast<uintptr_t>(G[i])) % 16 != 0) aligned = false;
   const bool l2 = h->norm == DOBB_NORM_L2;
-  const bool use_tc = h->path == 0 && aligned && !l2 && !h->any_wt;
+  const bool use_tc = h->path == 0 && aligned && !l2;
   for (const Chunk& ch : h->wl.chunks) {
     if (ch.step_n == 0) continue;
     StepArgs a{};
@@ -502,7 +501,9 @@ dobb_status do_step(dobb_handle h, void* const* W, const void* const* G, float l
           return fail(DOBB_ERR_UNSUPPORTED, "block width %d leaves no room for operand stages", kmax);
         const size_t smem = step_tc_smem(kmax, t.nastage, t.nbstage);
         const int g = std::max(1, std::min(hi - lo, h->sm_count));
-        cudaError_t e = launch_step_tc(at, t, h->pdt, g, smem, s);
+        bool may_t = false;
+        for (int i = ch.mat_base; i < ch.mat_end; ++i) may_t = may_t || h->info[i].wt;
+        cudaError_t e = launch_step_tc(at, t, h->pdt, may_t, g, smem, s);
         if (e != cudaSuccess) return fail(DOBB_ERR_CUDA, "tensor-core step launch: %s", cudaGetErrorString(e));
         ++h->launches;
       }
@@ -895,8 +896,6 @@ dobb_status dobb_set_side(dobb_handle h, int matrix, int side, void* stream) {
       return fail(DOBB_ERR_UNSUPPORTED, "block too wide for the FP32 update kernel");
   }
   for (int i = lo; i < hi; ++i) h->info[i].wt = side == DOBB_SIDE_OUTPUT ? 1 : 0;
-  h->any_wt = false;
-  for (const MatInfo& mi : h->info) h->any_wt = h->any_wt || mi.wt;
   CUDA_TRY(cudaMemcpyAsync(h->dinfo() + lo, h->info.data() + lo, sizeof(MatInfo) * (size_t)(hi - lo),
                            cudaMemcpyHostToDevice, static_cast<cudaStream_t>(stream)));
   // the host copy is the source of an asynchronous transfer: finish it here

@@ -171,8 +171,9 @@ int step_tc_bstages(int max_k, int nastage, size_t smem_limit);  // B stages tha
 int64_t tc_block_image_bytes(int k);
 bool tc_eligible(int64_t m, int64_t n, int k);
 cudaError_t configure_step_tc(size_t smem_limit);
-cudaError_t launch_step_tc(const StepArgs& a, const TcArgs& t, int param_dtype, int grid,
-                           size_t smem, cudaStream_t s);
+// may_t: some matrix of the launch has its W / G stored transposed (output side)
+cudaError_t launch_step_tc(const StepArgs& a, const TcArgs& t, int param_dtype, bool may_t,
+                           int grid, size_t smem, cudaStream_t s);
 cudaError_t launch_pack_bases(const float* Q, unsigned char* qpack, const MatInfo* info,
                               const Tile* items, int num_items, int npieces, int grid,
                               cudaStream_t s);

@@ -108,11 +108,42 @@ __device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16* p, const fl
   *reinterpret_cast<uint2*>(p) = t;
 }
 
+// Four consecutive columns of one row of a matrix whose caller's buffer is
+// the transpose (output side): elements `stride` apart.
+template <typename PT>
+__device__ __forceinline__ void load4_t(const PT* p, int64_t stride, float (&v)[4]);
+template <>
+__device__ __forceinline__ void load4_t<float>(const float* p, int64_t stride, float (&v)[4]) {
+#pragma unroll
+  for (int z = 0; z < 4; ++z) v[z] = p[z * stride];
+}
+template <>
+__device__ __forceinline__ void load4_t<__nv_bfloat16>(const __nv_bfloat16* p, int64_t stride,
+                                                      float (&v)[4]) {
+#pragma unroll
+  for (int z = 0; z < 4; ++z) v[z] = __bfloat162float(p[z * stride]);
+}
+template <typename PT>
+__device__ __forceinline__ void store4_t(PT* p, int64_t stride, const float (&v)[4]);
+template <>
+__device__ __forceinline__ void store4_t<float>(float* p, int64_t stride, const float (&v)[4]) {
+#pragma unroll
+  for (int z = 0; z < 4; ++z) p[z * stride] = v[z];
+}
+template <>
+__device__ __forceinline__ void store4_t<__nv_bfloat16>(__nv_bfloat16* p, int64_t stride,
+                                                       const float (&v)[4]) {
+#pragma unroll
+  for (int z = 0; z < 4; ++z) p[z * stride] = __float2bfloat16_rn(v[z]);
+}
+
 __device__ __forceinline__ uint32_t bf16_sign_bits(float x) {
   return x > 0.f ? 0x3F80u : (x < 0.f ? 0xBF80u : 0u);
 }
 
-template <typename PT>
+// kMayT: the launch may hold output-side matrices (caller's buffers
+// transposed); the instantiation without it carries none of that addressing.
+template <typename PT, bool kMayT>
 __global__ void __launch_bounds__(kThreads, 1)
 step_tc_kernel(const __grid_constant__ StepArgs a, const __grid_constant__ TcArgs t) {
   extern __shared__ __align__(1024) unsigned char smraw[];
@@ -386,7 +417,10 @@ step_tc_kernel(const __grid_constant__ StepArgs a, const __grid_constant__ TcArg
         for (int p = 0; p < 8; ++p) {
           const int r = crow + 16 * p;
           if (cvalid && row0 + r < mi.m) {
-            load4(G + (int64_t)(row0 + r) * n + (int64_t)tl.blk * k + col, g[p]);
+            if (kMayT && mi.wt)   // caller's G is the transpose: element (i, j) at j m + i
+              load4_t(G + ((int64_t)tl.blk * k + col) * mi.m + row0 + r, mi.m, g[p]);
+            else
+              load4(G + (int64_t)(row0 + r) * n + (int64_t)tl.blk * k + col, g[p]);
           } else {
             g[p][0] = g[p][1] = g[p][2] = g[p][3] = 0.f;
           }
@@ -441,6 +475,10 @@ step_tc_kernel(const __grid_constant__ StepArgs a, const __grid_constant__ TcArg
       const int64_t n = mi.n;
       const bool rvalid = tl.a + r < mi.m;
       const int64_t rowoff = (int64_t)(tl.a + r) * n + (int64_t)tl.blk * k;
+      // output side: the caller's W, G and signs are the transpose, element
+      // (i, j) at j m + i; this row's column 0 of the block is at colbase
+      const bool wt = kMayT && mi.wt != 0;
+      const int64_t colbase = (int64_t)tl.blk * k * mi.m + tl.a + r;
       PT* W = static_cast<PT*>(a.W[slot]);
       int8_t* Sout = a.S[slot];
       float c2 = 0.f, u2 = 0.f;
@@ -466,7 +504,9 @@ step_tc_kernel(const __grid_constant__ StepArgs a, const __grid_constant__ TcArg
           if (Sout) {
 #pragma unroll
             for (int i = 0; i < 32; ++i)
-              if (32 * cc + i < k) Sout[rowoff + 32 * cc + i] = (int8_t)sign_of(v[i]);
+              if (32 * cc + i < k)
+                Sout[wt ? colbase + (int64_t)(32 * cc + i) * mi.m : rowoff + 32 * cc + i] =
+                    (int8_t)sign_of(v[i]);
           }
         }
         tmem_st16(tc_row + 16 * cc, pk);
@@ -483,8 +523,12 @@ step_tc_kernel(const __grid_constant__ StepArgs a, const __grid_constant__ TcArg
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           float t4[4];
-          if (rvalid && l0 + 4 * e < k) load4(W + rowoff + l0 + 4 * e, t4);
-          else t4[0] = t4[1] = t4[2] = t4[3] = 0.f;
+          if (rvalid && l0 + 4 * e < k) {
+            if (wt) load4_t(W + colbase + (int64_t)(l0 + 4 * e) * mi.m, mi.m, t4);
+            else load4(W + rowoff + l0 + 4 * e, t4);
+          } else {
+            t4[0] = t4[1] = t4[2] = t4[3] = 0.f;
+          }
           dst[4 * e] = t4[0]; dst[4 * e + 1] = t4[1]; dst[4 * e + 2] = t4[2]; dst[4 * e + 3] = t4[3];
         }
       };
@@ -516,7 +560,8 @@ step_tc_kernel(const __grid_constant__ StepArgs a, const __grid_constant__ TcArg
                   u2 = fmaf(uu, uu, u2);
                   o[z] = fmaf(-a.lr_s, uu, wv[4 * e + z]);
                 }
-                store4(W + rowoff + l0 + 4 * e, o);
+                if (wt) store4_t(W + colbase + (int64_t)(l0 + 4 * e) * mi.m, mi.m, o);
+                else store4(W + rowoff + l0 + 4 * e, o);
               }
             }
           }
@@ -633,20 +678,25 @@ bool tc_eligible(int64_t m, int64_t n, int k) {
 }
 
 cudaError_t configure_step_tc(size_t smem_limit) {
-  cudaError_t e = cudaFuncSetAttribute(step_tc_kernel<float>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_limit);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(step_tc_kernel<__nv_bfloat16>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_limit);
+  const int lim = (int)smem_limit;
+  const auto attr = cudaFuncAttributeMaxDynamicSharedMemorySize;
+  cudaError_t e = cudaFuncSetAttribute(step_tc_kernel<float, false>, attr, lim);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(step_tc_kernel<float, true>, attr, lim);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(step_tc_kernel<__nv_bfloat16, false>, attr, lim);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(step_tc_kernel<__nv_bfloat16, true>, attr, lim);
+  return e;
 }
 
-cudaError_t launch_step_tc(const StepArgs& a, const TcArgs& t, int param_dtype, int grid,
-                           size_t smem, cudaStream_t s) {
+cudaError_t launch_step_tc(const StepArgs& a, const TcArgs& t, int param_dtype, bool may_t,
+                           int grid, size_t smem, cudaStream_t s) {
   if (a.num_tiles <= 0) return cudaSuccess;
-  if (param_dtype == kBF16)
-    step_tc_kernel<__nv_bfloat16><<<grid, kThreads, smem, s>>>(a, t);
-  else
-    step_tc_kernel<float><<<grid, kThreads, smem, s>>>(a, t);
+  if (param_dtype == kBF16) {
+    if (may_t) step_tc_kernel<__nv_bfloat16, true><<<grid, kThreads, smem, s>>>(a, t);
+    else step_tc_kernel<__nv_bfloat16, false><<<grid, kThreads, smem, s>>>(a, t);
+  } else {
+    if (may_t) step_tc_kernel<float, true><<<grid, kThreads, smem, s>>>(a, t);
+    else step_tc_kernel<float, false><<<grid, kThreads, smem, s>>>(a, t);
+  }
   return cudaGetLastError();
 }
 

@@ -160,8 +160,8 @@ dobb_status dobb_set_normalization(dobb_handle h, int norm);
  *   U_b = S_b' Q_b applied from the left (S_b' the normalised C_b, a sign
  *   or, with DOBB_NORM_L2, each ROW of C_b scaled to l2 norm sqrt(m)).  The
  *   momentum buffer (dobb_state_tensor) keeps the registered m x n layout,
- *   i.e. the transpose of the caller's momentum.  Steps of a handle with any
- *   output-side matrix run on the FP32 update kernel.
+ *   i.e. the transpose of the caller's momentum.  The update kernels read
+ *   and write the caller's buffers through the transposed index.
  * Copies the per-matrix table on `stream` and waits for it.  The side is
  * configuration, like the normalisation and the refresh method: the state
  * that dobb_get_state / dobb_set_state carry does not include it.

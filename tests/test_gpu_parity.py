@@ -603,30 +603,38 @@ def test_output_side_update_matches_oracle(pdt, norm, shapes, B):
             assert abs(st[opt.block_offset(i) + b, 0] - want) <= 1e-4 * max(want, 1)
 
 
-def test_output_side_is_input_side_on_the_transpose():
+@pytest.mark.parametrize("path,pdt", [("ffma", "f32"), ("auto", "f32"), ("auto", "bf16")])
+def test_output_side_is_input_side_on_the_transpose(path, pdt):
     """Dobb-G on W with output gradients D is Dobb on W^T with D as the
-    activations: both runs of the same registered problem agree bit for bit
-    (the FP32 update kernel in both)."""
+    activations: both runs of the same registered problem agree bit for bit,
+    on the FP32 update kernel and on the tensor-core one (k = 64: the
+    transposed parameter addressing is the only difference)."""
     m, n, B = 192, 80, 3
     rng = np.random.default_rng(32)
-    W = I.weights(m, n, rng)
-    kw = dict(beta1=0.9, beta2=0.95, refresh_period=2, scale_s=1.0)
+    W = I.weights(m, n, rng, dtype=pdt)
+    kw = dict(beta1=0.9, beta2=0.95, refresh_period=2, scale_s=1.0, param_dtype=pdt)
     opt_g = _dobb([(m, n)], B, side="output", **kw)
     opt_t = _dobb([(n, m)], B, **kw)
-    opt_t.set_step_path("ffma")
-    Wg, Wt = to_dev(W, "f32"), to_dev(W.T, "f32")
+    opt_g.set_step_path(path)
+    opt_t.set_step_path(path)
+    Wg, Wt = to_dev(W, pdt), to_dev(np.ascontiguousarray(W.T), pdt)
+    Sg = torch.zeros((m, n), dtype=torch.int8, device="cuda")
+    St = torch.zeros((n, m), dtype=torch.int8, device="cuda")
     for _ in range(4):
         D = I.activations(300, m, 0.25, rng)
         X = I.activations(300, n, 0.5, rng)
         G = (D.astype(np.float64).T @ X / 300).astype(np.float32)
+        if pdt == "bf16":
+            G = I.round_bf16_np(G)
         opt_g.accumulate([to_dev(D, "f32")])
         opt_t.accumulate([to_dev(D, "f32")])
-        opt_g.step([Wg], [to_dev(G, "f32")], 0.01)
-        opt_t.step([Wt], [to_dev(G.T, "f32")], 0.01)
+        opt_g.step([Wg], [to_dev(G, pdt)], 0.01, signs=[Sg])
+        opt_t.step([Wt], [to_dev(np.ascontiguousarray(G.T), pdt)], 0.01, signs=[St])
     torch.cuda.synchronize()
     assert torch.equal(opt_g.tensor("bases", 0), opt_t.tensor("bases", 0))
     assert torch.equal(opt_g.tensor("momentum", 0), opt_t.tensor("momentum", 0))
     assert torch.equal(Wg, Wt.T)
+    assert torch.equal(Sg, St.T)
 
 
 def test_mixed_sides_run_matches_oracle():
