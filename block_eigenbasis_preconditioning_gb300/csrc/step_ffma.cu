@@ -19,13 +19,14 @@
 namespace dobb {
 namespace {
 
-constexpr int kTM = 16;         // rows per tile
+constexpr int kTM = 32;         // rows per tile (the basis is staged once per tile and pass)
 constexpr int kThreads = 256;
 constexpr int kRG = kTM / 4;    // row groups (4 rows per thread)
 constexpr int kCG = kThreads / kRG;
-constexpr int kNC = kCG * 4;    // output columns per pass (256)
+constexpr int kNC = kCG * 4;    // output columns per pass (128)
 constexpr int kKC = 32;         // reduction chunk
 constexpr int kQS = kNC + 4;    // padded row of the Q stage
+constexpr int kL2MaxPass = 8;   // column passes of the l2 norm kernel
 
 __host__ __device__ __forceinline__ int pad16(int k) { return (k + 15) & ~15; }
 
@@ -233,7 +234,7 @@ __global__ void __launch_bounds__(kThreads)
 l2_norms_kernel(const __grid_constant__ StepArgs a) {
   extern __shared__ __align__(16) unsigned char smraw[];
   const int tid = threadIdx.x, cg = tid % kCG;
-  constexpr int kMaxPass = 4;  // k <= 4 kNC = 1024 (the FP32 path's widest block in this mode)
+  constexpr int kMaxPass = kL2MaxPass;  // k <= kMaxPass kNC = 1024 (the widest block in this mode)
   for (int w = blockIdx.x; w < a.num_tiles; w += gridDim.x) {
     const Tile t = a.tiles[w];
     const int slot = t.mat - a.mat_base;
@@ -297,7 +298,7 @@ l2_norms_kernel(const __grid_constant__ StepArgs a) {
 
 int step_rows_per_tile() { return kTM; }
 size_t step_smem_for(int k) { return smem_bytes(k); }
-int l2_max_k() { return 4 * kNC; }
+int l2_max_k() { return kL2MaxPass * kNC; }
 
 cudaError_t configure_step(size_t smem_limit) {
   cudaError_t e = cudaFuncSetAttribute(step_ffma_kernel<float>,
