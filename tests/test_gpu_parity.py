@@ -71,7 +71,7 @@ def test_moments_skip_null_and_flag_nonfinite():
 # (a2) eigen refresh
 # --------------------------------------------------------------------------
 
-@pytest.mark.parametrize("k", [1, 2, 3, 5, 16, 48, 100, 128, 168, 169, 192, 400])
+@pytest.mark.parametrize("k", [1, 2, 3, 5, 16, 48, 100, 128, 168, 169, 192, 400, 448])
 def test_refresh_on_spd_blocks_with_gaps(k):
     rng = np.random.default_rng(k)
     B = 2
