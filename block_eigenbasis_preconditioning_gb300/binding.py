@@ -65,8 +65,12 @@ SIGNATURES = [
     ("dobb_get_state", _c.c_int, [_VP, _VP, _c.c_size_t, _I64P, _VP]),
     ("dobb_set_state", _c.c_int, [_VP, _VP, _c.c_size_t, _c.c_int64, _VP]),
     ("dobb_launch_count", _c.c_int64, [_VP]),
+    ("dobb_describe_work", _c.c_int64, [_c.c_int, _I64P, _I64P, _c.c_int, _c.c_int, _I64P,
+                                        _c.c_int64]),
     ("dobb_set_step_path", _c.c_int, [_VP, _c.c_int]),
     ("dobb_sync_bases", _c.c_int, [_VP, _VP]),
+    ("dobb_peak_probe", _c.c_int, [_c.c_int, _VP, _c.c_size_t, _c.c_int,
+                                   _c.POINTER(_c.c_float), _c.POINTER(_c.c_double), _VP]),
     ("dobb_eigh_noalloc", _c.c_int, [_VP, _VP, _VP, _c.c_int, _c.c_int, _c.c_int,
                                      _c.POINTER(_c.c_uint32), _VP]),
     ("dobb_eigh_noalloc_last_error", _c.c_char_p, []),
@@ -112,6 +116,36 @@ def _i64(vals: Sequence[int]):
 
 def _ptrs(vals):
     return (ctypes.c_void_p * len(vals))(*[None if v is None else int(v) for v in vals])
+
+
+def describe_work(shapes: Sequence[Tuple[int, int]], B: int, phase: int):
+    """The scheduler's work list of one phase (see dobb_describe_work) as a
+    list of (launch, kind, mat_base, matrix, block, a, b) tuples."""
+    lib = load_library()
+    ms = _i64([s[0] for s in shapes])
+    ns = _i64([s[1] for s in shapes])
+    cnt = lib.dobb_describe_work(len(shapes), ms, ns, B, phase, None, 0)
+    if cnt < 0:
+        raise DobbError(1, lib.dobb_last_error().decode())
+    buf = (ctypes.c_int64 * (7 * max(cnt, 1)))()
+    lib.dobb_describe_work(len(shapes), ms, ns, B, phase, buf, cnt)
+    return [tuple(buf[7 * i:7 * i + 7]) for i in range(cnt)]
+
+
+PEAK_PROBES = {"ffma": 0, "mma_sync_tf32": 1, "tc_tf32": 2, "tc_bf16": 3}
+
+
+def peak_probe(which: str, scratch_ptr: int, scratch_bytes: int, iters: int, stream_ptr=None):
+    """One run of a throughput probe (see dobb_peak_probe): (ms, flops)."""
+    lib = load_library()
+    ms = ctypes.c_float()
+    fl = ctypes.c_double()
+    st = lib.dobb_peak_probe(PEAK_PROBES[which], ctypes.c_void_p(scratch_ptr),
+                             ctypes.c_size_t(scratch_bytes), int(iters), ctypes.byref(ms),
+                             ctypes.byref(fl), ctypes.c_void_p(stream_ptr) if stream_ptr else None)
+    if st != DOBB_OK:
+        raise DobbError(st, f"peak probe {which} failed")
+    return float(ms.value), float(fl.value)
 
 
 def state_bytes(shapes: Sequence[Tuple[int, int]], B: int) -> int:

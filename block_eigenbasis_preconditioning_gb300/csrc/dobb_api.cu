@@ -70,6 +70,7 @@ struct Chunk {
   int rest_off = 0, rest_n = 0;     // FFMA tiles of the other matrices
   int max_k_tc = 0, max_k_rest = 1;
   int syrk_off = 0, syrk_n = 0;
+  int syrk_rest_off = 0, syrk_rest_n = 0;  // FFMA moment tiles of matrices the tensor-core kernel skips
   int eig_off = 0, eig_n = 0;
   int l2_off = 0, l2_n = 0;         // column-l2 norm items: (matrix, block, row chunk)
   int max_k = 1;
@@ -89,7 +90,7 @@ struct WorkLists {
   std::vector<Tile> tiles;
   std::vector<Chunk> chunks;
   std::vector<SyrkChunk> syrk_tc;
-  int syrk_rest_off = 0, syrk_rest_n = 0;
+  int syrk_rest_total = 0;  // FFMA moment tiles over all chunks
   int blocks_off = 0, blocks_n = 0;  // every (matrix, block) once, by matrix
 };
 
@@ -250,20 +251,24 @@ WorkLists build_work(int num, const int64_t* m, const int64_t* n, int B) {
       wl.syrk_tc.push_back(sc);
       c0 = c1;
     }
-    // FFMA accumulate tiles of the matrices the tensor-core kernel skips
-    std::vector<std::pair<int64_t, Tile>> v;
-    for (int i = 0; i < num; ++i) {
-      const int k = (int)(n[i] / B);
-      if (syrk_tc_eligible(n[i], k)) continue;
-      const int nt = (k + ST - 1) / ST;
-      for (int b = 0; b < B; ++b)
-        for (int ti = 0; ti < nt; ++ti)
-          for (int tj = ti; tj < nt; ++tj) v.push_back({(int64_t)k, Tile{i, b, ti, tj}});
+    // FFMA accumulate tiles of the matrices the tensor-core kernel skips, per
+    // launch chunk (the pointer table of a launch holds kMaxMatPerLaunch)
+    for (Chunk& ch : wl.chunks) {
+      std::vector<std::pair<int64_t, Tile>> v;
+      for (int i = ch.mat_base; i < ch.mat_end; ++i) {
+        const int k = (int)(n[i] / B);
+        if (syrk_tc_eligible(n[i], k)) continue;
+        const int nt = (k + ST - 1) / ST;
+        for (int b = 0; b < B; ++b)
+          for (int ti = 0; ti < nt; ++ti)
+            for (int tj = ti; tj < nt; ++tj) v.push_back({(int64_t)k, Tile{i, b, ti, tj}});
+      }
+      std::stable_sort(v.begin(), v.end(), [](auto& x, auto& y) { return x.first > y.first; });
+      ch.syrk_rest_off = (int)wl.tiles.size();
+      ch.syrk_rest_n = (int)v.size();
+      wl.syrk_rest_total += ch.syrk_rest_n;
+      for (auto& e : v) wl.tiles.push_back(e.second);
     }
-    std::stable_sort(v.begin(), v.end(), [](auto& x, auto& y) { return x.first > y.first; });
-    wl.syrk_rest_off = (int)wl.tiles.size();
-    wl.syrk_rest_n = (int)v.size();
-    for (auto& e : v) wl.tiles.push_back(e.second);
   }
   wl.blocks_off = (int)wl.tiles.size();
   for (int i = 0; i < num; ++i)
@@ -723,8 +728,7 @@ dobb_status dobb_accumulate_moments(dobb_handle h, const void* const* X, const i
   for (int i = 0; i < h->num; ++i)
     if (X[i] && reinterpret_cast<uintptr_t>(X[i]) % 16 != 0) x_aligned = false;
   const bool use_tc = h->path == 0 && h->adt == DOBB_BF16 && h->encode && x_aligned &&
-                      !h->wl.syrk_tc.empty() &&
-                      (h->wl.syrk_rest_n == 0 || h->num <= kMaxMatPerLaunch);
+                      !h->wl.syrk_tc.empty();
   if (use_tc) {
     SyrkTcArgs* a = new SyrkTcArgs();
     for (const SyrkChunk& sc : h->wl.syrk_tc) {
@@ -786,25 +790,27 @@ dobb_status dobb_accumulate_moments(dobb_handle h, const void* const* X, const i
       }
     }
     delete a;
-    if (h->wl.syrk_rest_n == 0) return DOBB_OK;
-    // the matrices the tensor-core kernel does not cover (one FFMA launch;
-    // use_tc guarantees that all of them fit one pointer table)
-    AccArgs r{};
-    r.info = h->dinfo();
-    r.tiles = h->dtiles() + h->wl.syrk_rest_off;
-    r.num_tiles = h->wl.syrk_rest_n;
-    r.mat_base = 0;
-    r.A = h->A();
-    r.flags = h->flags();
-    r.beta2 = h->beta2;
-    for (int i = 0; i < h->num; ++i) {
-      r.X[i] = X[i];
-      r.N[i] = X[i] ? N[i] : 0;
+    // the matrices the tensor-core kernel does not cover: one FFMA launch per
+    // chunk that has any
+    for (const Chunk& ch : h->wl.chunks) {
+      if (ch.syrk_rest_n == 0) continue;
+      AccArgs r{};
+      r.info = h->dinfo();
+      r.tiles = h->dtiles() + ch.syrk_rest_off;
+      r.num_tiles = ch.syrk_rest_n;
+      r.mat_base = ch.mat_base;
+      r.A = h->A();
+      r.flags = h->flags();
+      r.beta2 = h->beta2;
+      for (int i = ch.mat_base; i < ch.mat_end; ++i) {
+        r.X[i - ch.mat_base] = X[i];
+        r.N[i - ch.mat_base] = X[i] ? N[i] : 0;
+      }
+      const int g = std::max(1, std::min(r.num_tiles, h->sm_count * 4));
+      cudaError_t e = launch_syrk_ema(r, h->adt, g, s);
+      if (e != cudaSuccess) return fail(DOBB_ERR_CUDA, "accumulate launch: %s", cudaGetErrorString(e));
+      ++h->launches;
     }
-    const int g = std::max(1, std::min(r.num_tiles, h->sm_count * 4));
-    cudaError_t e = launch_syrk_ema(r, h->adt, g, s);
-    if (e != cudaSuccess) return fail(DOBB_ERR_CUDA, "accumulate launch: %s", cudaGetErrorString(e));
-    ++h->launches;
     return DOBB_OK;
   }
   for (const Chunk& ch : h->wl.chunks) {
@@ -1047,6 +1053,77 @@ dobb_status dobb_set_state(dobb_handle h, const void* src_dev, size_t src_bytes,
 }
 
 int64_t dobb_launch_count(dobb_handle h) { return h ? h->launches : -1; }
+
+int64_t dobb_describe_work(int num_matrices, const int64_t* m, const int64_t* n, int B, int phase,
+                           int64_t* out, int64_t cap) {
+  if (!validate_shapes(num_matrices, m, n, B)) return -1;
+  if (phase < 0 || phase > 2) {
+    fail(DOBB_ERR_INVALID_ARG, "phase must be 0 (update), 1 (moments) or 2 (refresh)");
+    return -1;
+  }
+  const WorkLists wl = build_work(num_matrices, m, n, B);
+  const int TM = step_rows_per_tile();
+  int64_t cnt = 0;
+  int64_t launch = 0;
+  auto emit = [&](int64_t kind, int64_t base, const Tile& t, int64_t a, int64_t b) {
+    if (out && cnt < cap) {
+      int64_t* e = out + 7 * cnt;
+      e[0] = launch; e[1] = kind; e[2] = base; e[3] = t.mat; e[4] = t.blk; e[5] = a; e[6] = b;
+    }
+    ++cnt;
+  };
+  if (phase == 0) {
+    for (const Chunk& ch : wl.chunks) {
+      // the default path: tensor-core launches (wide, narrow), then the FFMA rest
+      for (int part = 0; part < 2; ++part) {
+        const int lo = part == 0 ? 0 : ch.tc_small, hi = part == 0 ? ch.tc_small : ch.tc_n;
+        if (hi <= lo) continue;
+        for (int j = lo; j < hi; ++j) {
+          const Tile& t = wl.tiles[ch.tc_off + j];
+          emit(0, ch.mat_base, t, t.a, std::min<int64_t>(kTcRows, m[t.mat] - t.a));
+        }
+        ++launch;
+      }
+      if (ch.tc_n > 0 ? ch.rest_n > 0 : ch.step_n > 0) {
+        const int off = ch.tc_n > 0 ? ch.rest_off : ch.step_off;
+        const int num = ch.tc_n > 0 ? ch.rest_n : ch.step_n;
+        for (int j = 0; j < num; ++j) {
+          const Tile& t = wl.tiles[off + j];
+          emit(1, ch.mat_base, t, t.a, std::min<int64_t>(TM, m[t.mat] - t.a));
+        }
+        ++launch;
+      }
+    }
+  } else if (phase == 1) {
+    // bf16 activations: tensor-core launches per chunk (wide, narrow), then one
+    // FFMA launch over the matrices the tensor-core kernel does not take
+    for (const SyrkChunk& sc : wl.syrk_tc) {
+      for (int part = 0; part < 2; ++part) {
+        const int lo = part == 0 ? 0 : sc.small, hi = part == 0 ? sc.small : sc.n;
+        if (hi <= lo) continue;
+        for (int j = lo; j < hi; ++j) {
+          const Tile& t = wl.tiles[sc.off + j];
+          emit(0, sc.mat_base, t, t.a, t.b);
+        }
+        ++launch;
+      }
+    }
+    for (const Chunk& ch : wl.chunks) {
+      if (ch.syrk_rest_n == 0) continue;
+      for (int j = 0; j < ch.syrk_rest_n; ++j) {
+        const Tile& t = wl.tiles[ch.syrk_rest_off + j];
+        emit(1, ch.mat_base, t, t.a, t.b);
+      }
+      ++launch;
+    }
+  } else {
+    for (const Chunk& ch : wl.chunks) {
+      for (int j = 0; j < ch.eig_n; ++j) emit(0, ch.mat_base, wl.tiles[ch.eig_off + j], 0, 0);
+      if (ch.eig_n > 0) ++launch;
+    }
+  }
+  return cnt;
+}
 
 dobb_status dobb_set_step_path(dobb_handle h, int path) {
   if (!h || path < 0 || path > 1) return fail(DOBB_ERR_INVALID_ARG, "path must be 0 or 1");

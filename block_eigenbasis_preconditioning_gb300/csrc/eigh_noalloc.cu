@@ -1,20 +1,19 @@
 // Block eigendecomposition for callers that cannot allocate device memory.
 //
-// Some callers of this library cannot call cudaMalloc at all: code running
-// inside a CUDA-graph-captured region that must not allocate, inference or
+// Some callers of this library cannot call cudaMalloc at all: inference or
 // embedded runtimes whose memory is fully reserved up front by an arena they
 // do not control, and plugins hosted by frameworks that forbid allocations
 // outside their own allocator.  They still want the exact block
 // eigendecomposition the optimizer refresh computes.  dobb_eigh_noalloc runs
-// the same eigensolver kernels on caller-provided inputs and outputs and keeps
+// the same eigensolver kernel (restarted Rayleigh-Ritz two-sided Jacobi,
+// started from the identity) on caller-provided inputs and outputs and keeps
 // its working memory in file-scope __device__ arrays of a fixed maximum size,
 // which every GPU that loads the library holds until the process exits.
 //
 // The arrays are shared by every call: calls whose work overlaps on the GPU
 // (different streams, or different host threads) race.  Set-up per device
 // (cudaGetSymbolAddress of each array, kernel attributes) happens on the
-// first call on that device, under a lock; that first call should come
-// before any stream capture.
+// first call on that device, under a lock.
 #include <algorithm>
 #include <mutex>
 #include <string>
@@ -106,6 +105,18 @@ extern "C" dobb_status dobb_eigh_noalloc(const float* A_dev, float* Q_dev, float
   if (!A_dev || !Q_dev || !lam_dev) return noalloc_fail(DOBB_ERR_INVALID_ARG, "NULL pointer argument");
   if (k < 1 || k > kNoAllocMaxK) return noalloc_fail(DOBB_ERR_INVALID_ARG, "k must lie in [1, 1024]");
   if (count < 0) return noalloc_fail(DOBB_ERR_INVALID_ARG, "count must be >= 0");
+  {
+    // the basis is set to the identity before the solver reads A: outputs
+    // that overlap the input would corrupt it
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(A_dev);
+    const uintptr_t a1 = a0 + sizeof(float) * (size_t)count * k * k;
+    const uintptr_t q0 = reinterpret_cast<uintptr_t>(Q_dev);
+    const uintptr_t q1 = q0 + sizeof(float) * (size_t)count * k * k;
+    const uintptr_t l0 = reinterpret_cast<uintptr_t>(lam_dev);
+    const uintptr_t l1 = l0 + sizeof(float) * (size_t)count * k;
+    if (count > 0 && ((q0 < a1 && a0 < q1) || (l0 < a1 && a0 < l1)))
+      return noalloc_fail(DOBB_ERR_INVALID_ARG, "Q_dev and lam_dev must not overlap A_dev");
+  }
   if (count > kNoAllocMaxBlocks)
     return noalloc_fail(DOBB_ERR_INVALID_ARG, "count exceeds the 4096 blocks the fixed work list holds");
   if ((size_t)count * 3 * (size_t)k * k > kNoAllocScratchFloats)

@@ -234,6 +234,22 @@ dobb_status dobb_set_state(dobb_handle h, const void* src_dev, size_t src_bytes,
 /* Number of kernel launches issued by this handle since creation (host count). */
 int64_t dobb_launch_count(dobb_handle h);
 
+/* Host-side view of the grouped work lists (the scheduler) of a handle over
+ * this matrix set; needs no device.  phase 0: the update tiles of a step on
+ * the default path (tensor-core launches, then the FFMA rest); 1: the moment
+ * units of an accumulate with bf16 activations; 2: the eigen items of a
+ * refresh.  Writes min(count, cap) entries of 7 int64 to `out` (may be NULL):
+ *   (launch, kind, mat_base, matrix, block, a, b)
+ * launch = index of the launch in the phase's sequence, kind = 0 for the
+ * tensor-core kernel (phase 0, 1) or the eigensolver (2) and 1 for the FFMA
+ * kernel, mat_base = the matrix in slot 0 of that launch's pointer table;
+ * (a, b) = (first row, rows) for update tiles, (first, end) 128-row slice of
+ * a tensor-core moment unit, (row, column) 64-tile of an FFMA moment tile,
+ * (0, 0) for eigen items.  Returns the number of entries, -1 on bad
+ * arguments (see dobb_last_error). */
+int64_t dobb_describe_work(int num_matrices, const int64_t* m, const int64_t* n, int B,
+                           int phase, int64_t* out, int64_t cap);
+
 /* Update-kernel selection: 0 (default) runs the tcgen05 tensor-core kernel for
  * every matrix with k % 4 == 0 and k <= 448 (and 16-byte aligned W, G) and the
  * FP32 FFMA kernel for the rest; 1 runs the FFMA kernel for all matrices.
@@ -245,24 +261,37 @@ dobb_status dobb_set_step_path(dobb_handle h, int path);
  * and dobb_set_state do this themselves. */
 dobb_status dobb_sync_bases(dobb_handle h, void* stream);
 
+/* Throughput probe for the roofline denominators (the pages have no
+ * counterpart): one launch of one instruction stream on every SM,
+ *   which 0: FP32 FFMA, 1: TF32 mma.sync (m16n8k8), 2: TF32 tcgen05.mma
+ *   (128 x 256 x 8), 3: BF16 tcgen05.mma (128 x 256 x 16);
+ * `iters` scales the work.  scratch_dev: caller device memory of at least
+ * 4 * (sms * 2048) + 256 bytes for the results (which mean nothing).
+ * Synchronises `stream`; returns the launch's event time in ms and its exact
+ * flop count (2 per multiply-add). */
+dobb_status dobb_peak_probe(int which, void* scratch_dev, size_t scratch_bytes, int iters,
+                            float* ms_out, double* flops_out, void* stream);
+
 /* ------------------------------------------------------------------------
  * Allocation-free block eigendecomposition.
  *
- * The pages have no counterpart of this call; it exists for callers of this
- * library that cannot call cudaMalloc: code inside a stream-captured region
- * that must not allocate, runtimes whose device memory is reserved up front
- * by an arena they do not control, and plugins of frameworks that forbid
- * allocations outside their own allocator.  It runs the eigensolver of the
- * refresh (one-sided Jacobi from the identity, then the Newton-Schulz /
- * two-sided polish) on caller buffers and allocates nothing: its working
- * memory is a file-scope device array of DOBB_NOALLOC_SCRATCH_FLOATS floats
- * (16 MiB) plus small fixed work-list arrays, which every GPU that loads the
- * library holds until the process exits.
+ * The pages have no counterpart of this call.  It exists for callers of
+ * this library that cannot call cudaMalloc: runtimes whose device memory is
+ * reserved up front by an arena they do not control, and plugins of
+ * frameworks that forbid allocations outside their own allocator.  It runs
+ * the refresh eigensolver (the restarted Rayleigh-Ritz two-sided Jacobi of
+ * dobb_refresh_bases, started from the identity) on caller buffers and
+ * allocates nothing: its working memory is a file-scope device array of
+ * DOBB_NOALLOC_SCRATCH_FLOATS floats (16 MiB) plus small fixed work-list
+ * arrays, which every GPU that loads the library holds until the process
+ * exits.
  *
  *   A_dev    count symmetric k x k fp32 matrices, row-major, back to back (in)
  *   Q_dev    count k x k fp32 outputs, row-major, column j = eigenvector of
  *            the j-th largest eigenvalue (out; its contents are overwritten)
  *   lam_dev  count x k fp32 eigenvalues, descending (out)
+ *            Q_dev and lam_dev must not overlap A_dev (the basis is set to
+ *            the identity before A is read): DOBB_ERR_INVALID_ARG otherwise
  *   k        1 <= k <= 1024;  count 0 <= count <= 4096 and
  *            count * 3 * k * k <= DOBB_NOALLOC_SCRATCH_FLOATS, otherwise the
  *            call returns DOBB_ERR_INVALID_ARG without touching the device
@@ -270,10 +299,11 @@ dobb_status dobb_sync_bases(dobb_handle h, void* stream);
  *   flags_host  optional host array of count uint32 (DOBB_FLAG_* bits); when
  *               non-NULL the call synchronises `stream` and fills it
  * Asynchronous on `stream` otherwise.  The first call on a device resolves
- * the device addresses of the arrays (cudaGetSymbolAddress) and should come
- * before any stream capture.  All calls share the arrays, which keep the
- * last call's contents: calls that overlap on the GPU race.  Errors are
- * reported by dobb_eigh_noalloc_last_error() (thread-local). */
+ * the device addresses of the arrays (cudaGetSymbolAddress) and configures
+ * the kernel; later calls only enqueue work.  All calls share the arrays,
+ * which keep the last call's contents (the call clears what must start at
+ * zero): calls that overlap on the GPU race.  Errors are reported by
+ * dobb_eigh_noalloc_last_error() (thread-local). */
 #define DOBB_NOALLOC_SCRATCH_FLOATS (4u << 20)
 dobb_status dobb_eigh_noalloc(const float* A_dev, float* Q_dev, float* lam_dev, int k, int count,
                               int max_sweeps, uint32_t* flags_host, void* stream);

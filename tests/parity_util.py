@@ -144,50 +144,86 @@ def check_update(W_prev, M_prev, G, Q_gpu, S_gpu, W_gpu, M_gpu, beta1, lr, s, pa
     return {"sign": sa, "bf16": res, "m_err": dm}
 
 
-def l2_update_error_bound(M_new, Q, k, m):
-    """Frobenius bound on the error of a Dobb-l2 U computed in fp32 (the
-    tolerance is derived from the arithmetic, not chosen).  The projection's
-    k-term fp32 dot products have |C~ - C|_ij <= g (|M| |Q|)_ij, g = k u /
-    (1 - k u), u = 2^-24; normalising column j to norm sqrt(m) moves it by at
-    most 2 sqrt(m) ||e_j|| / ||c_j||; with Q_b orthonormal ||dU_b||_F equals
-    ||dS_b||_F.  Columns with little momentum energy dominate, as tiny |C|
-    entries do for the sign."""
+def l2_update_entry_bound(M_new, Q, lr_s):
+    """Per-entry bound on |U_gpu - U| * lr s for a Dobb-l2 update computed in
+    fp32 (a tolerance derived from the arithmetic, not chosen), for the
+    registered (input-side) layout: M_new m x n, Q (B, k, k).
+
+    * C = M_b Q_b from an fp32 momentum (one rounding, u |M|) by k-term fp32
+      dot products: |C~ - C|_ij <= (g_k + u) (|M_b| |Q_b|)_ij = E_ij,
+      g_k = k u / (1 - k u), u = 2^-24.
+    * S_j = sqrt(m) c_j / ||c_j||; to first order
+      |dS_ij| <= sqrt(m) (E_ij + |C_ij| ||E_j|| / ||c_j||) / ||c_j||, capped at
+      2 sqrt(m) (both sides lie in [-sqrt(m), sqrt(m)]), plus eta |S_ij| for
+      the fp32 column sum of squares over the m rows, its square root and the
+      division, eta = (m + 8) u.
+    * U_b = S_b Q_b^T by k-term fp32 dot products:
+      |dU| <= |dS| |Q_b|^T + g_k |S_b| |Q_b|^T.
+    Returns lr s |dU| bound (m x n) and the exact U."""
     u = 2.0 ** -24
+    M_new = np.asarray(M_new, dtype=np.float64)
+    m, n = M_new.shape
+    B, k, _ = Q.shape
     g = k * u / (1 - k * u)
-    Mn = np.abs(np.asarray(M_new, dtype=np.float64))
-    B = Q.shape[0]
-    tot = 0.0
+    eta = (m + 8) * u
+    out = np.empty_like(M_new)
+    U = np.empty_like(M_new)
     for b in range(B):
         sl = slice(b * k, (b + 1) * k)
-        C = np.asarray(M_new, dtype=np.float64)[:, sl] @ Q[b]
-        E = g * (Mn[:, sl] @ np.abs(Q[b]))
+        Qb = np.asarray(Q[b], dtype=np.float64)
+        C = M_new[:, sl] @ Qb
+        E = (g + u) * (np.abs(M_new[:, sl]) @ np.abs(Qb))
         cn = np.linalg.norm(C, axis=0)
         en = np.linalg.norm(E, axis=0)
-        ok = cn > 0
-        tot += float(((2 * math.sqrt(m) * en[ok] / cn[ok]) ** 2).sum())
-        # plus the rounding of the normalisation and the reconstruction
-        tot += (8 * k * u) ** 2 * m * k
-    return math.sqrt(tot)
+        safe = np.where(cn > 0, cn, 1.0)
+        S = np.where(cn > 0, math.sqrt(m) * C / safe, 0.0)
+        dS = math.sqrt(m) * (E + np.abs(C) * (en / safe)) / safe
+        dS = np.minimum(np.where(cn > 0, dS, 2 * math.sqrt(m)), 2 * math.sqrt(m)) + eta * np.abs(S)
+        out[:, sl] = lr_s * (dS @ np.abs(Qb).T + g * (np.abs(S) @ np.abs(Qb).T))
+        U[:, sl] = S @ Qb.T
+    return out, U
+
+
+def bf16_parity_entrywise(W_test_bf16, W_exact, band):
+    """bf16 parameters against the exact result with a per-entry band: the
+    pre-rounding value lies within band_ij of W_exact_ij and is rounded once
+    (monotone), so the output must lie in
+    [round(W_exact - band), round(W_exact + band)]."""
+    We = np.asarray(W_exact, dtype=np.float64)
+    Wt = np.asarray(W_test_bf16, dtype=np.float64)
+    lo = O.round_to_bf16(We - band)
+    hi = O.round_to_bf16(We + band)
+    return int((~((Wt >= lo) & (Wt <= hi))).sum())
 
 
 def check_update_l2(W_prev, M_prev, G, Q_gpu, W_gpu, M_gpu, beta1, lr, s, param_dtype,
                     basis_dtype="f32", side="input"):
     """Score a Dobb-l2 update (column l2 normalisation) against the oracle run
-    with the GPU basis.  The normalised coefficients are continuous, so W is
-    compared directly, in Frobenius norm, within lr s times the fp32 bound of
-    `l2_update_error_bound` (plus, for bf16 parameters, half a bf16 quantum per
-    entry, 2^-8 |W|).  Side "output" (Dobb-G) normalises the rows of C: the
-    bound is that of the transposed problem."""
+    with the GPU basis, entry by entry: every W entry within lr s times the
+    per-entry fp32 bound of `l2_update_entry_bound` (plus the final rounding
+    of the parameter: one fp32 rounding, or a bf16 rounding of a value inside
+    that band).  Side "output" (Dobb-G) normalises the rows of C: the bound is
+    that of the transposed problem, transposed back."""
     ref = O.update_from_bases(W_prev, M_prev, G, Q_gpu, beta1, lr, s, "f32",
                               basis_dtype=basis_dtype, norm="l2", side=side)
     dm = np.abs(M_gpu - ref["M"]).max() / max(np.abs(ref["M"]).max(), 1e-30)
     assert dm <= 1e-6, f"momentum relative error {dm:.3e}"
     Mt = ref["M"].T if side == "output" else ref["M"]
-    m = Mt.shape[0]
-    k = Q_gpu.shape[1]
-    bound = lr * s * l2_update_error_bound(Mt, Q_gpu, k, m)
+    Qb = O.basis_for_update(Q_gpu, basis_dtype)
+    band, U = l2_update_entry_bound(Mt, Qb, lr * s)
+    if side == "output":
+        band, U = band.T, U.T
+    Wg = np.asarray(W_gpu, dtype=np.float64)
     if param_dtype == "bf16":
-        bound += float(np.linalg.norm(2.0 ** -8 * np.abs(ref["W"])))
-    err = float(np.linalg.norm(np.asarray(W_gpu, dtype=np.float64) - ref["W"]))
-    assert err <= bound, f"W error {err:.3e} above the fp32 bound {bound:.3e}"
-    return err, bound
+        bad = bf16_parity_entrywise(Wg, ref["W"], band)
+        assert bad == 0, f"{bad} bf16 W entries outside the per-entry fp32 band"
+    else:
+        u = 2.0 ** -24
+        err = np.abs(Wg - ref["W"])
+        # one rounding of the fused W - (lr s) U, and lr s itself rounded to fp32
+        lim = band + u * np.abs(ref["W"]) + u * lr * s * np.abs(U)
+        bad = int((err > lim).sum())
+        assert bad == 0, (f"{bad} W entries outside the per-entry bound "
+                          f"(worst ratio {float((err / lim).max()):.3g})")
+    err = np.abs(Wg - ref["W"]).max()
+    return float(err), float(band.max())

@@ -1,5 +1,7 @@
 """Parity of the CUDA path (through the C ABI) with the fp64 oracle on the
 same seeded inputs, phase by phase and over whole multi-step runs."""
+import math
+
 import numpy as np
 import pytest
 import torch
@@ -674,3 +676,117 @@ def test_mixed_sides_run_matches_oracle():
                          M_gpu.T if sd == "output" else M_gpu, 0.95, 0.02, 1.0, "f32",
                          (m if sd == "output" else n) // B, side=sd)
             orcs[i].M[0] = O.momentum(M_prev[i], to_np(Gd[i]), 0.95)
+
+
+# --------------------------------------------------------------------------
+# (a8) the invariant check and the per-block sums, scored against fp64
+# --------------------------------------------------------------------------
+
+def test_check_bases_matches_oracle_residuals():
+    """dobb_check_bases gives, per block, the three residuals of
+    `oracle.metrics.eig_residuals` evaluated on the same fp32 A, Q, Lambda:
+    on converged bases, and on bases with a planted error (a column mixed
+    with its neighbour, a column scaled), where the residuals are large."""
+    shapes, B = [(16, 96), (16, 400), (8, 1600)], 2     # k = 48, 200, 800
+    Xs, _, _ = make_problem(shapes, 2048, 0.3, seed=40)
+    opt = _dobb(shapes, B, beta2=0.0, refresh_period=0)
+    opt.accumulate([to_dev(x, "f32") for x in Xs])
+    opt.refresh()
+    torch.cuda.synchronize()
+
+    def compare():
+        chk = opt.check_bases()
+        for i in range(len(shapes)):
+            A = to_np(opt.tensor("moments", i))
+            Q = to_np(opt.tensor("bases", i))
+            lam = to_np(opt.tensor("eigvals", i))
+            for b in range(B):
+                r = MX.eig_residuals(A[b], Q[b], lam[b])
+                got = chk[opt.block_offset(i) + b]
+                for j, key in enumerate(("residual", "orth", "recon")):
+                    assert abs(got[j] - r[key]) <= 1e-5 * r[key] + 1e-12, (i, b, key, got[j], r[key])
+        return chk
+
+    chk = compare()
+    assert chk[:, 0].max() <= 1e-5
+    # planted errors in the stored bases (written through the state view)
+    Qv = opt.tensor("bases", 1)
+    Qv[0, :, 0] += 1e-2 * Qv[0, :, 50]
+    Qv[1, :, 7] *= 1.01
+    torch.cuda.synchronize()
+    chk = compare()
+    assert chk[opt.block_offset(1), 0] > 1e-5 and chk[opt.block_offset(1) + 1, 1] > 1e-2
+
+
+@pytest.mark.parametrize("path", ["auto", "ffma"])
+def test_block_stats_match_fp64_coefficient_norms(path):
+    """Per-block sums of a step: ||C_b||_F^2 against the fp64 ||M_b Q_b||_F^2
+    of the GPU's momentum and basis, within the fp32 bound of its evaluation:
+    (k + ceil(m / 32) + 8) u for the sums of squares, and 2 sqrt(k) (k u +
+    2^-21) for C itself (|sum 2 C e| <= 2 ||C|| ||e||, ||e|| <= (k u +
+    2^-21) || |M_b| |Q_b| ||_F <= (k u + 2^-21) sqrt(k) ||C||, the 2^-21 from
+    the split-precision products); ||U_b||_F^2 against the number of nonzero
+    signs."""
+    shapes, B = [(300, 1600), (130, 800), (64, 96)], 16     # k = 100, 50, 6
+    Xs, Gs, Ws = make_problem(shapes, 1024, 0.2, seed=41, param_dtype="bf16")
+    opt = _dobb(shapes, B, beta1=0.9, refresh_period=1, param_dtype="bf16")
+    opt.set_step_path(path)
+    Wd = [to_dev(w, "bf16") for w in Ws]
+    Sd = [torch.zeros(w.shape, dtype=torch.int8, device="cuda") for w in Ws]
+    opt.accumulate([to_dev(x, "f32") for x in Xs])
+    opt.step(Wd, [to_dev(g, "bf16") for g in Gs], 0.02, signs=Sd)
+    torch.cuda.synchronize()
+    st = opt.block_stats()
+    u = 2.0 ** -24
+    for i, (m, n) in enumerate(shapes):
+        k = n // B
+        M = to_np(opt.tensor("momentum", i))
+        Q = to_np(opt.tensor("bases", i))
+        S = to_np(Sd[i])
+        for b in range(B):
+            C = M[:, b * k:(b + 1) * k] @ Q[b]
+            want = float((C ** 2).sum())
+            tol = (k + math.ceil(m / 32) + 8) * u + 2 * math.sqrt(k) * (k * u + 2.0 ** -21)
+            got = float(st[opt.block_offset(i) + b, 1])
+            assert abs(got - want) <= tol * want, (i, b, got, want)
+            nnz = np.count_nonzero(S[:, b * k:(b + 1) * k])
+            assert abs(st[opt.block_offset(i) + b, 0] - nnz) <= 1e-4 * max(nnz, 1)
+
+
+# --------------------------------------------------------------------------
+# failure detection without a GPU fault: the eigensolver's sweep cap
+# --------------------------------------------------------------------------
+
+def test_sweep_cap_sets_not_converged_and_writes_a_basis():
+    """With the sweep cap at 1, a cold refresh of an ill-conditioned block
+    cannot converge: the block gets DOBB_FLAG_NOT_CONVERGED, the basis is
+    still written (orthonormal to fp32 level, no longer the identity) and
+    the step that follows runs.  Raising the cap again clears the
+    condition on the next refresh."""
+    k, B = 100, 2
+    rng = np.random.default_rng(42)
+    A = np.stack([I.spd_with_gap(k, rng, cond=1e6)[0] for _ in range(B)])
+    opt = _dobb([(64, B * k)], B, refresh_period=0)
+    opt.tensor("moments", 0).copy_(torch.from_numpy(A.astype(np.float32)).view(B, k, k))
+    opt.set_jacobi(max_sweeps=1)
+    opt.refresh()
+    torch.cuda.synchronize()
+    flags = opt.block_flags()
+    assert np.all(flags & 8), flags
+    st = opt.block_stats()
+    assert np.all(st[:, 2] == 1.0)
+    Q = to_np(opt.tensor("bases", 0))
+    for b in range(B):
+        assert np.all(np.isfinite(Q[b]))
+        assert np.linalg.norm(Q[b].T @ Q[b] - np.eye(k)) <= 1e-4 * np.sqrt(k)
+        assert np.abs(Q[b] - np.eye(k)).max() > 0.1
+    W = to_dev(I.weights(64, B * k, rng), "f32")
+    opt.step([W], [to_dev(rng.standard_normal((64, B * k)).astype(np.float32), "f32")], 0.01)
+    torch.cuda.synchronize()
+    assert opt.device_error() == 0 and torch.isfinite(W).all()
+    opt.clear_flags()
+    opt.set_jacobi(max_sweeps=40)
+    opt.refresh()
+    torch.cuda.synchronize()
+    assert np.all(opt.block_flags() == 0)
+    check_bases(opt, [A.astype(np.float32).astype(np.float64)])

@@ -703,3 +703,132 @@ def test_generators_hit_target_effective_rank():
     gaps = -np.diff(lam) / lam[:-1]
     assert gaps.min() >= 1e-3 and abs(lam[0] / lam[-1] - 1e6) < 1e-3 * 1e6
     assert MX.eig_residuals(a, q, lam)["residual"] < 1e-12
+
+
+# --------------------------------------------------------------------------
+# the parity rules themselves, pinned by hand-computed values
+# --------------------------------------------------------------------------
+
+def test_w_rel_error_reports_known_offsets():
+    """max_ij |W_test - W_ref| / max_ij |W_ref|: the largest offset (not the
+    sum or the mean), over the largest |entry| of the reference (not of the
+    tested matrix, not a Frobenius norm, with the sign of the entry dropped)."""
+    W = np.array([[2.0, -3.0], [1.0, 0.0]])
+    one = W.copy()
+    one[1, 1] += 0.006
+    assert MX.w_rel_error(one, W) == pytest.approx(0.002, rel=1e-12)
+    two = W.copy()
+    two[0, 0] += 0.003
+    two[1, 0] -= 0.0015
+    assert MX.w_rel_error(two, W) == pytest.approx(0.001, rel=1e-12)       # max, not sum / mean
+    at_max = W.copy()
+    at_max[0, 1] -= 0.3                                                      # |W_test| max 3.3
+    assert MX.w_rel_error(at_max, W) == pytest.approx(0.1, rel=1e-12)       # reference's max
+    assert MX.w_rel_error(-W, -W) == 0.0
+    neg = -W
+    neg[0, 0] += 0.03
+    assert MX.w_rel_error(neg, -W) == pytest.approx(0.01, rel=1e-12)
+    # homogeneous of degree 0: scaling both sides leaves it unchanged
+    assert MX.w_rel_error(7.0 * one, 7.0 * W) == pytest.approx(0.002, rel=1e-12)
+
+
+def test_eig_residuals_closed_forms_flag_wrong_decompositions():
+    """Hand-derived residuals of wrong decompositions of A = diag(l1, l2):
+    a basis rotated by theta gives ||AQ - Q Lambda||_F = ||Q Lambda Q^T - A||_F
+    = sqrt(2) |l1 - l2| |sin theta| and zero orthogonality error; permuted
+    eigenvalues, a scaled column and a sheared basis each move the residual
+    they must move, by the amount computed by hand."""
+    l1, l2 = 3.0, 1.0
+    A = np.diag([l1, l2])
+    fro = math.sqrt(l1 ** 2 + l2 ** 2)
+    exact = MX.eig_residuals(A, np.eye(2), np.array([l1, l2]))
+    assert exact == {"residual": 0.0, "orth": 0.0, "recon": 0.0}
+    th = 0.01
+    c, s = math.cos(th), math.sin(th)
+    Qr = np.array([[c, -s], [s, c]])
+    r = MX.eig_residuals(A, Qr, np.array([l1, l2]))
+    want = math.sqrt(2) * abs(l1 - l2) * abs(s) / fro
+    assert r["residual"] == pytest.approx(want, rel=1e-9)
+    assert r["recon"] == pytest.approx(want, rel=1e-9)
+    assert r["orth"] < 1e-15
+    # permuted eigenvalues, exact basis
+    A3 = np.diag([1.0, 2.0, 3.0])
+    r = MX.eig_residuals(A3, np.eye(3), np.array([2.0, 1.0, 3.0]))
+    assert r["residual"] == pytest.approx(math.sqrt(2) / math.sqrt(14), rel=1e-12)
+    assert r["recon"] == pytest.approx(math.sqrt(2) / math.sqrt(14), rel=1e-12)
+    assert r["orth"] == 0.0
+    # a column scaled by (1 + e): orthogonality error 2e + e^2, reconstruction l1 (2e + e^2)
+    e = 1e-3
+    Qs = np.diag([1.0 + e, 1.0])
+    r = MX.eig_residuals(A, Qs, np.array([l1, l2]))
+    assert r["orth"] == pytest.approx(2 * e + e * e, rel=1e-9)
+    assert r["recon"] == pytest.approx(l1 * (2 * e + e * e) / fro, rel=1e-9)
+    assert r["residual"] == 0.0
+    # a sheared basis: Q^T Q - I = [[0, d], [d, d^2]]
+    d = 1e-2
+    Qh = np.array([[1.0, d], [0.0, 1.0]])
+    r = MX.eig_residuals(A, Qh, np.array([l1, l2]))
+    assert r["orth"] == pytest.approx(math.sqrt(2 * d * d + d ** 4), rel=1e-9)
+    # || A Q - Q Lambda || = || [[0, (l1 - l2) d], [0, 0]] ||
+    assert r["residual"] == pytest.approx(abs(l1 - l2) * d / fro, rel=1e-9)
+    # scale invariance of the relative residuals; orth does not see A at all
+    r10 = MX.eig_residuals(10 * A, Qr, 10 * np.array([l1, l2]))
+    assert r10["residual"] == pytest.approx(math.sqrt(2) * abs(l1 - l2) * abs(s) / fro, rel=1e-9)
+    # a random exact decomposition passes, a perturbed one fails in proportion
+    rng = np.random.default_rng(5)
+    a, lam, q = I.spd_with_gap(40, rng, cond=1e3)
+    assert MX.eig_residuals(a, q, lam)["residual"] < 1e-13
+    qp = q.copy()
+    qp[:, 7] += 1e-4 * q[:, 8]
+    rp = MX.eig_residuals(a, qp, lam)
+    assert rp["residual"] == pytest.approx(1e-4 * abs(lam[8] - lam[7]) / np.linalg.norm(a), rel=1e-6)
+    assert rp["orth"] == pytest.approx(1e-4 * math.sqrt(2 + 1e-8), rel=1e-6)
+
+
+def test_l2_entrywise_bound_holds_for_fp32_and_catches_a_planted_error():
+    """The per-entry Dobb-l2 tolerance of the GPU tests is derived from fp32
+    arithmetic: an fp32 evaluation of the update (numpy float32, a different
+    summation order than the GPU's) lies inside it, and one entry moved by
+    1 % of the update's RMS does not."""
+    import parity_util as PU
+    rng = np.random.default_rng(41)
+    m, n, B = 300, 192, 2
+    k = n // B
+    X = I.activations(4 * k, n, 0.3, rng)
+    A = O.block_moment_ema(np.zeros((B, k, k)), X, 0.0, B)
+    Q, _ = O.refresh_bases(A, "lapack")
+    W = I.weights(m, n, rng)
+    G = I.gradients(m, X, rng)
+    lr, s = 0.02, 1.5
+    ref = O.update_from_bases(W, np.zeros((m, n)), G, Q, 0.9, lr, s, "f32", norm="l2")
+    # fp32 evaluation
+    M32 = (np.float32(0.9) * np.zeros((m, n), np.float32) + G.astype(np.float32))
+    W32 = W.astype(np.float32).copy()
+    for b in range(B):
+        sl = slice(b * k, (b + 1) * k)
+        Q32 = Q[b].astype(np.float32)
+        C = M32[:, sl] @ Q32
+        nrm = np.sqrt((C * C).sum(axis=0, dtype=np.float32))
+        S = C * (np.float32(math.sqrt(m)) / nrm)[None, :]
+        W32[:, sl] = W32[:, sl] - np.float32(lr * s) * (S @ Q32.T)
+    W64 = W32.astype(np.float64)
+    err, bmax = PU.check_update_l2(W, np.zeros((m, n)), G, Q, W64, M32.astype(np.float64), 0.9, lr,
+                                   s, "f32")
+    assert 0 < err <= bmax
+    # the worst-case bound sits near 2.5e-3 of the update's RMS here: a 1 %
+    # error in one entry is caught
+    bad = W64.copy()
+    bad[17, 40] += 1e-2 * lr * s * math.sqrt((ref["U"] ** 2).mean())
+    with pytest.raises(AssertionError):
+        PU.check_update_l2(W, np.zeros((m, n)), G, Q, bad, M32.astype(np.float64), 0.9, lr, s, "f32")
+    # bf16 parameters: the rounded fp32 result passes, one bf16 ulp off does not
+    Wb = O.round_to_bf16(W)
+    ref_b = O.update_from_bases(Wb, np.zeros((m, n)), G, Q, 0.9, lr, s, "f32", norm="l2")
+    out = O.round_to_bf16(Wb + (W64 - W.astype(np.float32).astype(np.float64)))
+    PU.check_update_l2(Wb, np.zeros((m, n)), G, Q, out, M32.astype(np.float64), 0.9, lr, s, "bf16")
+    worse = out.copy()
+    worse[3, 5] = O.round_to_bf16(np.array([out[3, 5] * (1 + 2 ** -6)]))[0]
+    with pytest.raises(AssertionError):
+        PU.check_update_l2(Wb, np.zeros((m, n)), G, Q, worse, M32.astype(np.float64), 0.9, lr, s,
+                           "bf16")
+    assert ref_b["W"].shape == (m, n)

@@ -1,13 +1,13 @@
 """The allocation-free eigendecomposition entry point.
 
-Some callers of this library cannot call cudaMalloc (stream-captured code
-that must not allocate, runtimes whose device memory is reserved up front,
-plugins of frameworks that forbid outside allocations).  dobb_eigh_noalloc
-serves them from a fixed file-scope device array.  This test calls it
-through the C ABI twice in a row, on different blocks, and checks each
-result against the optimizer's own refresh (dobb_refresh_bases on the same
-moments) within the eigen tolerance the other GPU tests use.  The file is
-named so that pytest collects it last."""
+Some callers of this library cannot call cudaMalloc: runtimes whose device
+memory is reserved up front by an arena they do not control, and plugins of
+frameworks that forbid allocations outside their own allocator.
+dobb_eigh_noalloc serves them from a fixed file-scope device array.  This
+test calls it through the C ABI twice in a row, on different blocks, and
+checks each result against the optimizer's own refresh (dobb_refresh_bases
+on the same moments) within the eigen tolerance the other GPU tests use.
+The file is named so that pytest collects it last."""
 import ctypes
 
 import numpy as np
