@@ -919,6 +919,13 @@ dobb_status dobb_set_refresh(dobb_handle h, int method, int steps) {
   return DOBB_OK;
 }
 
+dobb_status dobb_set_refresh_period(dobb_handle h, int refresh_period) {
+  if (!h) return fail(DOBB_ERR_INVALID_ARG, "NULL handle");
+  if (refresh_period < 0) return fail(DOBB_ERR_INVALID_ARG, "refresh_period must be >= 0");
+  h->T = refresh_period;
+  return DOBB_OK;
+}
+
 dobb_status dobb_set_jacobi(dobb_handle h, int max_sweeps, float tol) {
   if (!h || max_sweeps < 1 || !(tol >= 0.f)) return fail(DOBB_ERR_INVALID_ARG, "bad eigensolver settings");
   h->max_sweeps = max_sweeps;

@@ -105,6 +105,12 @@ extern "C" dobb_status dobb_eigh_noalloc(const float* A_dev, float* Q_dev, float
   if (!A_dev || !Q_dev || !lam_dev) return noalloc_fail(DOBB_ERR_INVALID_ARG, "NULL pointer argument");
   if (k < 1 || k > kNoAllocMaxK) return noalloc_fail(DOBB_ERR_INVALID_ARG, "k must lie in [1, 1024]");
   if (count < 0) return noalloc_fail(DOBB_ERR_INVALID_ARG, "count must be >= 0");
+  if (count > kNoAllocMaxBlocks)
+    return noalloc_fail(DOBB_ERR_INVALID_ARG, "count exceeds the 4096 blocks the fixed work list holds");
+  if ((size_t)count * 3 * (size_t)k * k > kNoAllocScratchFloats)
+    return noalloc_fail(DOBB_ERR_INVALID_ARG,
+                        "count * 3 * k * k exceeds the 4 Mi-float (16 MiB) fixed scratch array");
+  if (max_sweeps < 1) return noalloc_fail(DOBB_ERR_INVALID_ARG, "max_sweeps must be >= 1");
   {
     // the basis is set to the identity before the solver reads A: outputs
     // that overlap the input would corrupt it
@@ -117,12 +123,6 @@ extern "C" dobb_status dobb_eigh_noalloc(const float* A_dev, float* Q_dev, float
     if (count > 0 && ((q0 < a1 && a0 < q1) || (l0 < a1 && a0 < l1)))
       return noalloc_fail(DOBB_ERR_INVALID_ARG, "Q_dev and lam_dev must not overlap A_dev");
   }
-  if (count > kNoAllocMaxBlocks)
-    return noalloc_fail(DOBB_ERR_INVALID_ARG, "count exceeds the 4096 blocks the fixed work list holds");
-  if ((size_t)count * 3 * (size_t)k * k > kNoAllocScratchFloats)
-    return noalloc_fail(DOBB_ERR_INVALID_ARG,
-                        "count * 3 * k * k exceeds the 4 Mi-float (16 MiB) fixed scratch array");
-  if (max_sweeps < 1) return noalloc_fail(DOBB_ERR_INVALID_ARG, "max_sweeps must be >= 1");
   if (count == 0) return DOBB_OK;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);

@@ -37,7 +37,9 @@ __all__ = [
     "haar_orthogonal",
     "matrix_with_singular_values",
     "activations",
+    "ActivationStream",
     "gradients",
+    "gradients_fp32",
     "weights",
     "round_bf16_np",
     "spd_with_gap",
@@ -153,6 +155,46 @@ def activations(N: int, n: int, target: float, rng: np.random.Generator,
     if dtype == "bf16":
         x = round_bf16_np(x)
     return x
+
+
+class ActivationStream:
+    """Activations of one matrix input step after step: a fixed column
+    covariance Q diag(lambda) Q^T (geometric spectrum at the target effective
+    rank, mean eigenvalue 1) and fresh Gaussian tokens at every draw, as a
+    layer sees during training.  Q is Haar, or a shared Haar basis of the
+    same width with rows permuted and sign-flipped (cheap distinct bases for
+    many matrices of one width).  Draws are computed in fp32."""
+
+    def __init__(self, n: int, target: float, rng: np.random.Generator,
+                 shared_basis: Optional[np.ndarray] = None):
+        lam = geometric_spectrum(n, target)
+        lam = lam * (n / lam.sum())
+        if shared_basis is None:
+            q = haar_orthogonal(n, rng)
+        else:
+            perm = rng.permutation(n)
+            flip = rng.choice(np.array([-1.0, 1.0]), size=n)
+            q = shared_basis[perm] * flip[:, None]
+        self.n = n
+        self.mix = (np.sqrt(lam)[:, None] * q.T).astype(np.float32)   # diag(sqrt lam) Q^T
+
+    def draw(self, N: int, rng: np.random.Generator, dtype: str = "f32") -> np.ndarray:
+        z = rng.standard_normal((N, self.n), dtype=np.float32)
+        x = z @ self.mix
+        if dtype == "bf16":
+            x = round_bf16_np(x)
+        return np.ascontiguousarray(x, dtype=np.float32)
+
+
+def gradients_fp32(m: int, X: np.ndarray, rng: np.random.Generator,
+                   dtype: str = "f32") -> np.ndarray:
+    """`gradients` evaluated in fp32 (the generator for model-sized runs)."""
+    N = X.shape[0]
+    d = rng.standard_normal((m, N), dtype=np.float32)
+    g = (d @ np.asarray(X, dtype=np.float32)) / np.float32(N)
+    if dtype == "bf16":
+        g = round_bf16_np(g)
+    return np.ascontiguousarray(g, dtype=np.float32)
 
 
 def gradients(m: int, X: np.ndarray, rng: np.random.Generator,

@@ -157,6 +157,10 @@ class Dobb:
     def device_error(self) -> int:
         return int(self.tensor("error").item())
 
+    def set_refresh_period(self, refresh_period: int) -> None:
+        """Refresh every `refresh_period` steps from now on (0 = never)."""
+        check(self.lib.dobb_set_refresh_period(self.handle, int(refresh_period)))
+
     def set_jacobi(self, max_sweeps: int = 40, tol: float = 0.0) -> None:
         check(self.lib.dobb_set_jacobi(self.handle, int(max_sweeps), float(tol)))
 

@@ -196,6 +196,10 @@ dobb_status dobb_set_refresh(dobb_handle h, int method, int steps);
  * dtype. */
 dobb_status dobb_set_basis_dtype(dobb_handle h, dobb_dtype basis_dtype, void* stream);
 
+/* Change the refresh period T of dobb_step (0 = never); the step counter is
+ * kept.  DOBB_ERR_INVALID_ARG for T < 0. */
+dobb_status dobb_set_refresh_period(dobb_handle h, int refresh_period);
+
 /* Eigensolver controls: sweep cap (default 40) and the convergence
  * threshold, the relative off-diagonal norm ||off(B)||_F / ||B||_F that the
  * last sweep of B = V^T A V may leave (0 = default 2e-6). */
