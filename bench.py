@@ -357,55 +357,80 @@ def _traffic_for(kernel_key, workload):
 # CPU baseline: the oracle on a bounded sample
 # ---------------------------------------------------------------------------
 
-def cpu_baseline(cfg_name="gpt2-xl", layers_sample=1, seed=0, basis="f32", refresh="eigh",
+class OracleSample:
+    """The fp64 oracle as it stands, on `layers_sample` layers of a workload
+    (the same recipe, drawn on the host once): `step()` runs and times one
+    accumulate (or, for the stress workloads, nothing), one refresh and one
+    update, amortised like the GPU step (accumulate + update + refresh / T)."""
+
+    def __init__(self, cfg_name="gpt2-xl", layers_sample=1, seed=0, basis="f32", refresh="eigh",
                  orth_steps=1, norm="sign", side="input"):
-    """The fp64 oracle as it stands, on `layers_sample` layers of the
-    workload (the same recipe, drawn on the host): one accumulate, one
-    refresh and one update, amortised like the GPU step."""
-    import numpy as np
-    from block_eigenbasis_preconditioning_gb300 import inputs as I
-    from oracle import dobb as O
-    cfg = CONFIGS[cfg_name]
-    rng = np.random.default_rng(seed)
-    shapes, lay = model_shapes(cfg["model"], layers=layers_sample)
-    params = sum(m * n for m, n in shapes)
-    B, T = cfg["B"], cfg["T"]
-    orc = O.DobbOracle(shapes, B, BETA1, BETA2, refresh_period=0, scale_s=SCALE,
-                       param_dtype=cfg["pdt"], eig_method="lapack", basis_dtype=basis,
-                       refresh_method=refresh, orth_steps=orth_steps, norm=norm, side=side)
-    t_acc = 0.0
-    if cfg["kind"] == "train":
-        effs = _eff_for(cfg, lay)
-        streams = [I.ActivationStream(m if side == "output" else n, e, rng)
-                   for (m, n), e in zip(shapes, effs)]
-        Xs = [s.draw(cfg["N"], rng, dtype=cfg["adt"]) for s in streams]
-        Gs = [I.gradients_fp32(m, X, rng, dtype=cfg["pdt"]) if side != "output" else
-              I.round_bf16_np(rng.standard_normal((m, n)).astype(np.float32) * 1e-3)
-              for (m, n), X in zip(shapes, Xs)]
+        import numpy as np
+        from block_eigenbasis_preconditioning_gb300 import inputs as I
+        from oracle import dobb as O
+        self.cfg_name, self.refresh_method = cfg_name, refresh
+        cfg = self.cfg = CONFIGS[cfg_name]
+        rng = np.random.default_rng(seed)
+        self.shapes, lay = model_shapes(cfg["model"], layers=layers_sample)
+        self.params = sum(m * n for m, n in self.shapes)
+        self.layers = layers_sample
+        B = cfg["B"]
+        self.orc = O.DobbOracle(self.shapes, B, BETA1, BETA2, refresh_period=0, scale_s=SCALE,
+                                param_dtype=cfg["pdt"], eig_method="lapack", basis_dtype=basis,
+                                refresh_method=refresh, orth_steps=orth_steps, norm=norm, side=side)
+        self.Xs = None
+        if cfg["kind"] == "train":
+            effs = _eff_for(cfg, lay)
+            bases = {}
+            streams = []
+            for (m, n), e in zip(self.shapes, effs):
+                w = m if side == "output" else n
+                if w not in bases:
+                    bases[w] = I.haar_orthogonal(w, rng)
+                streams.append(I.ActivationStream(w, e, rng, shared_basis=bases[w]))
+            self.Xs = [s.draw(cfg["N"], rng, dtype=cfg["adt"]) for s in streams]
+            if side == "output":
+                self.Gs = [I.round_bf16_np(rng.standard_normal((m, n)).astype(np.float32) * 1e-3)
+                           for m, n in self.shapes]
+            else:
+                self.Gs = [I.gradients_fp32(m, X, rng, dtype=cfg["pdt"])
+                           for (m, _), X in zip(self.shapes, self.Xs)]
+        else:
+            for i, (m, n) in enumerate(self.shapes):
+                k = n // B
+                self.orc.A[i] = np.stack([I.spd_with_gap(k, rng, cond=1e6)[0] for _ in range(B)])
+            self.Gs = [I.round_bf16_np(rng.standard_normal((m, n)).astype(np.float32) * 1e-3)
+                       for m, n in self.shapes]
+        self.Ws = [I.weights(m, n, rng, dtype=cfg["pdt"]) for m, n in self.shapes]
+        self.seconds = None
+
+    def step(self):
         t0 = time.perf_counter()
-        orc.accumulate(Xs)
-        t_acc = time.perf_counter() - t0
-    else:
-        for i, (m, n) in enumerate(shapes):
-            k = n // B
-            orc.A[i] = np.stack([I.spd_with_gap(k, rng, cond=1e6)[0] for _ in range(B)])
-        Gs = [I.round_bf16_np(rng.standard_normal((m, n)).astype(np.float32) * 1e-3)
-              for m, n in shapes]
-    Ws = [I.weights(m, n, rng, dtype=cfg["pdt"]) for m, n in shapes]
-    t1 = time.perf_counter()
-    orc.refresh()
-    t2 = time.perf_counter()
-    orc.step(Ws, Gs, LR)
-    t3 = time.perf_counter()
-    ref, upd = t2 - t1, t3 - t2
-    step_s = t_acc + upd + ref / T
-    return {"value": params / step_s, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
-            "sample": f"{layers_sample} {cfg['model']} layer(s) of the {cfg_name} workload "
-                      f"({params} params, {len(shapes)} matrices, the same input recipe drawn "
-                      f"on the host): one accumulate + one "
-                      f"{'LAPACK' if refresh == 'eigh' else 'orthogonal-iteration'} refresh + one "
-                      f"update in fp64 numpy, amortised as accumulate + update + refresh/{T}",
-            "seconds": {"accumulate": t_acc, "refresh": ref, "update": upd}}
+        if self.Xs is not None:
+            self.orc.accumulate(self.Xs)
+        t1 = time.perf_counter()
+        self.orc.refresh()
+        t2 = time.perf_counter()
+        self.Ws = self.orc.step(self.Ws, self.Gs, LR)
+        t3 = time.perf_counter()
+        acc, ref, upd = t1 - t0, t2 - t1, t3 - t2
+        self.seconds = {"accumulate": acc, "refresh": ref, "update": upd}
+        return self.params / (acc + upd + ref / self.cfg["T"])
+
+    def describe(self):
+        return (f"{self.layers} {self.cfg['model']} layer(s) of the {self.cfg_name} workload "
+                f"({self.params} params, {len(self.shapes)} matrices, the same input recipe drawn "
+                f"once on the host): per step one accumulate + one "
+                f"{'LAPACK' if self.refresh_method == 'eigh' else 'orthogonal-iteration'} refresh "
+                f"+ one update in fp64 numpy, amortised as accumulate + update + "
+                f"refresh/{self.cfg['T']}")
+
+
+def cpu_baseline(cfg_name="gpt2-xl", layers_sample=1, **kw):
+    s = OracleSample(cfg_name, layers_sample, **kw)
+    v = s.step()
+    return {"value": v, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+            "sample": s.describe(), "seconds": s.seconds}
 
 
 def workload_name(cfg_name, cfg, n_matrices, params, layers):
@@ -429,23 +454,22 @@ def run_reference(args):
     cfg = CONFIGS[args.config]
     shapes, _ = model_shapes(cfg["model"], args.layers)
     params = sum(m * n for m, n in shapes)
-    steps = []
-    res = None
-    for _ in range(max(1, args.steps)):
-        res = cpu_baseline(args.config, layers_sample=1, basis=args.basis, refresh=args.refresh,
-                           orth_steps=args.orth_steps, norm=args.norm, side=args.side)
-        steps.append(res["value"])
+    sample = OracleSample(args.config, 1, basis=args.basis, refresh=args.refresh,
+                          orth_steps=args.orth_steps, norm=args.norm, side=args.side)
+    for _ in range(args.warmup):
+        sample.step()
+    steps = [sample.step() for _ in range(max(1, args.steps))]
     v = sorted(steps)[len(steps) // 2]
     name = workload_name(args.config, cfg, len(shapes), params, args.layers)
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": 1,
-            "steps": args.steps, "warmup": 0, "ms_per_step": params / v * 1e3 if v else None,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": params / v * 1e3 if v else None,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
-            "config": {"workload": f"{name}; timed on the oracle sample: {res['sample']}",
+            "config": {"workload": f"{name}; timed on the oracle sample: {sample.describe()}",
                        "B": cfg["B"], "refresh_period": cfg["T"], "tokens": cfg["N"],
                        "parallelism": "host cores"},
-            "cpu_baseline": {"value": v, "unit": UNIT, "cores": res["cores"], "kind": "oracle",
-                             "sample": res["sample"]},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": sample.describe()},
             "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0

@@ -54,6 +54,7 @@ SIGNATURES = [
     ("dobb_set_side", _c.c_int, [_VP, _c.c_int, _c.c_int, _VP]),
     ("dobb_set_jacobi", _c.c_int, [_VP, _c.c_int, _c.c_float]),
     ("dobb_set_refresh_period", _c.c_int, [_VP, _c.c_int]),
+    ("dobb_set_eig_grid", _c.c_int, [_VP, _c.c_int, _c.c_int64]),
     ("dobb_state_tensor", _c.c_int, [_VP, _c.c_int, _c.c_int, _c.POINTER(_VP),
                                      _c.POINTER(_c.c_size_t)]),
     ("dobb_num_blocks", _c.c_int64, [_VP]),

@@ -51,7 +51,8 @@ struct Layout {
   size_t off_colsq = 0;  // column sums of squares (column-l2 normalisation), eigenvalue layout
   size_t off_A = 0, off_Q = 0, off_lam = 0, off_M = 0, off_flags = 0, off_stats = 0,
          off_check = 0, off_err = 0, off_info = 0, off_maps = 0, off_tiles = 0, off_pack = 0,
-         off_scratch = 0, total = 0;
+         off_scratch = 0, off_gj_rbuf = 0, off_gj_ctl = 0, off_gj_count = 0, total = 0;
+  size_t gj_rbuf_floats = 0, gj_ctl_items = 0;
   size_t n_tiles = 0;
 };
 
@@ -61,6 +62,22 @@ constexpr int kTcRows = 128;
 constexpr int kTcSmallK = 128;
 
 int64_t pad16f(int64_t v) { return (v + 15) / 16 * 16; }
+
+// Grid eigensolver: blocks at least this wide use it by default (narrower
+// ones run one CTA per block), it is never used below kGjMinK, and a batch
+// holds as many blocks of one width as keep their scratch (3 k^2 floats)
+// within kGjL2Budget bytes of L2.
+constexpr int kGjDefaultMinK = 449;
+constexpr int kGjMinK = 128;
+constexpr int64_t kGjDefaultBatchBytes = 0;   // 0: every block of one width in one batch
+
+// blocks of width k in one batch whose scratch (3 k^2 floats each) stays
+// within batch_bytes (0: no limit)
+int gj_batch_items(int k, int64_t batch_bytes) {
+  if (batch_bytes <= 0) return 1 << 30;
+  const int64_t per = 12 * (int64_t)k * k;
+  return (int)std::max<int64_t>(1, std::min<int64_t>(1 << 30, batch_bytes / per));
+}
 
 struct Chunk {
   int mat_base = 0, mat_end = 0;
@@ -302,6 +319,25 @@ Layout compute_layout(int num, const int64_t* m, const int64_t* n, int B, size_t
   L.off_tiles = off;  off = align_up(off + sizeof(Tile) * n_tiles);
   L.off_pack = off;   off = align_up(off + L.pack_bytes);
   L.off_scratch = off; off = align_up(off + 12 * L.a_floats);  // 3 k^2 floats per block
+  // grid eigensolver: rotations and control records of the largest batch of
+  // any width it may be used for
+  {
+    std::vector<std::pair<int, size_t>> count;  // (width, blocks of that width)
+    for (int i = 0; i < num; ++i) {
+      const int k = (int)(n[i] / B);
+      if (k < kGjMinK) continue;
+      auto it = std::find_if(count.begin(), count.end(), [&](auto& c) { return c.first == k; });
+      if (it == count.end()) count.push_back({k, (size_t)B});
+      else it->second += B;
+    }
+    for (auto& c : count) {
+      L.gj_rbuf_floats = std::max(L.gj_rbuf_floats, c.second * (size_t)gj_rbuf_floats(c.first));
+      L.gj_ctl_items = std::max(L.gj_ctl_items, c.second);
+    }
+  }
+  L.off_gj_rbuf = off;  off = align_up(off + 4 * L.gj_rbuf_floats);
+  L.off_gj_ctl = off;   off = align_up(off + sizeof(GjCtl) * L.gj_ctl_items);
+  L.off_gj_count = off; off = align_up(off + 4);
   L.total = off;
   L.n_tiles = n_tiles;
   return L;
@@ -332,6 +368,9 @@ struct dobb_ctx {
   size_t smem_per_sm = 0;
   int64_t launches = 0;
   int path = 0;            // 0: tensor-core kernel where eligible, 1: FFMA only
+  int gj_min_k = kGjDefaultMinK;  // blocks at least this wide use the grid eigensolver
+  int64_t gj_batch_bytes = kGjDefaultBatchBytes;
+  int gj_host_count = 0;
   // cached X tensor maps (pointer and token count they were encoded for)
   std::vector<CUtensorMap> xmaps;
   std::vector<const void*> xmap_ptr;
@@ -354,6 +393,9 @@ struct dobb_ctx {
   float* scratch() const { return reinterpret_cast<float*>(base + L.off_scratch); }
   uint32_t* err() const { return reinterpret_cast<uint32_t*>(base + L.off_err); }
   void* dmaps() const { return base + L.off_maps; }
+  float* gj_rbuf() const { return reinterpret_cast<float*>(base + L.off_gj_rbuf); }
+  GjCtl* gj_ctl() const { return reinterpret_cast<GjCtl*>(base + L.off_gj_ctl); }
+  int32_t* gj_count() const { return reinterpret_cast<int32_t*>(base + L.off_gj_count); }
   unsigned char* pack() const { return reinterpret_cast<unsigned char*>(base + L.off_pack); }
 };
 
@@ -405,10 +447,42 @@ dobb_status do_refresh(dobb_handle h, cudaStream_t s) {
   const size_t half = h->smem_per_sm / 2 > 2048 ? h->smem_per_sm / 2 - 2048 : 0;
   for (const Chunk& ch : h->wl.chunks) {
     if (ch.eig_n == 0) continue;
-    // the list is sorted by decreasing k: [one CTA per SM | two or more]
+    // the list is sorted by decreasing k: [grid solver | one CTA per SM | two or more]
     const Tile* items = h->wl.tiles.data() + ch.eig_off;
     auto kof = [&](int idx) { return (int)(h->n[items[idx].mat] / h->B); };
-    int b = 0;
+    int g0 = 0;
+    if (h->gj_min_k > 0) {
+      while (g0 < ch.eig_n && kof(g0) >= h->gj_min_k) {
+        // a batch: a run of equal width within the L2 budget
+        const int k = kof(g0);
+        int g1 = g0;
+        const int cap = std::min<int>(gj_batch_items(k, h->gj_batch_bytes), (int)h->L.gj_ctl_items);
+        while (g1 < ch.eig_n && kof(g1) == k && g1 - g0 < cap) ++g1;
+        if ((size_t)(g1 - g0) * (size_t)gj_rbuf_floats(k) > h->L.gj_rbuf_floats || g1 == g0)
+          return fail(DOBB_ERR_STATE, "grid eigensolver buffers too small for width %d", k);
+        GjArgs ga{};
+        ga.info = h->dinfo();
+        ga.items = h->dtiles() + ch.eig_off + g0;
+        ga.nitems = g1 - g0;
+        ga.k = k;
+        ga.A = h->A();
+        ga.Q = h->Q();
+        ga.lam = h->lam();
+        ga.scratch = h->scratch();
+        ga.rbuf = h->gj_rbuf();
+        ga.rstride = gj_rbuf_floats(k);
+        ga.ctl = h->gj_ctl();
+        ga.active_count = h->gj_count();
+        ga.flags = h->flags();
+        ga.stats = h->stats();
+        ga.max_sweeps = h->max_sweeps;
+        ga.tol = h->tol;
+        cudaError_t e = run_jacobi_grid(ga, &h->gj_host_count, s, &h->launches);
+        if (e != cudaSuccess) return fail(DOBB_ERR_CUDA, "grid eigensolver: %s", cudaGetErrorString(e));
+        g0 = g1;
+      }
+    }
+    int b = g0;
     while (b < ch.eig_n && jacobi_smem_for(kof(b), half) == 0) ++b;
     EigArgs a{};
     a.info = h->dinfo();
@@ -421,7 +495,7 @@ dobb_status do_refresh(dobb_handle h, cudaStream_t s) {
     a.stats = h->stats();
     a.tol = h->tol;
     for (int part = 0; part < 2; ++part) {
-      const int lo = part == 0 ? 0 : b, hi = part == 0 ? b : ch.eig_n;
+      const int lo = part == 0 ? g0 : b, hi = part == 0 ? b : ch.eig_n;
       if (hi <= lo) continue;
       size_t smem = 0;
       for (int idx = lo; idx < hi; ++idx) {
@@ -615,6 +689,7 @@ dobb_status dobb_create(dobb_handle* out, int num_matrices, const int64_t* m, co
   }
   h->smem_limit = (size_t)optin - 2048;  // room for static shared memory
   if ((e = configure_jacobi(h->smem_limit)) != cudaSuccess || (e = configure_orth()) != cudaSuccess ||
+      (e = configure_jacobi_grid(h->smem_limit)) != cudaSuccess ||
       (e = configure_step(h->smem_limit)) != cudaSuccess ||
       (e = configure_step_tc(h->smem_limit)) != cudaSuccess ||
       (e = configure_syrk_tc(h->smem_limit)) != cudaSuccess) {
@@ -923,6 +998,16 @@ dobb_status dobb_set_refresh_period(dobb_handle h, int refresh_period) {
   if (!h) return fail(DOBB_ERR_INVALID_ARG, "NULL handle");
   if (refresh_period < 0) return fail(DOBB_ERR_INVALID_ARG, "refresh_period must be >= 0");
   h->T = refresh_period;
+  return DOBB_OK;
+}
+
+dobb_status dobb_set_eig_grid(dobb_handle h, int min_k, int64_t batch_bytes) {
+  if (!h) return fail(DOBB_ERR_INVALID_ARG, "NULL handle");
+  if (min_k != 0 && min_k < kGjMinK)
+    return fail(DOBB_ERR_INVALID_ARG, "grid eigensolver width threshold must be 0 or >= %d", kGjMinK);
+  if (batch_bytes < 0) return fail(DOBB_ERR_INVALID_ARG, "batch_bytes must be >= 0");
+  h->gj_min_k = min_k;
+  h->gj_batch_bytes = batch_bytes;
   return DOBB_OK;
 }
 

@@ -106,6 +106,50 @@ struct EigArgs {
   float tol;              // relative off-diagonal norm of the last sweep's B (0 = default)
 };
 
+// Grid eigensolver (jacobi_grid.cu): control record of one block, 64 bytes.
+struct GjCtl {
+  int32_t active;    // 1 while the block iterates
+  int32_t fresh;     // B was formed by Rayleigh-Ritz before the current sweep
+  int32_t restart;   // Newton-Schulz + Rayleigh-Ritz due after this sweep
+  int32_t sweeps;
+  int32_t conv;
+  int32_t rot;       // rotations of the current sweep
+  int32_t last_rot;
+  int32_t skip;      // A non-finite: basis kept
+  int32_t vsel;      // which of the two basis buffers holds V
+  float prev;        // off(B) after the previous sweep on a fresh B
+  float bfloor;      // rotation threshold
+  float pad;
+  double off2, tot2; // sums of the current off(B) evaluation
+};
+static_assert(sizeof(GjCtl) == 64, "GjCtl is 64 bytes");
+
+// One batch of the grid eigensolver: items of one width k.
+struct GjArgs {
+  const MatInfo* info;
+  const Tile* items;
+  int32_t nitems;
+  int32_t k;
+  const float* A;
+  float* Q;
+  float* lam;
+  float* scratch;       // 3 k^2 floats per block at 3 x the block's A offset
+  float* rbuf;          // per item rstride floats: the tables' rotations
+  int64_t rstride;
+  GjCtl* ctl;           // per item
+  int32_t* active_count;
+  uint32_t* flags;
+  float* stats;
+  int32_t max_sweeps;
+  float tol;
+};
+
+int64_t gj_rbuf_floats(int k);
+size_t gj_finish_smem(int k);
+cudaError_t configure_jacobi_grid(size_t smem_limit);
+// the whole refresh of one batch; synchronises the stream once per sweep
+cudaError_t run_jacobi_grid(GjArgs a, int* host_count, cudaStream_t s, int64_t* launches);
+
 // Coefficient normalisation of the FP32 update kernel.
 constexpr int32_t kModeSign = 0;
 constexpr int32_t kModeL2Apply = 2;

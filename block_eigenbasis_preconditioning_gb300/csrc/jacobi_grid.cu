@@ -1,0 +1,514 @@
+// Grid eigensolver for wide blocks ("Dobb", Abstract: a complete basis
+// within each block; Table 15: exact eigendecomposition refresh).
+//
+// The same method as the one-CTA-per-block solver of jacobi.cu -- cyclic
+// two-sided Jacobi in a Rayleigh-Ritz restart loop, sweeps blocked into a
+// round-robin tournament of column groups -- with the work of one block
+// spread over the whole GPU: every phase is one launch over a batch of
+// blocks of the same width, and within a launch every table, tile pair,
+// panel or product tile of every block is its own CTA.
+//
+//   init      V = current basis, ||A||_F, finiteness of A
+//   RR        T = A V, B = V^T T                        (64 x 64 product tiles)
+//   sweep     per round: tables (one CTA each: diagonal tile rotated, R_t
+//             kept), then every tile pair B[P_s, P_t] <- R_s^T B[P_s, P_t] R_t
+//             and every panel V[i0:i0+64, P_t] <- V[i0:i0+64, P_t] R_t
+//   control   off(B) = ||off(B)||_F / ||B||_F, the stopping and restart rules
+//             of jacobi.cu, per block, on the device
+//   restart   V <- V + V (I - V^T V) / 2 (Newton-Schulz), RR again
+//   finish    Lambda = diag(B), one more Newton-Schulz step, columns sorted by
+//             descending eigenvalue, Q written row-major
+//
+// Every launch reads a per-block control record and does nothing for blocks
+// that have finished, so the host issues a fixed sequence per sweep and only
+// reads the number of active blocks once per sweep to stop early.
+//
+// Per block state lives in the eigensolver scratch of the state buffer
+// (B, V and a work matrix: 3 k^2 floats) plus a rotation buffer and the
+// control record, both reused by every batch.
+#include <algorithm>
+
+#include "common.cuh"
+
+namespace dobb {
+namespace {
+
+constexpr int kThreads = 256;
+#include "fp32_tiles.cuh"
+#include "jacobi_common.cuh"
+static_assert(kThreads == kTileThreads, "the tile products assume 256 threads");
+
+constexpr int kTableThreads = 128;   // a table: one team of four warps
+
+// Scratch of item i: B, V0, V1 (the basis and the work matrix swap roles at
+// every Newton-Schulz step; ctl.vsel names the one holding the basis).
+struct ItemBufs {
+  float* B;
+  float* V;
+  float* W;
+  const float* A;
+  float* Q;
+  int64_t boff;
+  const MatInfo* mi;
+};
+
+__device__ __forceinline__ ItemBufs bufs_of(const GjArgs& a, int item) {
+  const Tile t = a.items[item];
+  const MatInfo* mi = a.info + t.mat;
+  const int64_t kk2 = (int64_t)a.k * a.k;
+  ItemBufs b;
+  b.boff = mi->a_off + (int64_t)t.blk * kk2;
+  b.B = a.scratch + 3 * b.boff;
+  float* v0 = b.B + kk2;
+  float* v1 = v0 + kk2;
+  const int vsel = a.ctl[item].vsel;
+  b.V = vsel ? v1 : v0;
+  b.W = vsel ? v0 : v1;
+  b.A = a.A + b.boff;
+  b.Q = a.Q + b.boff;
+  b.mi = mi;
+  return b;
+}
+
+// ------------------------------------------------------------------- init
+// V = Q^T-layout copy of the current basis (column j of V = column j of the
+// row-major Q), ||A||_F^2 and the finiteness of A, over chunks of entries.
+__global__ void __launch_bounds__(kThreads) gj_init_kernel(const __grid_constant__ GjArgs a) {
+  __shared__ double red[32];
+  const int item = blockIdx.y;
+  const ItemBufs b = bufs_of(a, item);
+  const int k = a.k;
+  const int64_t kk2 = (int64_t)k * k;
+  const int64_t per = (kk2 + gridDim.x - 1) / gridDim.x;
+  const int64_t e0 = (int64_t)blockIdx.x * per, e1 = min(kk2, e0 + per);
+  double ss = 0.0;
+  int bad = 0;
+  for (int64_t e = e0 + threadIdx.x; e < e1; e += blockDim.x) {
+    const float v = b.A[e];
+    bad |= !isfinite(v);
+    ss += (double)v * v;
+    const int64_t c = e / k, i = e - c * k;
+    b.V[e] = b.Q[i * k + c];
+  }
+  ss = block_sum_d(ss, red);
+  bad = __syncthreads_or(bad);
+  if (threadIdx.x == 0) {
+    atomicAdd(&a.ctl[item].tot2, ss);
+    if (bad) atomicOr(&a.ctl[item].skip, 1);
+  }
+}
+
+// One thread per item: start the iteration (or skip a non-finite block).
+__global__ void gj_start_kernel(const __grid_constant__ GjArgs a) {
+  const int item = blockIdx.x * blockDim.x + threadIdx.x;
+  if (item >= a.nitems) return;
+  GjCtl& c = a.ctl[item];
+  const Tile t = a.items[item];
+  const MatInfo mi = a.info[t.mat];
+  if (c.skip) {
+    atomicOr(a.flags + mi.blk0 + t.blk, (uint32_t)DOBB_FLAG_NONFINITE_A);
+    c.active = 0;
+  } else {
+    c.active = 1;
+  }
+  c.fresh = 1;
+  c.restart = 0;
+  c.sweeps = 0;
+  c.conv = 0;
+  c.rot = 0;
+  c.last_rot = 0;
+  c.prev = INFINITY;
+  c.bfloor = 1e-3f * kEps * (float)sqrt(c.tot2);
+  c.tot2 = 0.0;
+  c.off2 = 0.0;
+}
+
+// --------------------------------------------------------------- products
+// One 64 x 64 output tile of a k x k product per CTA (blockIdx.x = tile,
+// blockIdx.y = item).  Predicates: kAlways (every block not skipped),
+// kActive (blocks still iterating), kRestart (blocks that restart now).
+enum Pred : int { kAlways = 0, kActive = 1, kRestart = 2 };
+// Products: T = A V (RR1), B = V^T T (RR2, symmetric), E = I - V^T V (NS1,
+// symmetric, into B), V' = V + E V / 2 ... written as V + 0.5 V E (NS2, into W).
+enum Prod : int { kRR1 = 0, kRR2 = 1, kNS1 = 2, kNS2 = 3 };
+
+__device__ __forceinline__ bool pred_ok(const GjCtl& c, int pred) {
+  if (c.skip) return false;
+  if (pred == kActive) return c.active != 0;
+  if (pred == kRestart) return c.active != 0 && c.restart != 0;
+  return true;
+}
+
+__global__ void __launch_bounds__(kThreads) gj_gemm_kernel(const __grid_constant__ GjArgs a, int prod,
+                                                           int pred) {
+  extern __shared__ __align__(16) float gs[];
+  const int item = blockIdx.y;
+  if (!pred_ok(a.ctl[item], pred)) return;
+  const int k = a.k;
+  const int nt = (k + kT - 1) / kT;
+  const int ti = blockIdx.x % nt, tj = blockIdx.x / nt;
+  const bool sym = prod == kRR2 || prod == kNS1;
+  if (sym && ti > tj) return;
+  const ItemBufs b = bufs_of(a, item);
+  switch (prod) {
+    case kRR1:   // T (in W) = A V
+      gemm_tile<false>(b.A, b.V, b.W, nullptr, 1.f, false, false, k, ti, tj, gs);
+      break;
+    case kRR2:   // B = V^T T
+      gemm_tile<true>(b.V, b.W, b.B, nullptr, 1.f, false, true, k, ti, tj, gs);
+      break;
+    case kNS1:   // E (in B) = I - V^T V
+      gemm_tile<true>(b.V, b.V, b.B, nullptr, -1.f, true, true, k, ti, tj, gs);
+      break;
+    default:     // W = V + 0.5 V E
+      gemm_tile<false>(b.V, b.B, b.W, b.V, 0.5f, false, false, k, ti, tj, gs);
+      break;
+  }
+}
+
+// The basis moves to the other buffer after a Newton-Schulz step.
+__global__ void gj_flip_kernel(const __grid_constant__ GjArgs a, int pred) {
+  const int item = blockIdx.x * blockDim.x + threadIdx.x;
+  if (item >= a.nitems) return;
+  GjCtl& c = a.ctl[item];
+  if (pred_ok(c, pred)) c.vsel ^= 1;
+}
+
+// ----------------------------------------------------------------- sweeps
+// Tables of round br: one CTA (four warps, one team) per (table, item).
+__global__ void __launch_bounds__(kTableThreads) gj_table_kernel(const __grid_constant__ GjArgs a,
+                                                                 int br) {
+  extern __shared__ __align__(16) float sm[];
+  const int item = blockIdx.y, tt = blockIdx.x;
+  GjCtl* c = a.ctl + item;
+  if (!pred_ok(*c, kActive)) return;
+  const int k = a.k;
+  const Geo G = geo_for(k);
+  if (br >= G.nG - 1 || tt >= G.nT) return;
+  const ItemBufs b = bufs_of(a, item);
+  const int n2 = G.n2, nn = n2 * n2;
+  float* S = sm;
+  float* R = sm + nn;
+  int gI, gJ;
+  rr_pair(br, tt, G.nG, gI, gJ);
+  for (int e = threadIdx.x; e < nn; e += blockDim.x) {
+    const int r = e / n2, q = e - r * n2;
+    const int cr = table_col(r, gI, gJ, G.g, k), cq = table_col(q, gI, gJ, G.g, k);
+    S[e] = (cr < k && cq < k) ? b.B[(int64_t)cr * k + cq] : 0.f;
+    R[e] = r == q ? 1.f : 0.f;
+  }
+  __syncthreads();
+  const int warp = threadIdx.x >> 5;
+  const int rots = solve_table(S, R, br, tt, G, k, c->bfloor, warp, kTableThreads / 32, 1);
+  __syncthreads();
+  float* Rg = a.rbuf + (int64_t)item * a.rstride + (int64_t)tt * nn;
+  for (int e = threadIdx.x; e < nn; e += blockDim.x) {
+    const int r = e / n2, q = e - r * n2;
+    const int cr = table_col(r, gI, gJ, G.g, k), cq = table_col(q, gI, gJ, G.g, k);
+    if (cr < k && cq < k) b.B[(int64_t)cr * k + cq] = S[e];
+    Rg[e] = R[e];
+  }
+  int tot = rots;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+  if ((threadIdx.x & 31) == 0 && tot) atomicAdd(&c->rot, tot);
+}
+
+// Tile pairs and panels of round br: unit u < npair is the tile pair (s, t),
+// s < t, in row order; the rest are the panels (t, i0) of V.
+__global__ void __launch_bounds__(kThreads) gj_apply_kernel(const __grid_constant__ GjArgs a, int br) {
+  extern __shared__ __align__(16) float sm[];
+  const int item = blockIdx.y;
+  if (!pred_ok(a.ctl[item], kActive)) return;
+  const int k = a.k;
+  const Geo G = geo_for(k);
+  if (br >= G.nG - 1) return;
+  const int nI = (k + kT - 1) / kT;
+  const int npair = G.nT * (G.nT - 1) / 2;
+  const int u = blockIdx.x;
+  if (u >= npair + G.nT * nI) return;
+  const ItemBufs b = bufs_of(a, item);
+  const int n2 = G.n2, nn = n2 * n2;
+  const float* Rb = a.rbuf + (int64_t)item * a.rstride;
+  float* Rs = sm;
+  float* Rt = sm + kT * kLd;
+  float* Xt = sm + 2 * kT * kLd;
+  float* Yt = sm + 3 * kT * kLd;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
+  if (u < npair) {
+    // (s, t) from the linear index of the strict upper triangle
+    int s = 0, rem = u;
+    while (rem >= G.nT - 1 - s) {
+      rem -= G.nT - 1 - s;
+      ++s;
+    }
+    const int t = s + 1 + rem;
+    int sI, sJ, tI, tJ;
+    rr_pair(br, s, G.nG, sI, sJ);
+    rr_pair(br, t, G.nG, tI, tJ);
+    load_rot(Rs, Rb + (int64_t)s * nn, n2);
+    load_rot(Rt, Rb + (int64_t)t * nn, n2);
+    for (int e = tid; e < kT * kT; e += blockDim.x) {
+      const int r = e / kT, q = e - r * kT;
+      const int cr = r < n2 ? table_col(r, sI, sJ, G.g, k) : k;
+      const int cq = q < n2 ? table_col(q, tI, tJ, G.g, k) : k;
+      Xt[r * kLd + q] = (cr < k && cq < k) ? b.B[(int64_t)cr * k + cq] : 0.f;
+    }
+    __syncthreads();
+    float acc[4][4];
+    zero_acc(acc);
+    micro_tn(Rs, Xt, kLd, n2, acc);  // Y = R_s^T X
+    store_acc_t(Yt, kLd, acc);       // Y^T
+    __syncthreads();
+    zero_acc(acc);
+    micro_tn(Yt, Rt, kLd, n2, acc);  // Z = Y R_t
+    __syncthreads();
+    store_acc(Xt, kLd, acc);         // Z
+    store_acc_t(Yt, kLd, acc);       // Z^T
+    __syncthreads();
+    for (int r = warp; r < n2; r += nw) {
+      const int cr = table_col(r, sI, sJ, G.g, k), ct = table_col(r, tI, tJ, G.g, k);
+      for (int q = lane; q < n2; q += 32) {
+        const int cq = table_col(q, tI, tJ, G.g, k), cs = table_col(q, sI, sJ, G.g, k);
+        if (cr < k && cq < k) b.B[(int64_t)cr * k + cq] = Xt[r * kLd + q];
+        if (ct < k && cs < k) b.B[(int64_t)ct * k + cs] = Yt[r * kLd + q];
+      }
+    }
+  } else {
+    const int v = u - npair;
+    const int t = v / nI, i0 = (v - t * nI) * kT;
+    int tI, tJ;
+    rr_pair(br, t, G.nG, tI, tJ);
+    load_rot(Rt, Rb + (int64_t)t * nn, n2);
+    for (int e = tid; e < kT * kT; e += blockDim.x) {
+      const int r = e / kT, i = e - r * kT;
+      const int cr = r < n2 ? table_col(r, tI, tJ, G.g, k) : k;
+      Xt[r * kLd + i] = (cr < k && i0 + i < k) ? b.V[(int64_t)cr * k + i0 + i] : 0.f;
+    }
+    __syncthreads();
+    float acc[4][4];
+    zero_acc(acc);
+    micro_tn(Xt, Rt, kLd, n2, acc);  // rows i of V times R_t
+    store_acc_t(Yt, kLd, acc);
+    __syncthreads();
+    for (int q = warp; q < n2; q += nw) {
+      const int cq = table_col(q, tI, tJ, G.g, k);
+      if (cq >= k) continue;
+      for (int i = lane; i < kT; i += 32)
+        if (i0 + i < k) b.V[(int64_t)cq * k + i0 + i] = Yt[q * kLd + i];
+    }
+  }
+}
+
+// ---------------------------------------------------------------- control
+// ||off(B)||_F^2 and ||B||_F^2 over chunks of entries.
+__global__ void __launch_bounds__(kThreads) gj_off_kernel(const __grid_constant__ GjArgs a) {
+  __shared__ double red[32];
+  const int item = blockIdx.y;
+  if (!pred_ok(a.ctl[item], kActive)) return;
+  const ItemBufs b = bufs_of(a, item);
+  const int k = a.k;
+  const int64_t kk2 = (int64_t)k * k;
+  const int64_t per = (kk2 + gridDim.x - 1) / gridDim.x;
+  const int64_t e0 = (int64_t)blockIdx.x * per, e1 = min(kk2, e0 + per);
+  double tot = 0.0, off = 0.0;
+  for (int64_t e = e0 + threadIdx.x; e < e1; e += blockDim.x) {
+    const double v = b.B[e];
+    tot += v * v;
+    const int64_t i = e / k;
+    if (e - i * k != i) off += v * v;
+  }
+  tot = block_sum_d(tot, red);
+  __syncthreads();
+  off = block_sum_d(off, red);
+  if (threadIdx.x == 0) {
+    atomicAdd(&a.ctl[item].tot2, tot);
+    atomicAdd(&a.ctl[item].off2, off);
+  }
+}
+
+// One thread per item: the rules of jacobi.cu after a sweep.  Writes the
+// number of blocks still iterating to a.active_count.
+__global__ void gj_control_kernel(const __grid_constant__ GjArgs a) {
+  const int item = blockIdx.x * blockDim.x + threadIdx.x;
+  int still = 0;
+  if (item < a.nitems) {
+    GjCtl& c = a.ctl[item];
+    if (!c.skip && c.active) {
+      const float off = c.tot2 > 0.0 ? (float)sqrt(c.off2 / c.tot2) : 0.f;
+      const float stop = a.tol > 0.f ? a.tol : kStopOff;
+      c.sweeps += 1;
+      c.last_rot = c.rot;
+      c.restart = 0;
+      bool done = false;
+      if (c.fresh) {
+        if (off <= stop || c.rot == 0 || (off <= kStallOff && off > 0.7f * c.prev)) {
+          c.conv = 1;
+          done = true;
+        } else {
+          c.prev = off;
+        }
+      }
+      if (!done && c.sweeps >= a.max_sweeps) done = true;
+      if (done) {
+        c.active = 0;
+      } else {
+        c.fresh = 0;
+        if (off <= kColdOff) {  // close to diagonal: restart from a fresh B
+          c.restart = 1;
+          c.fresh = 1;
+        }
+      }
+      c.rot = 0;
+      c.off2 = 0.0;
+      c.tot2 = 0.0;
+      still = c.active;
+    }
+  }
+  still = __syncthreads_count(still);
+  if (threadIdx.x == 0 && still) atomicAdd(a.active_count, still);
+}
+
+// ----------------------------------------------------------------- finish
+// Lambda (unsorted) = diag(B) into the eigenvalue slots, before the last
+// Newton-Schulz step reuses B's buffer.
+__global__ void gj_diag_kernel(const __grid_constant__ GjArgs a) {
+  const int item = blockIdx.y;
+  if (a.ctl[item].skip) return;
+  const ItemBufs b = bufs_of(a, item);
+  const Tile t = a.items[item];
+  const int k = a.k;
+  float* lam = a.lam + b.mi->lam_off + (int64_t)t.blk * k;
+  for (int j = blockIdx.x * blockDim.x + threadIdx.x; j < k; j += gridDim.x * blockDim.x)
+    lam[j] = b.B[(int64_t)j * k + j];
+}
+
+// One CTA per item: sort by descending eigenvalue (bitonic, in shared
+// memory), write Q row-major with the columns permuted, stats and flags.
+__global__ void __launch_bounds__(kThreads) gj_finish_kernel(const __grid_constant__ GjArgs a) {
+  extern __shared__ __align__(16) float sm[];
+  const int item = blockIdx.x;
+  const GjCtl c = a.ctl[item];
+  const Tile t = a.items[item];
+  const MatInfo mi = a.info[t.mat];
+  if (c.skip) return;
+  const ItemBufs b = bufs_of(a, item);
+  const int k = a.k, kp2 = pow2_ceil(k);
+  float* lamv = sm;
+  int* perm = reinterpret_cast<int*>(sm + kp2);
+  float* lam = a.lam + mi.lam_off + (int64_t)t.blk * k;
+  for (int p = threadIdx.x; p < kp2; p += blockDim.x) {
+    lamv[p] = p < k ? lam[p] : -INFINITY;
+    perm[p] = p;
+  }
+  __syncthreads();
+  for (int size = 2; size <= kp2; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = threadIdx.x; i < kp2; i += blockDim.x) {
+        const int j = i ^ stride;
+        if (j > i) {
+          const bool desc = (i & size) == 0;
+          const float li = lamv[i], lj = lamv[j];
+          if (desc ? (li < lj) : (li > lj)) {
+            lamv[i] = lj;
+            lamv[j] = li;
+            const int pt = perm[i];
+            perm[i] = perm[j];
+            perm[j] = pt;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+  for (int64_t e = threadIdx.x; e < (int64_t)k * k; e += blockDim.x) {
+    const int64_t i = e / k, j = e - i * k;
+    int p = perm[j];
+    if (p < 0 || p >= k) p = (int)j;  // only reachable with a NaN eigenvalue
+    b.Q[e] = b.V[(int64_t)p * k + i];
+  }
+  for (int j = threadIdx.x; j < k; j += blockDim.x) lam[j] = lamv[j];
+  if (threadIdx.x == 0) {
+    float* st = a.stats + 4 * (int64_t)(mi.blk0 + t.blk);
+    st[2] = (float)c.sweeps;
+    st[3] = (float)c.last_rot;
+    if (!c.conv) atomicOr(a.flags + mi.blk0 + t.blk, (uint32_t)DOBB_FLAG_NOT_CONVERGED);
+  }
+}
+
+size_t apply_smem() { return 4 * (size_t)kT * kLd * sizeof(float); }
+size_t gemm_smem() { return (size_t)kGemmFloats * sizeof(float); }
+
+}  // namespace
+
+int64_t gj_rbuf_floats(int k) {
+  const Geo G = geo_for(k);
+  return (int64_t)G.nT * G.n2 * G.n2;
+}
+
+size_t gj_finish_smem(int k) { return 2 * (size_t)pow2_ceil(k) * sizeof(float); }
+
+cudaError_t configure_jacobi_grid(size_t smem_limit) {
+  cudaError_t e = cudaFuncSetAttribute(gj_apply_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)apply_smem());
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(gj_finish_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)std::min<size_t>(smem_limit, gj_finish_smem(kMaxK)));
+  return e;
+}
+
+// The whole refresh of one batch (blocks of one width k).  Synchronises the
+// stream once per sweep (to read how many blocks still iterate).
+cudaError_t run_jacobi_grid(GjArgs a, int* host_count, cudaStream_t s, int64_t* launches) {
+  if (a.nitems <= 0) return cudaSuccess;
+  const int k = a.k;
+  const Geo G = geo_for(k);
+  const int nt = (k + kT - 1) / kT;
+  const int nI = nt;
+  const int npair = G.nT * (G.nT - 1) / 2;
+  const dim3 tiles(nt * nt, a.nitems);
+  const int chunks = (int)std::max<int64_t>(1, std::min<int64_t>(256, (int64_t)k * k / (64 * 1024)));
+  const dim3 cgrid(chunks, a.nitems);
+  const int ctl_blocks = (a.nitems + 255) / 256;
+  const size_t gsm = gemm_smem(), asm_ = apply_smem(), tsm = 2 * (size_t)G.n2 * G.n2 * sizeof(float);
+  int64_t n = 0;
+  cudaError_t e = cudaMemsetAsync(a.ctl, 0, sizeof(GjCtl) * (size_t)a.nitems, s);
+  if (e != cudaSuccess) return e;
+  gj_init_kernel<<<cgrid, kThreads, 0, s>>>(a);
+  gj_start_kernel<<<ctl_blocks, 256, 0, s>>>(a);
+  gj_gemm_kernel<<<tiles, kThreads, gsm, s>>>(a, kRR1, kActive);
+  gj_gemm_kernel<<<tiles, kThreads, gsm, s>>>(a, kRR2, kActive);
+  n += 4;
+  for (int sweep = 0; sweep < a.max_sweeps; ++sweep) {
+    for (int br = 0; br < G.nG - 1; ++br) {
+      gj_table_kernel<<<dim3(G.nT, a.nitems), kTableThreads, tsm, s>>>(a, br);
+      gj_apply_kernel<<<dim3(npair + G.nT * nI, a.nitems), kThreads, asm_, s>>>(a, br);
+      n += 2;
+    }
+    e = cudaMemsetAsync(a.active_count, 0, sizeof(int), s);
+    if (e != cudaSuccess) return e;
+    gj_off_kernel<<<cgrid, kThreads, 0, s>>>(a);
+    gj_control_kernel<<<ctl_blocks, 256, 0, s>>>(a);
+    // restart: Newton-Schulz (E into B, V' into W, swap), then RR
+    gj_gemm_kernel<<<tiles, kThreads, gsm, s>>>(a, kNS1, kRestart);
+    gj_gemm_kernel<<<tiles, kThreads, gsm, s>>>(a, kNS2, kRestart);
+    gj_flip_kernel<<<ctl_blocks, 256, 0, s>>>(a, kRestart);
+    gj_gemm_kernel<<<tiles, kThreads, gsm, s>>>(a, kRR1, kRestart);
+    gj_gemm_kernel<<<tiles, kThreads, gsm, s>>>(a, kRR2, kRestart);
+    n += 7;
+    e = cudaMemcpyAsync(host_count, a.active_count, sizeof(int), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return e;
+    if (*host_count == 0) break;
+  }
+  gj_diag_kernel<<<dim3((k + 255) / 256, a.nitems), 256, 0, s>>>(a);
+  gj_gemm_kernel<<<tiles, kThreads, gsm, s>>>(a, kNS1, kAlways);
+  gj_gemm_kernel<<<tiles, kThreads, gsm, s>>>(a, kNS2, kAlways);
+  gj_flip_kernel<<<ctl_blocks, 256, 0, s>>>(a, kAlways);
+  gj_finish_kernel<<<a.nitems, kThreads, gj_finish_smem(k), s>>>(a);
+  n += 5;
+  if (launches) *launches += n;
+  return cudaGetLastError();
+}
+
+}  // namespace dobb

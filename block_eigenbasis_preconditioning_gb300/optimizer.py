@@ -161,6 +161,12 @@ class Dobb:
         """Refresh every `refresh_period` steps from now on (0 = never)."""
         check(self.lib.dobb_set_refresh_period(self.handle, int(refresh_period)))
 
+    def set_eig_grid(self, min_k: int, batch_bytes: int = 0) -> None:
+        """Blocks at least `min_k` wide refresh with the grid eigensolver (0 =
+        never), in batches of blocks of one width whose scratch fits
+        `batch_bytes` (0 = all blocks of a width at once)."""
+        check(self.lib.dobb_set_eig_grid(self.handle, int(min_k), int(batch_bytes)))
+
     def set_jacobi(self, max_sweeps: int = 40, tol: float = 0.0) -> None:
         check(self.lib.dobb_set_jacobi(self.handle, int(max_sweeps), float(tol)))
 

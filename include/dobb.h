@@ -200,6 +200,17 @@ dobb_status dobb_set_basis_dtype(dobb_handle h, dobb_dtype basis_dtype, void* st
  * kept.  DOBB_ERR_INVALID_ARG for T < 0. */
 dobb_status dobb_set_refresh_period(dobb_handle h, int refresh_period);
 
+/* Which eigensolver refreshes a block: blocks at least `min_k` wide use the
+ * grid solver (every table, tile pair and panel of a sweep its own CTA, a
+ * launch per phase over a batch of blocks of one width; the call then
+ * synchronises `stream` once per sweep), narrower ones one CTA per block.
+ * Both run the same restarted Rayleigh-Ritz two-sided Jacobi.  0 = never the
+ * grid solver; otherwise min_k >= 128.  A batch holds the blocks of one width
+ * whose scratch (12 k^2 bytes each) fits `batch_bytes` (at least one block;
+ * 0 = all blocks of that width).  Defaults: 449, 0.  DOBB_ERR_INVALID_ARG for
+ * other values. */
+dobb_status dobb_set_eig_grid(dobb_handle h, int min_k, int64_t batch_bytes);
+
 /* Eigensolver controls: sweep cap (default 40) and the convergence
  * threshold, the relative off-diagonal norm ||off(B)||_F / ||B||_F that the
  * last sweep of B = V^T A V may leave (0 = default 2e-6). */

@@ -76,7 +76,23 @@ def make_output_side_problem(shapes, N, eff, seed, param_dtype="f32", act_dtype=
     return Ds, Gs, Ws
 
 
-def check_moments(opt, orc, matrices=None):
+def moment_tolerance(N):
+    """Tolerance of fp32 block moments accumulated over N tokens: max(1e-5,
+    N u / 2), u = 2^-24.  Each of the N additions into an fp32 accumulator
+    may lose up to u of the partial sum (N u relative on the diagonal, whose
+    terms are all positive); an accumulator that truncates loses half of that
+    on average, which is what a sum on the tensor cores shows (1.1e-5 at
+    N = 4096).  Small N keeps the fixed 1e-5, which the per-token moment tests
+    (ragged N up to 300) use; at N = 4096 a block missing one token (2.4e-4)
+    still fails."""
+    return max(TOL_A, N * 2.0 ** -24 / 2)
+
+
+def check_moments(opt, orc, matrices=None, N=None):
+    """GPU block moments against the oracle's, relative Frobenius per block,
+    within TOL_A, or within `moment_tolerance(N)` when the token count of the
+    accumulations is given."""
+    tol = moment_tolerance(N) if N is not None else TOL_A
     worst = 0.0
     for i in (matrices if matrices is not None else range(len(orc.shapes))):
         Ag = to_np(opt.tensor("moments", i))
@@ -86,7 +102,7 @@ def check_moments(opt, orc, matrices=None):
             err = np.linalg.norm(Ag[b] - Ar[b]) / (fro if fro > 0 else 1.0)
             worst = max(worst, err)
             assert np.array_equal(Ag[b], Ag[b].T), "A must stay exactly symmetric"
-    assert worst <= TOL_A, f"block moments relative error {worst:.3e}"
+            assert err <= tol, f"matrix {i} block {b}: moments relative error {err:.3e} > {tol:.3e}"
     return worst
 
 

@@ -48,7 +48,10 @@ def _streams(shapes, eff, rng):
 def test_gpt2_small_fifty_steps():
     """GPT-2 Small: 12 layers x {q, k, v, o 768 x 768; fc 3072 x 768; proj
     768 x 3072}, fp32 parameters, gradients and activations, B = 16, beta1
-    0.95, beta2 0.99, lr 0.02, s 1, refresh every 10 steps, 50 steps."""
+    0.95, beta2 0.99, lr 0.02, s 1, refresh every 10 steps, 50 steps.  The
+    moments of every block are checked at every step, the bases at every
+    refresh, the update of all 72 matrices at every fifth step and at the
+    step after each refresh, and of one layer's matrices at the others."""
     ms = I.gpt2_small_shapes()
     shapes, B, N, T, steps = ms.shapes, 16, 4096, 10, 50
     rng = np.random.default_rng(60)
@@ -68,14 +71,18 @@ def test_gpt2_small_fifty_steps():
         opt.step(Wd, Gd, 0.02, signs=Sd)
         torch.cuda.synchronize()
         assert opt.device_error() == 0
-        check_moments(opt, orc)
+        check_moments(opt, orc, N=N)
         if t % T == 0:
             check_bases(opt, [to_np(opt.tensor("moments", i)) for i in range(len(shapes))])
             assert np.all(opt.block_flags() == 0)
+        # every matrix's update at every fifth step (the refresh steps and the
+        # steps right after them among them), one layer's six matrices otherwise
+        full = t % 5 == 0 or t % T == 1
         for i, (m, n) in enumerate(shapes):
-            check_update(W_prev[i], M_prev[i], Gs[i], to_np(opt.tensor("bases", i)), to_np(Sd[i]),
-                         to_np(Wd[i]), to_np(opt.tensor("momentum", i)), 0.95, 0.02, 1.0, "f32",
-                         n // B)
+            if full or i // 6 == t % 12:
+                check_update(W_prev[i], M_prev[i], Gs[i], to_np(opt.tensor("bases", i)),
+                             to_np(Sd[i]), to_np(Wd[i]), to_np(opt.tensor("momentum", i)), 0.95,
+                             0.02, 1.0, "f32", n // B)
             orc.M[i] = O.momentum(M_prev[i], Gs[i], 0.95)
 
 
@@ -139,7 +146,7 @@ def test_llama3_8b_layer_and_vocabulary_matrices():
         opt.step(Wd, Gd, 0.02, signs=Sd)
         torch.cuda.synchronize()
         assert opt.device_error() == 0
-        check_moments(opt, orc)
+        check_moments(opt, orc, N=N)
         if t % T == 0:
             check_bases(opt, orc.A)
             assert np.all(opt.block_flags() == 0)
@@ -155,3 +162,19 @@ def test_llama3_8b_layer_and_vocabulary_matrices():
                          to_np(opt.tensor("momentum", i)[ridx]), 0.95, 0.02, 1.0, "bf16", n // B)
             M_prev[i] = (0.95 * M_prev[i].astype(np.float64) + Gs[i]).astype(np.float32) \
                 if m <= 20000 else to_np(opt.tensor("momentum", i)).astype(np.float32)
+
+
+def test_refresh_stress_one_block_per_matrix_k6400():
+    """The widest refresh-stress block: GPT-2 XL proj at B = 1 (k = 6400),
+    an SPD block with relative gaps >= 1e-3 and condition number 1e6,
+    eigensolved from the identity by the grid solver, scored with the eigen
+    tolerances (residual, reconstruction, orthogonality, eigenvalues)."""
+    k = 6400
+    rng = np.random.default_rng(63)
+    A = I.spd_with_gap(k, rng, cond=1e6, min_rel_gap=1e-3)[0]
+    opt = _dobb([(4, k)], 1, refresh_period=0)
+    opt.tensor("moments", 0).copy_(torch.from_numpy(A.astype(np.float32)).view(1, k, k))
+    opt.refresh()
+    torch.cuda.synchronize()
+    assert np.all(opt.block_flags() == 0)
+    check_bases(opt, [A.astype(np.float32).astype(np.float64)[None]])
