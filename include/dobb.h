@@ -205,9 +205,9 @@ dobb_status dobb_set_refresh_period(dobb_handle h, int refresh_period);
  * launch per phase over a batch of blocks of one width; the call then
  * synchronises `stream` once per sweep), narrower ones one CTA per block.
  * Both run the same restarted Rayleigh-Ritz two-sided Jacobi.  0 = never the
- * grid solver; otherwise min_k >= 128.  A batch holds the blocks of one width
+ * grid solver; otherwise min_k >= 64.  A batch holds the blocks of one width
  * whose scratch (12 k^2 bytes each) fits `batch_bytes` (at least one block;
- * 0 = all blocks of that width).  Defaults: 449, 0.  DOBB_ERR_INVALID_ARG for
+ * 0 = all blocks of that width).  Defaults: 128, 0.  DOBB_ERR_INVALID_ARG for
  * other values. */
 dobb_status dobb_set_eig_grid(dobb_handle h, int min_k, int64_t batch_bytes);
 

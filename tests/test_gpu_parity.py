@@ -73,12 +73,17 @@ def test_moments_skip_null_and_flag_nonfinite():
 # (a2) eigen refresh
 # --------------------------------------------------------------------------
 
-@pytest.mark.parametrize("k", [1, 2, 3, 5, 16, 48, 100, 128, 168, 169, 192, 400, 448])
-def test_refresh_on_spd_blocks_with_gaps(k):
+@pytest.mark.parametrize("solver", ["default", "one-cta"])
+@pytest.mark.parametrize("k", [1, 2, 3, 5, 16, 48, 64, 100, 128, 168, 169, 192, 400, 448])
+def test_refresh_on_spd_blocks_with_gaps(k, solver):
+    """Both eigensolvers (by default the grid solver for k >= 128 and one CTA
+    per block below; "one-cta" forces the latter) on SPD blocks with gaps."""
     rng = np.random.default_rng(k)
     B = 2
     shapes = [(4, B * k)]
     opt = _dobb(shapes, B, refresh_period=0)
+    if solver == "one-cta":
+        opt.set_eig_grid(0)
     A = np.stack([I.spd_with_gap(k, rng, cond=1e6)[0] if k > 1 else np.array([[0.7]])
                   for _ in range(B)])
     opt.tensor("moments", 0).copy_(torch.from_numpy(A.astype(np.float32)).view(B, k, k))
