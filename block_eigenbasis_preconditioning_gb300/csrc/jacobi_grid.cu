@@ -36,6 +36,7 @@ namespace {
 constexpr int kThreads = 256;
 #include "fp32_tiles.cuh"
 #include "jacobi_common.cuh"
+#include "mma_tf32.cuh"
 static_assert(kThreads == kTileThreads, "the tile products assume 256 threads");
 
 constexpr int kTableThreads = 128;   // a table: one team of four warps
@@ -214,12 +215,35 @@ __global__ void __launch_bounds__(kTableThreads) gj_table_kernel(const __grid_co
   if ((threadIdx.x & 31) == 0 && tot) atomicAdd(&c->rot, tot);
 }
 
+// E = R - I of table t into a zero-padded 64 x kLdM tile.
+__device__ __forceinline__ void load_corr(float* dst, const float* src, int n2) {
+  for (int e = threadIdx.x; e < kT * kT; e += blockDim.x) {
+    const int r = e / kT, q = e - r * kT;
+    dst[r * kLdM + q] = (r < n2 && q < n2) ? src[r * n2 + q] - (r == q ? 1.f : 0.f) : 0.f;
+  }
+}
+
+template <int kPasses>
+__device__ __forceinline__ void corr_product(const float* P, const float* Q, int n, float (&acc)[4][4]) {
+  mma_tn_64<kPasses>(P, Q, n, acc);
+}
+
 // Tile pairs and panels of round br: unit u < npair is the tile pair (s, t),
-// s < t, in row order; the rest are the panels (t, i0) of V.
+// s < t, in row order; the rest are the panels (t, i0) of V.  The products
+// run on the warp-level tensor cores in correction form: with E = R - I,
+//   Y = X + E_s^T X,  Z = Y + Y E_t       (B[P_s, P_t] <- R_s^T X R_t)
+//   V' = V + V E_t                         (V[i0:i0+64, P_t] <- V R_t)
+// the TF32-rounded products added onto fp32 X, Y, V.  A sweep on a freshly
+// formed B (the only kind that can end the iteration) multiplies in split
+// precision (~2^-21 |E| |X|); the other sweeps, whose B is re-formed from A
+// before the iteration can stop and whose basis only seeds that re-forming,
+// in plain TF32.
 __global__ void __launch_bounds__(kThreads) gj_apply_kernel(const __grid_constant__ GjArgs a, int br) {
   extern __shared__ __align__(16) float sm[];
   const int item = blockIdx.y;
-  if (!pred_ok(a.ctl[item], kActive)) return;
+  const GjCtl& cref = a.ctl[item];
+  if (!pred_ok(cref, kActive)) return;
+  const bool precise = cref.fresh != 0;
   const int k = a.k;
   const Geo G = geo_for(k);
   if (br >= G.nG - 1) return;
@@ -230,11 +254,12 @@ __global__ void __launch_bounds__(kThreads) gj_apply_kernel(const __grid_constan
   const ItemBufs b = bufs_of(a, item);
   const int n2 = G.n2, nn = n2 * n2;
   const float* Rb = a.rbuf + (int64_t)item * a.rstride;
-  float* Rs = sm;
-  float* Rt = sm + kT * kLd;
-  float* Xt = sm + 2 * kT * kLd;
-  float* Yt = sm + 3 * kT * kLd;
+  float* Es = sm;
+  float* Et = sm + kT * kLdM;
+  float* Xs = sm + 2 * kT * kLdM;
+  float* Ys = sm + 3 * kT * kLdM;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
+  float acc[4][4];
   if (u < npair) {
     // (s, t) from the linear index of the strict upper triangle
     int s = 0, rem = u;
@@ -246,32 +271,32 @@ __global__ void __launch_bounds__(kThreads) gj_apply_kernel(const __grid_constan
     int sI, sJ, tI, tJ;
     rr_pair(br, s, G.nG, sI, sJ);
     rr_pair(br, t, G.nG, tI, tJ);
-    load_rot(Rs, Rb + (int64_t)s * nn, n2);
-    load_rot(Rt, Rb + (int64_t)t * nn, n2);
+    load_corr(Es, Rb + (int64_t)s * nn, n2);
+    load_corr(Et, Rb + (int64_t)t * nn, n2);
     for (int e = tid; e < kT * kT; e += blockDim.x) {
       const int r = e / kT, q = e - r * kT;
       const int cr = r < n2 ? table_col(r, sI, sJ, G.g, k) : k;
       const int cq = q < n2 ? table_col(q, tI, tJ, G.g, k) : k;
-      Xt[r * kLd + q] = (cr < k && cq < k) ? b.B[(int64_t)cr * k + cq] : 0.f;
+      Xs[r * kLdM + q] = (cr < k && cq < k) ? b.B[(int64_t)cr * k + cq] : 0.f;
     }
     __syncthreads();
-    float acc[4][4];
-    zero_acc(acc);
-    micro_tn(Rs, Xt, kLd, n2, acc);  // Y = R_s^T X
-    store_acc_t(Yt, kLd, acc);       // Y^T
+    mma_load_acc<false>(Xs, acc);                     // X
+    if (precise) corr_product<3>(Es, Xs, n2, acc);    // Y = X + E_s^T X
+    else corr_product<1>(Es, Xs, n2, acc);
+    mma_store_acc<true>(Ys, acc);                     // Y^T
     __syncthreads();
-    zero_acc(acc);
-    micro_tn(Yt, Rt, kLd, n2, acc);  // Z = Y R_t
+    if (precise) corr_product<3>(Ys, Et, n2, acc);    // Z = Y + Y E_t
+    else corr_product<1>(Ys, Et, n2, acc);
     __syncthreads();
-    store_acc(Xt, kLd, acc);         // Z
-    store_acc_t(Yt, kLd, acc);       // Z^T
+    mma_store_acc<false>(Xs, acc);                    // Z
+    mma_store_acc<true>(Ys, acc);                     // Z^T
     __syncthreads();
     for (int r = warp; r < n2; r += nw) {
       const int cr = table_col(r, sI, sJ, G.g, k), ct = table_col(r, tI, tJ, G.g, k);
       for (int q = lane; q < n2; q += 32) {
         const int cq = table_col(q, tI, tJ, G.g, k), cs = table_col(q, sI, sJ, G.g, k);
-        if (cr < k && cq < k) b.B[(int64_t)cr * k + cq] = Xt[r * kLd + q];
-        if (ct < k && cs < k) b.B[(int64_t)ct * k + cs] = Yt[r * kLd + q];
+        if (cr < k && cq < k) b.B[(int64_t)cr * k + cq] = Xs[r * kLdM + q];
+        if (ct < k && cs < k) b.B[(int64_t)ct * k + cs] = Ys[r * kLdM + q];
       }
     }
   } else {
@@ -279,23 +304,23 @@ __global__ void __launch_bounds__(kThreads) gj_apply_kernel(const __grid_constan
     const int t = v / nI, i0 = (v - t * nI) * kT;
     int tI, tJ;
     rr_pair(br, t, G.nG, tI, tJ);
-    load_rot(Rt, Rb + (int64_t)t * nn, n2);
+    load_corr(Et, Rb + (int64_t)t * nn, n2);
     for (int e = tid; e < kT * kT; e += blockDim.x) {
       const int r = e / kT, i = e - r * kT;
       const int cr = r < n2 ? table_col(r, tI, tJ, G.g, k) : k;
-      Xt[r * kLd + i] = (cr < k && i0 + i < k) ? b.V[(int64_t)cr * k + i0 + i] : 0.f;
+      Xs[r * kLdM + i] = (cr < k && i0 + i < k) ? b.V[(int64_t)cr * k + i0 + i] : 0.f;
     }
     __syncthreads();
-    float acc[4][4];
-    zero_acc(acc);
-    micro_tn(Xt, Rt, kLd, n2, acc);  // rows i of V times R_t
-    store_acc_t(Yt, kLd, acc);
+    mma_load_acc<true>(Xs, acc);                      // V rows i, table columns q
+    if (precise) corr_product<3>(Xs, Et, n2, acc);    // V + V E_t
+    else corr_product<1>(Xs, Et, n2, acc);
+    mma_store_acc<true>(Ys, acc);
     __syncthreads();
     for (int q = warp; q < n2; q += nw) {
       const int cq = table_col(q, tI, tJ, G.g, k);
       if (cq >= k) continue;
       for (int i = lane; i < kT; i += 32)
-        if (i0 + i < k) b.V[(int64_t)cq * k + i0 + i] = Yt[q * kLd + i];
+        if (i0 + i < k) b.V[(int64_t)cq * k + i0 + i] = Ys[q * kLdM + i];
     }
   }
 }
@@ -436,7 +461,7 @@ __global__ void __launch_bounds__(kThreads) gj_finish_kernel(const __grid_consta
   }
 }
 
-size_t apply_smem() { return 4 * (size_t)kT * kLd * sizeof(float); }
+size_t apply_smem() { return 4 * (size_t)kT * kLdM * sizeof(float); }
 size_t gemm_smem() { return (size_t)kGemmFloats * sizeof(float); }
 
 }  // namespace
