@@ -706,50 +706,58 @@ def run_gpu(args):
     return 0
 
 
-def _bind_to_gpu_local_cpus(torch):
-    """Run this process on the host cores attached to the current GPU while the
-    pinned input buffers are allocated, so that their pages land in that
-    socket's memory.  Best effort: a system that does not expose the GPU's
-    local CPUs is left as is."""
-    try:
-        props = torch.cuda.get_device_properties(torch.cuda.current_device())
-        bus = "%04x:%02x:%02x.0" % (props.pci_domain_id, props.pci_bus_id, props.pci_device_id)
-        with open(f"/sys/bus/pci/devices/{bus}/local_cpulist") as f:
-            spec = f.read().strip()
-        cpus = set()
-        for part in spec.split(","):
-            lo, _, hi = part.partition("-")
-            cpus.update(range(int(lo), int(hi or lo) + 1))
-        if cpus:
-            os.sched_setaffinity(0, cpus)
-    except Exception:
-        pass
+def _flat(torch, like, device=None, pin=False):
+    """One flat buffer with room for tensors shaped like `like` (one dtype),
+    each view starting on a 256-byte boundary; returns (buffer, views)."""
+    esz = like[0].element_size()
+    align = max(1, 256 // esz)
+    offs, tot = [], 0
+    for t in like:
+        offs.append(tot)
+        tot += (t.numel() + align - 1) // align * align
+    if pin:
+        buf = torch.empty(tot, dtype=like[0].dtype).pin_memory()
+    else:
+        buf = torch.empty(tot, dtype=like[0].dtype, device=device)
+    views = [buf[o:o + t.numel()].view(t.shape) for o, t in zip(offs, like)]
+    return buf, views
 
 
 def run_e2e(torch, opt, cfg, shapes, lay, sides, W, K, stream, params, world):
     """End to end through the public API with host buffers.  Every step
     copies that step's activations and gradients from pinned host memory
-    (two independently drawn host sets, alternating), runs accumulate (+
-    refresh) + step, and copies the updated parameters back to pinned host
-    memory.  The input copies of step i+1 run on two copy streams during
-    step i (double-buffered device inputs); the parameter copy of step i
-    runs on a third stream while step i+1 accumulates, and step i+1's update
-    waits for it."""
-    prev_cpus = os.sched_getaffinity(0)
-    _bind_to_gpu_local_cpus(torch)
-    Xs2, Gs2, _ = make_train_inputs(torch, dict(cfg, pool=2), shapes, lay, W[0].device, seed=777,
+    (two independently drawn host sets, alternating) and copies the updated
+    parameters back to pinned host memory; the inputs and parameters of all
+    matrices sit in one flat buffer per kind (a flat parameter buffer, as a
+    training loop keeps them), so a step moves three contiguous copies.  The
+    input copies of step i+1 run on two copy streams during step i
+    (double-buffered device inputs); the parameter copy of step i runs on a
+    third stream during step i+1's accumulate, and step i+1's update waits
+    for it."""
+    dev = W[0].device
+    Xs2, Gs2, _ = make_train_inputs(torch, dict(cfg, pool=2), shapes, lay, dev, seed=777,
                                     pool=2, sides=sides)
-    Xh = [[x.cpu().pin_memory() for x in xs] for xs in Xs2]
-    Gh = [[g.cpu().pin_memory() for g in gs] for gs in Gs2]
-    Wh = [w.cpu().pin_memory() for w in W]
+    Xh, Gh = [], []
+    for s2 in range(2):
+        hb, hv = _flat(torch, Xs2[s2], pin=True)
+        for v, x in zip(hv, Xs2[s2]):
+            v.copy_(x)
+        Xh.append(hb)
+        hb, hv = _flat(torch, Gs2[s2], pin=True)
+        for v, g in zip(hv, Gs2[s2]):
+            g_ = g
+            v.copy_(g_)
+        Gh.append(hb)
+    Xd = [_flat(torch, Xs2[0], device=dev) for _ in range(2)]
+    Gd = [_flat(torch, Gs2[0], device=dev) for _ in range(2)]
     del Xs2, Gs2
-    os.sched_setaffinity(0, prev_cpus)
+    Wd_buf, Wd = _flat(torch, W, device=dev)
+    for v, w in zip(Wd, W):
+        v.copy_(w)
+    Wh = torch.empty_like(Wd_buf, device="cpu").pin_memory()
     link = host_link_rates(torch)
-    Xd = [[torch.empty_like(x) for x in Xh[0]] for _ in range(2)]
-    Gd = [[torch.empty_like(g) for g in Gh[0]] for _ in range(2)]
-    nb = lambda ts: sum(t.numel() * t.element_size() for t in ts)
-    h2d = nb(Xh[0]) + nb(Gh[0])
-    d2h = nb(Wh)
+    h2d = Xh[0].numel() * Xh[0].element_size() + Gh[0].numel() * Gh[0].element_size()
+    d2h = Wh.numel() * Wh.element_size()
     cx, cg, cw = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
     x_done = [torch.cuda.Event() for _ in range(2)]
     g_done = [torch.cuda.Event() for _ in range(2)]
@@ -758,14 +766,13 @@ def run_e2e(torch, opt, cfg, shapes, lay, sides, W, K, stream, params, world):
     w_ready, w_out = torch.cuda.Event(), torch.cuda.Event()
 
     def issue(i):
-        b, src = i % 2, i % 2
-        for cs, dst, hs, used, done in ((cx, Xd[b], Xh[src], x_used[b], x_done[b]),
-                                        (cg, Gd[b], Gh[src], g_used[b], g_done[b])):
+        b = i % 2
+        for cs, dst, src, used, done in ((cx, Xd[b][0], Xh[b], x_used[b], x_done[b]),
+                                         (cg, Gd[b][0], Gh[b], g_used[b], g_done[b])):
             if i >= 2:
                 cs.wait_event(used)
             with torch.cuda.stream(cs):
-                for d_, h_ in zip(dst, hs):
-                    d_.copy_(h_, non_blocking=True)
+                dst.copy_(src, non_blocking=True)
             done.record(cs)
 
     torch.cuda.synchronize()
@@ -781,18 +788,17 @@ def run_e2e(torch, opt, cfg, shapes, lay, sides, W, K, stream, params, world):
     for i in range(K):
         b = i % 2
         stream.wait_event(x_done[b])
-        opt.accumulate(Xd[b])
+        opt.accumulate(Xd[b][1])
         x_used[b].record(stream)
         stream.wait_event(g_done[b])
         if i > 0:
             stream.wait_event(w_out)      # the previous step's parameters have left
-        opt.step(W, Gd[b], LR)
+        opt.step(Wd, Gd[b][1], LR)
         g_used[b].record(stream)
         w_ready.record(stream)
         cw.wait_event(w_ready)
         with torch.cuda.stream(cw):
-            for h_, d_ in zip(Wh, W):
-                h_.copy_(d_, non_blocking=True)
+            Wh.copy_(Wd_buf, non_blocking=True)
         w_out.record(cw)
         if i + 2 < K:
             issue(i + 2)
@@ -806,7 +812,7 @@ def run_e2e(torch, opt, cfg, shapes, lay, sides, W, K, stream, params, world):
             "host_link": link,
             "copy_floor_ms": max(h2d / (link["h2d_gbs"] * 1e9), d2h / (link["d2h_gbs"] * 1e9)) * 1e3,
             "overlap": "inputs of step i+1 copied on two streams during step i; parameters of "
-                       "step i copied back during step i+1's accumulate"}
+                       "step i copied back during step i+1's accumulate; one flat buffer per kind"}
 
 
 def _relaunch_distributed(args):

@@ -74,3 +74,43 @@ def test_moment_allreduce_equals_ema_of_averaged_moments():
     for rank, err, n_sync in res:
         assert n_sync == 3
         assert err < 1e-13
+
+
+def _placement_worker(rank, world, port, out_q):
+    import sys
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    from block_eigenbasis_preconditioning_gb300 import inputs as I
+    from block_eigenbasis_preconditioning_gb300.sharding import matrix_cost, partition_matrices
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    shapes = I.gpt2_xl_shapes().shapes
+    owned = partition_matrices(shapes, 16, world)
+    mine = torch.tensor(owned[rank] + [-1] * (len(shapes) - len(owned[rank])), dtype=torch.int64)
+    gathered = [torch.empty_like(mine) for _ in range(world)]
+    dist.all_gather(gathered, mine)
+    lists = [[int(v) for v in g.tolist() if v >= 0] for g in gathered]
+    cost = [sum(matrix_cost(*shapes[i], 16, 8192, 10) for i in lst) for lst in lists]
+    out_q.put((rank, lists == owned, sorted(sum(lists, [])) == list(range(len(shapes))),
+               max(cost) / min(cost)))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_matrix_placement_across_ranks():
+    """Two ranks compute the placement of the GPT-2 XL matrices on their own
+    and agree on it (exchanged with an all-gather); every matrix is owned by
+    exactly one rank and the estimated loads differ by less than 5 %."""
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_placement_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = [q.get(timeout=120) for _ in procs]
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for rank, same, cover, imbalance in res:
+        assert same and cover
+        assert imbalance < 1.05
