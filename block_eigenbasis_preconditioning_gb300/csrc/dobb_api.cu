@@ -67,7 +67,7 @@ int64_t pad16f(int64_t v) { return (v + 15) / 16 * 16; }
 // ones run one CTA per block), it is never used below kGjMinK, and a batch
 // holds as many blocks of one width as keep their scratch (3 k^2 floats)
 // within kGjL2Budget bytes of L2.
-constexpr int kGjDefaultMinK = 128;
+constexpr int kGjDefaultMinK = 64;
 constexpr int kGjMinK = 64;
 constexpr int64_t kGjDefaultBatchBytes = 0;   // 0: every block of one width in one batch
 

@@ -207,7 +207,7 @@ dobb_status dobb_set_refresh_period(dobb_handle h, int refresh_period);
  * Both run the same restarted Rayleigh-Ritz two-sided Jacobi.  0 = never the
  * grid solver; otherwise min_k >= 64.  A batch holds the blocks of one width
  * whose scratch (12 k^2 bytes each) fits `batch_bytes` (at least one block;
- * 0 = all blocks of that width).  Defaults: 128, 0.  DOBB_ERR_INVALID_ARG for
+ * 0 = all blocks of that width).  Defaults: 64, 0.  DOBB_ERR_INVALID_ARG for
  * other values. */
 dobb_status dobb_set_eig_grid(dobb_handle h, int min_k, int64_t batch_bytes);
 

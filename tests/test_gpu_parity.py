@@ -76,7 +76,7 @@ def test_moments_skip_null_and_flag_nonfinite():
 @pytest.mark.parametrize("solver", ["default", "one-cta"])
 @pytest.mark.parametrize("k", [1, 2, 3, 5, 16, 48, 64, 100, 128, 168, 169, 192, 400, 448])
 def test_refresh_on_spd_blocks_with_gaps(k, solver):
-    """Both eigensolvers (by default the grid solver for k >= 128 and one CTA
+    """Both eigensolvers (by default the grid solver for k >= 64 and one CTA
     per block below; "one-cta" forces the latter) on SPD blocks with gaps."""
     rng = np.random.default_rng(k)
     B = 2
