@@ -73,6 +73,7 @@ SIGNATURES = [
     ("dobb_sync_bases", _c.c_int, [_VP, _VP]),
     ("dobb_peak_probe", _c.c_int, [_c.c_int, _VP, _c.c_size_t, _c.c_int,
                                    _c.POINTER(_c.c_float), _c.POINTER(_c.c_double), _VP]),
+    ("dobb_selftest_wait_timeout", _c.c_int, [_c.POINTER(_c.c_uint32), _c.c_uint64, _VP]),
     ("dobb_eigh_noalloc", _c.c_int, [_VP, _VP, _VP, _c.c_int, _c.c_int, _c.c_int,
                                      _c.POINTER(_c.c_uint32), _VP]),
     ("dobb_eigh_noalloc_last_error", _c.c_char_p, []),

@@ -575,6 +575,7 @@ dobb_status do_step(dobb_handle h, void* const* W, const void* const* G, float l
         t.nastage = step_tc_astages(kmax);
         t.nbstage = step_tc_bstages(kmax, t.nastage, h->smem_limit);
         t.npieces = h->basis_bf16 ? 1 : 2;
+        t.rpieces = h->basis_bf16 ? 1 : 3;
         t.defer = ((kmax + 15) & ~15) <= 128 ? 1 : 0;
         if (t.nbstage < 2)
           return fail(DOBB_ERR_UNSUPPORTED, "block width %d leaves no room for operand stages", kmax);

@@ -48,7 +48,7 @@ struct TcArgs {
   int32_t npieces;         // basis operand pieces: 2 (fp32 basis: hi, lo) or 1 (bf16 basis)
   int32_t defer;           // 1: every block of the launch has kpN <= 128 (reconstructs deferred)
   int32_t nastage;         // momentum (A operand) stages (2 ... 4)
-  int32_t pad;
+  int32_t rpieces;         // reconstruct basis pieces: 3 (fp32 basis: bf16 hi, lo, lo2) or 1
 };
 
 // One unit of grouped work: matrix, block and two phase-specific indices.

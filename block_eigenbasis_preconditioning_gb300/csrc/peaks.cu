@@ -226,3 +226,29 @@ extern "C" dobb_status dobb_peak_probe(int which, void* scratch_dev, size_t scra
   *flops_out = flops;
   return DOBB_OK;
 }
+
+// ------------------------------------------------------------------
+// Failure-detection self-test: the bounded mbarrier wait every tensor-core
+// kernel of this library uses, on a barrier that nothing arrives on.  The
+// wait gives up after `timeout_ns`, the kernel records DOBB error code 0x100
+// in `err_dev` and returns; the context stays usable.
+namespace dobb {
+namespace {
+__global__ void wait_timeout_kernel(uint32_t* err, uint64_t timeout_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(&bar, 1);
+    ptx::fence_mbar_init();
+  }
+  __syncthreads();
+  const bool ok = ptx::mbar_wait(&bar, 0, timeout_ns);
+  if (!ok && threadIdx.x == 0) atomicOr(err, 0x100u);
+}
+}  // namespace
+}  // namespace dobb
+
+extern "C" dobb_status dobb_selftest_wait_timeout(uint32_t* err_dev, uint64_t timeout_ns, void* stream) {
+  if (!err_dev || timeout_ns == 0 || timeout_ns > 5000000000ull) return DOBB_ERR_INVALID_ARG;
+  dobb::wait_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(err_dev, timeout_ns);
+  return cudaGetLastError() == cudaSuccess ? DOBB_OK : DOBB_ERR_CUDA;
+}

@@ -12,8 +12,10 @@
 // Precision.  sign(C) is decided near |C| ~ 0, so C is formed at fp32-level
 // accuracy with the split-precision product M Q ~ Mh Qh + Mh Ql + Ml Qh
 // (h = TF32 rounding, l = remainder), relative error ~2^-21.  S is exactly
-// representable in bf16, so U needs only Q split in two bf16 pieces
-// (16 significant bits, relative error <= 2^-17).
+// representable in bf16, so U needs only Q split into bf16 pieces: three
+// (Q = Qh + Ql + Qll, 24 significant bits, representation error <= 2^-27 |Q|
+// per entry, i.e. |dU_ij| <= 2^-27 sum_l |Q_jl| <= 2^-27 sqrt(k)) for the fp32
+// basis, one (exact) for the bf16 basis.
 //
 // Warp roles (320 threads): warp 0 loads (TMA for M tiles, bulk copies for
 // the pre-packed Q operand images), warp 1 allocates TMEM and issues the
@@ -206,7 +208,7 @@ step_tc_kernel(const __grid_constant__ StepArgs a, const __grid_constant__ TcArg
         int64_t off = 0;
         for (int c0 = 0; c0 < kpN && !aborted(sh); c0 += kUCols) {
           const int nn = min(kUCols, kpN - c0);
-          const uint32_t bytes = (uint32_t)t.npieces * nn * 32u;
+          const uint32_t bytes = (uint32_t)t.rpieces * nn * 32u;
           for (int s = 0; s < kpN / 16; ++s) {
             if (!mbar_wait(&sh->b_empty[bs], bp ^ 1)) { raise(sh, t.err, 3); return; }
             mbar_arrive_expect_tx(&sh->b_full[bs], bytes);
@@ -276,9 +278,9 @@ step_tc_kernel(const __grid_constant__ StepArgs a, const __grid_constant__ TcArg
           tc_fence_after();
           if (lane == 0) {
             const uint32_t b_hi = smem_u32(b_buf + bs * t.bstage);
-            const uint32_t b_lo = b_hi + nn * 32;
-            mma_f16_ts(d, tmem + cb + 8 * s, smem_desc(b_hi, 16, 256, kSw32), idr, s == 0 ? 0u : 1u);
-            if (two) mma_f16_ts(d, tmem + cb + 8 * s, smem_desc(b_lo, 16, 256, kSw32), idr, 1u);
+            for (int p = 0; p < t.rpieces; ++p)
+              mma_f16_ts(d, tmem + cb + 8 * s, smem_desc(b_hi + p * nn * 32, 16, 256, kSw32), idr,
+                         (s == 0 && p == 0) ? 0u : 1u);
             tc_commit(&sh->b_empty[bs]);
           }
           __syncwarp();
@@ -596,11 +598,11 @@ step_tc_kernel(const __grid_constant__ StepArgs a, const __grid_constant__ TcArg
 //   project, K = l, N = j: per 8-wide K step s and piece (TF32 hi[, lo]),
 //     kpN rows of 32 bytes (row n holds Q[8s .. 8s+7][n]), 32-byte swizzle;
 //   reconstruct, K = j, N = l: per 128-wide output chunk, per 16-wide K step
-//     and piece (bf16 hi[, lo]), nn rows of 32 bytes (row n holds
+//     and piece (bf16 hi[, lo, lo2]), nn rows of 32 bytes (row n holds
 //     Q[c0 + n][16s .. 16s+15]), 32-byte swizzle.
 __global__ void __launch_bounds__(256)
 pack_bases_kernel(const float* Q, unsigned char* qpack, const MatInfo* info, const Tile* items,
-                  int num_items, int npieces) {
+                  int num_items, int npieces, int rpieces) {
   for (int w = blockIdx.x; w < num_items; w += gridDim.x) {
     const Tile tl = items[w];
     const MatInfo mi = info[tl.mat];
@@ -630,12 +632,18 @@ pack_bases_kernel(const float* Q, unsigned char* qpack, const MatInfo* info, con
       const int s = j / 16, jj = j % 16;
       const float q = (l < k && j < k) ? Qb[(int64_t)l * k + j] : 0.f;
       const __nv_bfloat16 h = __float2bfloat16_rn(q);
-      const int64_t cbase = (int64_t)c0 * (kpN / 16) * npieces * 32;  // chunks before: 128 rows each
-      unsigned char* sub = rimg + cbase + (int64_t)s * npieces * nn * 32;
+      const int64_t cbase = (int64_t)c0 * (kpN / 16) * rpieces * 32;  // chunks before: 128 rows each
+      unsigned char* sub = rimg + cbase + (int64_t)s * rpieces * nn * 32;
       const uint32_t off = ptx::swz_offset((uint32_t)(nrow * 32 + jj * 2), 1);
       *reinterpret_cast<__nv_bfloat16*>(sub + off) = h;
-      if (npieces == 2)
-        *reinterpret_cast<__nv_bfloat16*>(sub + nn * 32 + off) = __float2bfloat16_rn(q - __bfloat162float(h));
+      if (rpieces == 3) {
+        // q - h and q - h - l are exact in fp32 (bf16 pieces of an fp32 value)
+        const float r1 = q - __bfloat162float(h);
+        const __nv_bfloat16 l = __float2bfloat16_rn(r1);
+        *reinterpret_cast<__nv_bfloat16*>(sub + nn * 32 + off) = l;
+        *reinterpret_cast<__nv_bfloat16*>(sub + 2 * nn * 32 + off) =
+            __float2bfloat16_rn(r1 - __bfloat162float(l));
+      }
     }
   }
 }
@@ -644,7 +652,7 @@ pack_bases_kernel(const float* Q, unsigned char* qpack, const MatInfo* info, con
 
 size_t step_tc_bstage(int max_k) {
   const int kpN = (max_k + 15) & ~15;
-  return (size_t)std::max(2 * kpN * 32, 2 * kUCols * 32);
+  return (size_t)std::max(2 * kpN * 32, 3 * kUCols * 32);
 }
 
 size_t step_tc_smem(int max_k, int nastage, int nbstage) {
@@ -668,7 +676,8 @@ int step_tc_bstages(int max_k, int nastage, size_t smem_limit) {
 
 int64_t tc_block_image_bytes(int k) {
   const int kpN = (k + 15) & ~15, nsub = (k + 7) / 8;
-  int64_t bytes = (int64_t)nsub * 2 * kpN * 32 + (int64_t)kpN * kpN * 4;
+  // project: up to two TF32 pieces; reconstruct: up to three bf16 pieces
+  int64_t bytes = (int64_t)nsub * 2 * kpN * 32 + (int64_t)kpN * kpN * 6;
   return (bytes + 1023) / 1024 * 1024;
 }
 
@@ -703,7 +712,8 @@ cudaError_t launch_step_tc(const StepArgs& a, const TcArgs& t, int param_dtype, 
 cudaError_t launch_pack_bases(const float* Q, unsigned char* qpack, const MatInfo* info,
                               const Tile* items, int num_items, int npieces, int grid, cudaStream_t s) {
   if (num_items <= 0) return cudaSuccess;
-  pack_bases_kernel<<<grid, 256, 0, s>>>(Q, qpack, info, items, num_items, npieces);
+  pack_bases_kernel<<<grid, 256, 0, s>>>(Q, qpack, info, items, num_items, npieces,
+                                         npieces == 2 ? 3 : 1);
   return cudaGetLastError();
 }
 

@@ -287,6 +287,14 @@ dobb_status dobb_sync_bases(dobb_handle h, void* stream);
 dobb_status dobb_peak_probe(int which, void* scratch_dev, size_t scratch_bytes, int iters,
                             float* ms_out, double* flops_out, void* stream);
 
+/* Failure-detection self-test (the pages have no counterpart): one launch of
+ * the bounded mbarrier wait the tensor-core kernels use, on a barrier that
+ * nothing arrives on.  After timeout_ns (1 ns ... 5 s) the wait gives up, the
+ * kernel ORs 0x100 into *err_dev (device memory) and returns; asynchronous on
+ * `stream`.  DOBB_ERR_INVALID_ARG for a NULL pointer or a timeout out of
+ * range. */
+dobb_status dobb_selftest_wait_timeout(uint32_t* err_dev, uint64_t timeout_ns, void* stream);
+
 /* ------------------------------------------------------------------------
  * Allocation-free block eigendecomposition.
  *

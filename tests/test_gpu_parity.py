@@ -795,3 +795,32 @@ def test_sweep_cap_sets_not_converged_and_writes_a_basis():
     torch.cuda.synchronize()
     assert np.all(opt.block_flags() == 0)
     check_bases(opt, [A.astype(np.float32).astype(np.float64)])
+
+
+def test_bounded_wait_gives_up_and_the_context_stays_usable():
+    """The bounded mbarrier wait of the tensor-core kernels, on a barrier
+    nothing arrives on (a flag nothing sets): it gives up after its limit,
+    the error word carries 0x100, and the next optimizer step runs."""
+    import ctypes
+    import time
+    from block_eigenbasis_preconditioning_gb300 import binding
+    lib = binding.load_library()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    st = lib.dobb_selftest_wait_timeout(ctypes.cast(ctypes.c_void_p(err.data_ptr()),
+                                                    ctypes.POINTER(ctypes.c_uint32)),
+                                        ctypes.c_uint64(50_000_000), None)
+    assert st == 0
+    torch.cuda.synchronize()
+    dt = time.perf_counter() - t0
+    assert int(err.item()) == 0x100
+    assert 0.04 <= dt < 2.0
+    shapes = [(64, 256)]
+    Xs, Gs, Ws = make_problem(shapes, 512, 0.3, seed=43, param_dtype="bf16", act_dtype="bf16")
+    opt = _dobb(shapes, 2, refresh_period=1, param_dtype="bf16", act_dtype="bf16")
+    Wd = [to_dev(Ws[0], "bf16")]
+    opt.accumulate([to_dev(Xs[0], "bf16")])
+    opt.step(Wd, [to_dev(Gs[0], "bf16")], 0.02)
+    torch.cuda.synchronize()
+    assert opt.device_error() == 0 and np.all(opt.block_flags() == 0)
