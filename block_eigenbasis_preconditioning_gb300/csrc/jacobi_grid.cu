@@ -176,10 +176,28 @@ __global__ void gj_flip_kernel(const __grid_constant__ GjArgs a, int pred) {
 }
 
 // ----------------------------------------------------------------- sweeps
-// Tables of round br: one CTA (four warps, one team) per (table, item).
+// Tables of round br: one CTA of four warps per (table, item).  The table's
+// diagonal tile S (2g x 2g) and its rotation R live in shared memory.  Each
+// inner step rotates a set of disjoint column pairs ("slots", at most 32;
+// the first round's steps inside each group have a slot with a single member
+// when g is odd), computed by the first warp (lane = slot).  The
+// two-sided update S <- J^T S J is done block by block: for slots X <= Y the
+// 2 x 2 block of S on their members becomes G_X S_XY G_Y^T (G = [[c, -s],
+// [s, c]]) and is written to both (X, Y) and (Y, X), so every entry of S is
+// read once and written once per step and S stays exactly symmetric; R <- R J
+// updates two columns per slot (kept transposed, rows contiguous).  Two
+// barriers per step.
+constexpr int kLS = 65;             // row stride of S and R^T in shared memory
+constexpr int kMaxSlots = 32;
+constexpr int kBlockMap = kMaxSlots * (kMaxSlots + 1) / 2;
+
 __global__ void __launch_bounds__(kTableThreads) gj_table_kernel(const __grid_constant__ GjArgs a,
                                                                  int br) {
-  extern __shared__ __align__(16) float sm[];
+  __shared__ float S[64 * kLS];
+  __shared__ float Rt[64 * kLS];
+  __shared__ uint16_t bmap[kBlockMap];   // block u of the upper triangle -> (X, Y), ordered by Y
+  __shared__ int slot_p[kMaxSlots], slot_q[kMaxSlots];
+  __shared__ float slot_c[kMaxSlots], slot_s[kMaxSlots];
   const int item = blockIdx.y, tt = blockIdx.x;
   GjCtl* c = a.ctl + item;
   if (!pred_ok(*c, kActive)) return;
@@ -187,32 +205,135 @@ __global__ void __launch_bounds__(kTableThreads) gj_table_kernel(const __grid_co
   const Geo G = geo_for(k);
   if (br >= G.nG - 1 || tt >= G.nT) return;
   const ItemBufs b = bufs_of(a, item);
-  const int n2 = G.n2, nn = n2 * n2;
-  float* S = sm;
-  float* R = sm + nn;
+  const int n2 = G.n2, g = G.g, nn = n2 * n2;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   int gI, gJ;
   rr_pair(br, tt, G.nG, gI, gJ);
-  for (int e = threadIdx.x; e < nn; e += blockDim.x) {
+  for (int e = tid; e < nn; e += blockDim.x) {
     const int r = e / n2, q = e - r * n2;
-    const int cr = table_col(r, gI, gJ, G.g, k), cq = table_col(q, gI, gJ, G.g, k);
-    S[e] = (cr < k && cq < k) ? b.B[(int64_t)cr * k + cq] : 0.f;
-    R[e] = r == q ? 1.f : 0.f;
+    const int cr = table_col(r, gI, gJ, g, k), cq = table_col(q, gI, gJ, g, k);
+    S[r * kLS + q] = (cr < k && cq < k) ? b.B[(int64_t)cr * k + cq] : 0.f;
+    Rt[r * kLS + q] = r == q ? 1.f : 0.f;
+  }
+  for (int u = tid; u < kBlockMap; u += blockDim.x) {
+    int y = 0;
+    while ((y + 1) * (y + 2) / 2 <= u) ++y;
+    bmap[u] = (uint16_t)(((u - y * (y + 1) / 2) << 8) | y);
   }
   __syncthreads();
-  const int warp = threadIdx.x >> 5;
-  const int rots = solve_table(S, R, br, tt, G, k, c->bfloor, warp, kTableThreads / 32, 1);
-  __syncthreads();
+  const float bfloor = c->bfloor;
+  const int gp = g + (g & 1);
+  const int n_intra = br == 0 ? gp - 1 : 0;
+  int rots = 0;
+  for (int step = 0; step < n_intra + g; ++step) {
+    const bool intra = step < n_intra;
+    const int r = intra ? step : step - n_intra;
+    const int nslots = intra ? gp : g;
+    if (warp == 0) {
+      // slot `lane`: members p < q (q = -1: a single member), rotation (cs, sn)
+      int p = -1, q = -1;
+      float cs = 1.f, sn = 0.f;
+      if (lane < nslots) {
+        if (intra) {
+          const int half = gp >> 1, grp = lane / half, ii = lane - grp * half;
+          int pp, qq;
+          rr_pair(r, ii, gp, pp, qq);
+          if (pp >= g) pp = -1;
+          if (qq >= g) qq = -1;
+          if (pp < 0) { pp = qq; qq = -1; }
+          p = pp + grp * g;
+          q = qq < 0 ? -1 : qq + grp * g;
+        } else {
+          p = lane;
+          q = g + (lane + r) % g;
+        }
+        if (q >= 0 && q < p) {
+          const int t = p; p = q; q = t;
+        }
+        if (q >= 0 && table_col(p, gI, gJ, g, k) < k && table_col(q, gI, gJ, g, k) < k) {
+          const float bpq = S[p * kLS + q];
+          if (fabsf(bpq) > bfloor) {
+            const float ta = (S[q * kLS + q] - S[p * kLS + p]) / (2.f * bpq);
+            const float tn = ta >= 0.f ? 1.f / (ta + sqrtf(1.f + ta * ta)) : -1.f / (-ta + sqrtf(1.f + ta * ta));
+            cs = 1.f / sqrtf(1.f + tn * tn);
+            sn = tn * cs;
+            ++rots;
+          }
+        }
+        slot_p[lane] = p;
+        slot_q[lane] = q;
+        slot_c[lane] = cs;
+        slot_s[lane] = sn;
+      }
+    }
+    __syncthreads();
+    // S blocks (X <= Y)
+    const int nblk = nslots * (nslots + 1) / 2;
+    for (int u = tid; u < nblk; u += blockDim.x) {
+      const int X = bmap[u] >> 8, Y = bmap[u] & 0xFF;
+      const float sX = slot_s[X], sY = slot_s[Y];
+      if (sX == 0.f && sY == 0.f) continue;
+      const int pX = slot_p[X], qX = slot_q[X], pY = slot_p[Y], qY = slot_q[Y];
+      const float cX = slot_c[X], cY = slot_c[Y];
+      const bool hX = qX >= 0, hY = qY >= 0;
+      const float m00 = S[pX * kLS + pY];
+      const float m01 = hY ? S[pX * kLS + qY] : 0.f;
+      const float m10 = hX ? S[qX * kLS + pY] : 0.f;
+      const float m11 = (hX && hY) ? S[qX * kLS + qY] : 0.f;
+      // rows: G_X M
+      const float t00 = cX * m00 - sX * m10, t01 = cX * m01 - sX * m11;
+      const float t10 = sX * m00 + cX * m10, t11 = sX * m01 + cX * m11;
+      // columns: (G_X M) G_Y^T
+      const float n00 = cY * t00 - sY * t01, n01 = sY * t00 + cY * t01;
+      const float n10 = cY * t10 - sY * t11, n11 = sY * t10 + cY * t11;
+      if (X == Y) {
+        S[pX * kLS + pX] = n00;
+        if (hX) {
+          S[qX * kLS + qX] = n11;
+          S[pX * kLS + qX] = n01;
+          S[qX * kLS + pX] = n01;
+        }
+      } else {
+        S[pX * kLS + pY] = n00;
+        S[pY * kLS + pX] = n00;
+        if (hY) {
+          S[pX * kLS + qY] = n01;
+          S[qY * kLS + pX] = n01;
+        }
+        if (hX) {
+          S[qX * kLS + pY] = n10;
+          S[pY * kLS + qX] = n10;
+        }
+        if (hX && hY) {
+          S[qX * kLS + qY] = n11;
+          S[qY * kLS + qX] = n11;
+        }
+      }
+    }
+    // R <- R J: columns p, q of R = rows p, q of R^T
+    for (int u = tid; u < nslots * n2; u += blockDim.x) {
+      const int X = u / n2, j = u - X * n2;
+      const float sX = slot_s[X];
+      if (sX == 0.f) continue;
+      const int pX = slot_p[X], qX = slot_q[X];
+      const float cX = slot_c[X];
+      const float ra = Rt[pX * kLS + j], rb = Rt[qX * kLS + j];
+      Rt[pX * kLS + j] = cX * ra - sX * rb;
+      Rt[qX * kLS + j] = sX * ra + cX * rb;
+    }
+    __syncthreads();
+  }
   float* Rg = a.rbuf + (int64_t)item * a.rstride + (int64_t)tt * nn;
-  for (int e = threadIdx.x; e < nn; e += blockDim.x) {
+  for (int e = tid; e < nn; e += blockDim.x) {
     const int r = e / n2, q = e - r * n2;
-    const int cr = table_col(r, gI, gJ, G.g, k), cq = table_col(q, gI, gJ, G.g, k);
-    if (cr < k && cq < k) b.B[(int64_t)cr * k + cq] = S[e];
-    Rg[e] = R[e];
+    const int cr = table_col(r, gI, gJ, g, k), cq = table_col(q, gI, gJ, g, k);
+    if (cr < k && cq < k) b.B[(int64_t)cr * k + cq] = S[r * kLS + q];
+    Rg[e] = Rt[q * kLS + r];   // R[r][q]
   }
   int tot = rots;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
-  if ((threadIdx.x & 31) == 0 && tot) atomicAdd(&c->rot, tot);
+  if (lane == 0 && warp == 0 && tot) atomicAdd(&c->rot, tot);
 }
 
 // E = R - I of table t into a zero-padded 64 x kLdM tile.
@@ -254,10 +375,11 @@ __global__ void __launch_bounds__(kThreads) gj_apply_kernel(const __grid_constan
   const ItemBufs b = bufs_of(a, item);
   const int n2 = G.n2, nn = n2 * n2;
   const float* Rb = a.rbuf + (int64_t)item * a.rstride;
+  // three tiles: E_s (then Y^T and Z^T), E_t, X (then Z)
   float* Es = sm;
   float* Et = sm + kT * kLdM;
   float* Xs = sm + 2 * kT * kLdM;
-  float* Ys = sm + 3 * kT * kLdM;
+  float* Ys = Es;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
   float acc[4][4];
   if (u < npair) {
@@ -283,7 +405,8 @@ __global__ void __launch_bounds__(kThreads) gj_apply_kernel(const __grid_constan
     mma_load_acc<false>(Xs, acc);                     // X
     if (precise) corr_product<3>(Es, Xs, n2, acc);    // Y = X + E_s^T X
     else corr_product<1>(Es, Xs, n2, acc);
-    mma_store_acc<true>(Ys, acc);                     // Y^T
+    __syncthreads();                                  // E_s read by every warp
+    mma_store_acc<true>(Ys, acc);                     // Y^T over E_s
     __syncthreads();
     if (precise) corr_product<3>(Ys, Et, n2, acc);    // Z = Y + Y E_t
     else corr_product<1>(Ys, Et, n2, acc);
@@ -461,7 +584,7 @@ __global__ void __launch_bounds__(kThreads) gj_finish_kernel(const __grid_consta
   }
 }
 
-size_t apply_smem() { return 4 * (size_t)kT * kLdM * sizeof(float); }
+size_t apply_smem() { return 3 * (size_t)kT * kLdM * sizeof(float); }
 size_t gemm_smem() { return (size_t)kGemmFloats * sizeof(float); }
 
 }  // namespace
@@ -495,7 +618,7 @@ cudaError_t run_jacobi_grid(GjArgs a, int* host_count, cudaStream_t s, int64_t* 
   const int chunks = (int)std::max<int64_t>(1, std::min<int64_t>(256, (int64_t)k * k / (64 * 1024)));
   const dim3 cgrid(chunks, a.nitems);
   const int ctl_blocks = (a.nitems + 255) / 256;
-  const size_t gsm = gemm_smem(), asm_ = apply_smem(), tsm = 2 * (size_t)G.n2 * G.n2 * sizeof(float);
+  const size_t gsm = gemm_smem(), asm_ = apply_smem();
   int64_t n = 0;
   cudaError_t e = cudaMemsetAsync(a.ctl, 0, sizeof(GjCtl) * (size_t)a.nitems, s);
   if (e != cudaSuccess) return e;
@@ -506,7 +629,7 @@ cudaError_t run_jacobi_grid(GjArgs a, int* host_count, cudaStream_t s, int64_t* 
   n += 4;
   for (int sweep = 0; sweep < a.max_sweeps; ++sweep) {
     for (int br = 0; br < G.nG - 1; ++br) {
-      gj_table_kernel<<<dim3(G.nT, a.nitems), kTableThreads, tsm, s>>>(a, br);
+      gj_table_kernel<<<dim3(G.nT, a.nitems), kTableThreads, 0, s>>>(a, br);
       gj_apply_kernel<<<dim3(npair + G.nT * nI, a.nitems), kThreads, asm_, s>>>(a, br);
       n += 2;
     }

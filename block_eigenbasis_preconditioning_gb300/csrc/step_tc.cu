@@ -665,7 +665,7 @@ int step_tc_astages(int max_k) { (void)max_k; return 2; }
 // Basis stages a launch uses at most.  Shared memory left unused stays L1
 // cache, which the per-row gradient and parameter accesses of the converter
 // and epilogue warps rely on.
-static int step_tc_bstage_cap(int max_k) { return max_k <= 128 ? 12 : 6; }
+static int step_tc_bstage_cap(int max_k) { return max_k <= 128 ? 8 : 6; }
 
 int step_tc_bstages(int max_k, int nastage, size_t smem_limit) {
   const size_t fixed = step_tc_smem(max_k, nastage, 0);
