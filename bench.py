@@ -339,15 +339,16 @@ def _kernel_source_sha(name):
 
 
 def _traffic_for(kernel_key, workload):
-    """DRAM bytes per launch of that kernel from a committed ncu summary, if it
-    was taken on the current source of the kernel and on this workload."""
+    """DRAM bytes per unit of work of that kernel (a launch, or for the
+    eigensolver one refresh) from a committed ncu summary, if it was taken on
+    the current sources of the kernel and on this workload."""
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             t = json.load(f)
         e = t.get(kernel_key)
-        if e and e.get("source_sha") == _kernel_source_sha(e.get("source")) and \
-                e.get("workload") == workload:
-            return e.get("bytes_per_launch")
+        if e and e.get("workload") == workload and all(
+                sha == _kernel_source_sha(src) for src, sha in e.get("sources", {}).items()):
+            return e.get("bytes_per_unit")
     except Exception:
         pass
     return None
@@ -642,7 +643,9 @@ def run_gpu(args):
                        "peak": hbm, "peak_source": mp["source"], "unit": "GB/s",
                        "flops": wm["acc_flops"], "bytes": wm["acc_bytes"]},
         "refresh": {"ms": refresh_ms, "cold_ms": cold_ms,
-                    "kernel": "jacobi_kernel" if args.refresh == "eigh" else "orth_kernel",
+                    "kernel": ("grid eigensolver (gj_* kernels)" if args.refresh == "eigh"
+                               else "orth_kernel"),
+                    "unit_of_work": "one refresh of every block (all its launches)",
                     "bound": "alu", "achieved": wm["refresh_flops"] / (refresh_ms * 1e-3) / 1e12,
                     "peak": ffma_peak, "peak_source": ffma_src, "unit": "TFLOP/s",
                     "flops": wm["refresh_flops"]},

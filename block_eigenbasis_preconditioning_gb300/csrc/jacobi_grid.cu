@@ -189,13 +189,11 @@ __global__ void gj_flip_kernel(const __grid_constant__ GjArgs a, int pred) {
 // barriers per step.
 constexpr int kLS = 65;             // row stride of S and R^T in shared memory
 constexpr int kMaxSlots = 32;
-constexpr int kBlockMap = kMaxSlots * (kMaxSlots + 1) / 2;
 
 __global__ void __launch_bounds__(kTableThreads) gj_table_kernel(const __grid_constant__ GjArgs a,
                                                                  int br) {
   __shared__ float S[64 * kLS];
   __shared__ float Rt[64 * kLS];
-  __shared__ uint16_t bmap[kBlockMap];   // block u of the upper triangle -> (X, Y), ordered by Y
   __shared__ int slot_p[kMaxSlots], slot_q[kMaxSlots];
   __shared__ float slot_c[kMaxSlots], slot_s[kMaxSlots];
   const int item = blockIdx.y, tt = blockIdx.x;
@@ -214,11 +212,6 @@ __global__ void __launch_bounds__(kTableThreads) gj_table_kernel(const __grid_co
     const int cr = table_col(r, gI, gJ, g, k), cq = table_col(q, gI, gJ, g, k);
     S[r * kLS + q] = (cr < k && cq < k) ? b.B[(int64_t)cr * k + cq] : 0.f;
     Rt[r * kLS + q] = r == q ? 1.f : 0.f;
-  }
-  for (int u = tid; u < kBlockMap; u += blockDim.x) {
-    int y = 0;
-    while ((y + 1) * (y + 2) / 2 <= u) ++y;
-    bmap[u] = (uint16_t)(((u - y * (y + 1) / 2) << 8) | y);
   }
   __syncthreads();
   const float bfloor = c->bfloor;
@@ -267,11 +260,14 @@ __global__ void __launch_bounds__(kTableThreads) gj_table_kernel(const __grid_co
       }
     }
     __syncthreads();
-    // S blocks (X <= Y)
-    const int nblk = nslots * (nslots + 1) / 2;
-    for (int u = tid; u < nblk; u += blockDim.x) {
-      const int X = bmap[u] >> 8, Y = bmap[u] & 0xFF;
-      const float sX = slot_s[X], sY = slot_s[Y];
+    // S blocks (X <= Y): warp w takes the block rows X = w, w + 4, ...,
+    // lane Y the blocks (X, Y) with Y >= X; reads along the rows of slot X
+    // and mirrored writes (row stride 65) fall in distinct banks
+    for (int X = warp; X < nslots; X += kTableThreads / 32) {
+      const int Y = lane;
+      const float sX = slot_s[X];
+      if (Y < X || Y >= nslots) continue;
+      const float sY = slot_s[Y];
       if (sX == 0.f && sY == 0.f) continue;
       const int pX = slot_p[X], qX = slot_q[X], pY = slot_p[Y], qY = slot_q[Y];
       const float cX = slot_c[X], cY = slot_c[Y];
@@ -310,16 +306,18 @@ __global__ void __launch_bounds__(kTableThreads) gj_table_kernel(const __grid_co
         }
       }
     }
-    // R <- R J: columns p, q of R = rows p, q of R^T
-    for (int u = tid; u < nslots * n2; u += blockDim.x) {
-      const int X = u / n2, j = u - X * n2;
+    // R <- R J: columns p, q of R = rows p, q of R^T; warp per slot, lanes
+    // along the row
+    for (int X = warp; X < nslots; X += kTableThreads / 32) {
       const float sX = slot_s[X];
       if (sX == 0.f) continue;
       const int pX = slot_p[X], qX = slot_q[X];
       const float cX = slot_c[X];
-      const float ra = Rt[pX * kLS + j], rb = Rt[qX * kLS + j];
-      Rt[pX * kLS + j] = cX * ra - sX * rb;
-      Rt[qX * kLS + j] = sX * ra + cX * rb;
+      for (int j = lane; j < n2; j += 32) {
+        const float ra = Rt[pX * kLS + j], rb = Rt[qX * kLS + j];
+        Rt[pX * kLS + j] = cX * ra - sX * rb;
+        Rt[qX * kLS + j] = sX * ra + cX * rb;
+      }
     }
     __syncthreads();
   }
@@ -338,9 +336,18 @@ __global__ void __launch_bounds__(kTableThreads) gj_table_kernel(const __grid_co
 
 // E = R - I of table t into a zero-padded 64 x kLdM tile.
 __device__ __forceinline__ void load_corr(float* dst, const float* src, int n2) {
-  for (int e = threadIdx.x; e < kT * kT; e += blockDim.x) {
+  constexpr int kPer = kT * kT / kThreads;
+  float v[kPer];
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int e = threadIdx.x + i * kThreads;
     const int r = e / kT, q = e - r * kT;
-    dst[r * kLdM + q] = (r < n2 && q < n2) ? src[r * n2 + q] - (r == q ? 1.f : 0.f) : 0.f;
+    v[i] = (r < n2 && q < n2) ? src[r * n2 + q] - (r == q ? 1.f : 0.f) : 0.f;
+  }
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int e = threadIdx.x + i * kThreads;
+    dst[(e / kT) * kLdM + (e % kT)] = v[i];
   }
 }
 
@@ -393,13 +400,24 @@ __global__ void __launch_bounds__(kThreads) gj_apply_kernel(const __grid_constan
     int sI, sJ, tI, tJ;
     rr_pair(br, s, G.nG, sI, sJ);
     rr_pair(br, t, G.nG, tI, tJ);
-    load_corr(Es, Rb + (int64_t)s * nn, n2);
-    load_corr(Et, Rb + (int64_t)t * nn, n2);
-    for (int e = tid; e < kT * kT; e += blockDim.x) {
-      const int r = e / kT, q = e - r * kT;
-      const int cr = r < n2 ? table_col(r, sI, sJ, G.g, k) : k;
-      const int cq = q < n2 ? table_col(q, tI, tJ, G.g, k) : k;
-      Xs[r * kLdM + q] = (cr < k && cq < k) ? b.B[(int64_t)cr * k + cq] : 0.f;
+    {
+      constexpr int kPer = kT * kT / kThreads;
+      float v[kPer];
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) {
+        const int e = tid + i * kThreads;
+        const int r = e / kT, q = e - r * kT;
+        const int cr = r < n2 ? table_col(r, sI, sJ, G.g, k) : k;
+        const int cq = q < n2 ? table_col(q, tI, tJ, G.g, k) : k;
+        v[i] = (cr < k && cq < k) ? b.B[(int64_t)cr * k + cq] : 0.f;
+      }
+      load_corr(Es, Rb + (int64_t)s * nn, n2);
+      load_corr(Et, Rb + (int64_t)t * nn, n2);
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) {
+        const int e = tid + i * kThreads;
+        Xs[(e / kT) * kLdM + (e % kT)] = v[i];
+      }
     }
     __syncthreads();
     mma_load_acc<false>(Xs, acc);                     // X
@@ -427,11 +445,22 @@ __global__ void __launch_bounds__(kThreads) gj_apply_kernel(const __grid_constan
     const int t = v / nI, i0 = (v - t * nI) * kT;
     int tI, tJ;
     rr_pair(br, t, G.nG, tI, tJ);
-    load_corr(Et, Rb + (int64_t)t * nn, n2);
-    for (int e = tid; e < kT * kT; e += blockDim.x) {
-      const int r = e / kT, i = e - r * kT;
-      const int cr = r < n2 ? table_col(r, tI, tJ, G.g, k) : k;
-      Xs[r * kLdM + i] = (cr < k && i0 + i < k) ? b.V[(int64_t)cr * k + i0 + i] : 0.f;
+    {
+      constexpr int kPer = kT * kT / kThreads;
+      float v[kPer];
+#pragma unroll
+      for (int ii = 0; ii < kPer; ++ii) {
+        const int e = tid + ii * kThreads;
+        const int r = e / kT, i = e - r * kT;
+        const int cr = r < n2 ? table_col(r, tI, tJ, G.g, k) : k;
+        v[ii] = (cr < k && i0 + i < k) ? b.V[(int64_t)cr * k + i0 + i] : 0.f;
+      }
+      load_corr(Et, Rb + (int64_t)t * nn, n2);
+#pragma unroll
+      for (int ii = 0; ii < kPer; ++ii) {
+        const int e = tid + ii * kThreads;
+        Xs[(e / kT) * kLdM + (e % kT)] = v[ii];
+      }
     }
     __syncthreads();
     mma_load_acc<true>(Xs, acc);                      // V rows i, table columns q
