@@ -330,14 +330,15 @@ Layout compute_layout(int num, const int64_t* m, const int64_t* n, int B, size_t
       if (it == count.end()) count.push_back({k, (size_t)B});
       else it->second += B;
     }
+    // every width's blocks may be in flight at once (concurrent batches)
     for (auto& c : count) {
-      L.gj_rbuf_floats = std::max(L.gj_rbuf_floats, c.second * (size_t)gj_rbuf_floats(c.first));
-      L.gj_ctl_items = std::max(L.gj_ctl_items, c.second);
+      L.gj_rbuf_floats += c.second * (size_t)gj_rbuf_floats(c.first);
+      L.gj_ctl_items += c.second;
     }
   }
   L.off_gj_rbuf = off;  off = align_up(off + 4 * L.gj_rbuf_floats);
   L.off_gj_ctl = off;   off = align_up(off + sizeof(GjCtl) * L.gj_ctl_items);
-  L.off_gj_count = off; off = align_up(off + 4);
+  L.off_gj_count = off; off = align_up(off + 4 * kGjMaxBatches);
   L.total = off;
   L.n_tiles = n_tiles;
   return L;
@@ -370,7 +371,15 @@ struct dobb_ctx {
   int path = 0;            // 0: tensor-core kernel where eligible, 1: FFMA only
   int gj_min_k = kGjDefaultMinK;  // blocks at least this wide use the grid eigensolver
   int64_t gj_batch_bytes = kGjDefaultBatchBytes;
-  int gj_host_count = 0;
+  int gj_host_counts[kGjMaxBatches] = {};
+  cudaStream_t gj_streams[kGjStreams] = {};   // the grid eigensolver's own streams
+  cudaEvent_t gj_events[kGjStreams + 1] = {};
+  ~dobb_ctx() {
+    for (int i = 0; i < kGjStreams; ++i)
+      if (gj_streams[i]) cudaStreamDestroy(gj_streams[i]);
+    for (int i = 0; i <= kGjStreams; ++i)
+      if (gj_events[i]) cudaEventDestroy(gj_events[i]);
+  }
   // cached X tensor maps (pointer and token count they were encoded for)
   std::vector<CUtensorMap> xmaps;
   std::vector<const void*> xmap_ptr;
@@ -441,6 +450,29 @@ dobb_status do_refresh_orth(dobb_handle h, cudaStream_t s) {
   return do_pack(h, s);
 }
 
+// Run grid-eigensolver batches: batch i on the caller's stream (i % 3 == 0)
+// or one of the handle's two streams, joined back into the caller's stream.
+cudaError_t run_grid_batches(dobb_handle h, const GjArgs* batches, int nb, cudaStream_t s) {
+  if (nb <= 0) return cudaSuccess;
+  cudaStream_t streams[kGjMaxBatches];
+  const int nstreams = std::min(nb, kGjStreams + 1);
+  for (int b = 0; b < nb; ++b) streams[b] = (b % nstreams) == 0 ? s : h->gj_streams[b % nstreams - 1];
+  cudaError_t e = cudaSuccess;
+  if (nstreams > 1) {
+    e = cudaEventRecord(h->gj_events[0], s);
+    for (int i = 1; i < nstreams && e == cudaSuccess; ++i)
+      e = cudaStreamWaitEvent(h->gj_streams[i - 1], h->gj_events[0], 0);
+    if (e != cudaSuccess) return e;
+  }
+  e = run_jacobi_grid(batches, nb, streams, h->gj_host_counts, &h->launches);
+  for (int i = 1; i < nstreams; ++i) {
+    cudaError_t e2 = cudaEventRecord(h->gj_events[i], h->gj_streams[i - 1]);
+    if (e2 == cudaSuccess) e2 = cudaStreamWaitEvent(s, h->gj_events[i], 0);
+    if (e == cudaSuccess) e = e2;
+  }
+  return e;
+}
+
 dobb_status do_refresh(dobb_handle h, cudaStream_t s) {
   if (h->refresh_method == DOBB_REFRESH_ORTH) return do_refresh_orth(h, s);
   // blocks whose solver fits in half of an SM's shared memory run two CTAs per SM
@@ -452,35 +484,56 @@ dobb_status do_refresh(dobb_handle h, cudaStream_t s) {
     auto kof = [&](int idx) { return (int)(h->n[items[idx].mat] / h->B); };
     int g0 = 0;
     if (h->gj_min_k > 0) {
+      // batches: runs of one width, split by the byte budget, or in two when
+      // no budget is set and the width has many blocks (two batches of one
+      // width interleave their table solves and tile products)
+      GjArgs batches[kGjMaxBatches];
+      int nb = 0;
+      int64_t ctl_off = 0, rbuf_off = 0;
       while (g0 < ch.eig_n && kof(g0) >= h->gj_min_k) {
-        // a batch: a run of equal width within the L2 budget
         const int k = kof(g0);
         int g1 = g0;
-        const int cap = std::min<int>(gj_batch_items(k, h->gj_batch_bytes), (int)h->L.gj_ctl_items);
-        while (g1 < ch.eig_n && kof(g1) == k && g1 - g0 < cap) ++g1;
-        if ((size_t)(g1 - g0) * (size_t)gj_rbuf_floats(k) > h->L.gj_rbuf_floats || g1 == g0)
-          return fail(DOBB_ERR_STATE, "grid eigensolver buffers too small for width %d", k);
-        GjArgs ga{};
-        ga.info = h->dinfo();
-        ga.items = h->dtiles() + ch.eig_off + g0;
-        ga.nitems = g1 - g0;
-        ga.k = k;
-        ga.A = h->A();
-        ga.Q = h->Q();
-        ga.lam = h->lam();
-        ga.scratch = h->scratch();
-        ga.rbuf = h->gj_rbuf();
-        ga.rstride = gj_rbuf_floats(k);
-        ga.ctl = h->gj_ctl();
-        ga.active_count = h->gj_count();
-        ga.flags = h->flags();
-        ga.stats = h->stats();
-        ga.max_sweeps = h->max_sweeps;
-        ga.tol = h->tol;
-        cudaError_t e = run_jacobi_grid(ga, &h->gj_host_count, s, &h->launches);
-        if (e != cudaSuccess) return fail(DOBB_ERR_CUDA, "grid eigensolver: %s", cudaGetErrorString(e));
+        while (g1 < ch.eig_n && kof(g1) == k) ++g1;
+        const int count = g1 - g0;
+        int per = std::min(count, gj_batch_items(k, h->gj_batch_bytes));
+        if (h->gj_batch_bytes == 0 && count >= 64) per = (count + 1) / 2;
+        for (int b0 = g0; b0 < g1; b0 += per) {
+          const int nitems = std::min(per, g1 - b0);
+          if (nb == kGjMaxBatches) {
+            cudaError_t e = run_grid_batches(h, batches, nb, s);
+            if (e != cudaSuccess) return fail(DOBB_ERR_CUDA, "grid eigensolver: %s", cudaGetErrorString(e));
+            nb = 0;
+            ctl_off = rbuf_off = 0;
+          }
+          if ((size_t)(ctl_off + nitems) > h->L.gj_ctl_items ||
+              (size_t)(rbuf_off + (int64_t)nitems * gj_rbuf_floats(k)) > h->L.gj_rbuf_floats)
+            return fail(DOBB_ERR_STATE, "grid eigensolver buffers too small for width %d", k);
+          GjArgs& ga = batches[nb];
+          ga = GjArgs{};
+          ga.info = h->dinfo();
+          ga.items = h->dtiles() + ch.eig_off + b0;
+          ga.nitems = nitems;
+          ga.k = k;
+          ga.A = h->A();
+          ga.Q = h->Q();
+          ga.lam = h->lam();
+          ga.scratch = h->scratch();
+          ga.rbuf = h->gj_rbuf() + rbuf_off;
+          ga.rstride = gj_rbuf_floats(k);
+          ga.ctl = h->gj_ctl() + ctl_off;
+          ga.active_count = h->gj_count() + nb;
+          ga.flags = h->flags();
+          ga.stats = h->stats();
+          ga.max_sweeps = h->max_sweeps;
+          ga.tol = h->tol;
+          ctl_off += nitems;
+          rbuf_off += (int64_t)nitems * gj_rbuf_floats(k);
+          ++nb;
+        }
         g0 = g1;
       }
+      cudaError_t e = run_grid_batches(h, batches, nb, s);
+      if (e != cudaSuccess) return fail(DOBB_ERR_CUDA, "grid eigensolver: %s", cudaGetErrorString(e));
     }
     int b = g0;
     while (b < ch.eig_n && jacobi_smem_for(kof(b), half) == 0) ++b;
@@ -696,6 +749,15 @@ dobb_status dobb_create(dobb_handle* out, int num_matrices, const int64_t* m, co
       (e = configure_syrk_tc(h->smem_limit)) != cudaSuccess) {
     delete h;
     return fail(DOBB_ERR_CUDA, "kernel configuration: %s", cudaGetErrorString(e));
+  }
+
+  for (int i = 0; i < kGjStreams && e == cudaSuccess; ++i)
+    e = cudaStreamCreateWithFlags(&h->gj_streams[i], cudaStreamNonBlocking);
+  for (int i = 0; i <= kGjStreams && e == cudaSuccess; ++i)
+    e = cudaEventCreateWithFlags(&h->gj_events[i], cudaEventDisableTiming);
+  if (e != cudaSuccess) {
+    delete h;
+    return fail(DOBB_ERR_CUDA, "stream creation: %s", cudaGetErrorString(e));
   }
 
   // per-matrix metadata

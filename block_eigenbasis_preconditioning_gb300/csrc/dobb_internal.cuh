@@ -144,11 +144,18 @@ struct GjArgs {
   float tol;
 };
 
+// batches of the grid eigensolver that run at once (interleaved, on their own streams)
+constexpr int kGjMaxBatches = 16;
+// streams the grid eigensolver uses besides the caller's
+constexpr int kGjStreams = 2;
+
 int64_t gj_rbuf_floats(int k);
 size_t gj_finish_smem(int k);
 cudaError_t configure_jacobi_grid(size_t smem_limit);
-// the whole refresh of one batch; synchronises the stream once per sweep
-cudaError_t run_jacobi_grid(GjArgs a, int* host_count, cudaStream_t s, int64_t* launches);
+// the whole refresh of nb batches (batch b on streams[b]); synchronises the
+// streams once per sweep
+cudaError_t run_jacobi_grid(const GjArgs* batches, int nb, const cudaStream_t* streams,
+                            int* host_counts, int64_t* launches);
 
 // Coefficient normalisation of the FP32 update kernel.
 constexpr int32_t kModeSign = 0;

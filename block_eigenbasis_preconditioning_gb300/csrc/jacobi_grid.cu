@@ -634,56 +634,95 @@ cudaError_t configure_jacobi_grid(size_t smem_limit) {
   return e;
 }
 
-// The whole refresh of one batch (blocks of one width k).  Synchronises the
-// stream once per sweep (to read how many blocks still iterate).
-cudaError_t run_jacobi_grid(GjArgs a, int* host_count, cudaStream_t s, int64_t* launches) {
-  if (a.nitems <= 0) return cudaSuccess;
-  const int k = a.k;
-  const Geo G = geo_for(k);
-  const int nt = (k + kT - 1) / kT;
-  const int nI = nt;
-  const int npair = G.nT * (G.nT - 1) / 2;
-  const dim3 tiles(nt * nt, a.nitems);
-  const int chunks = (int)std::max<int64_t>(1, std::min<int64_t>(256, (int64_t)k * k / (64 * 1024)));
-  const dim3 cgrid(chunks, a.nitems);
-  const int ctl_blocks = (a.nitems + 255) / 256;
+// The whole refresh of nb batches (each: blocks of one width), batch b on
+// streams[b]: the launches of all batches are interleaved round by round, so
+// the table solves of one batch (latency-bound) overlap the tile products of
+// another (memory- and tensor-bound).  Synchronises the streams once per
+// sweep (to read how many blocks still iterate in each batch).
+cudaError_t run_jacobi_grid(const GjArgs* batches, int nb, const cudaStream_t* streams,
+                            int* host_counts, int64_t* launches) {
+  struct Geom {
+    Geo G;
+    int nt, npair, ctl_blocks;
+    dim3 tiles, cgrid;
+  };
+  Geom gm[kGjMaxBatches];
+  if (nb <= 0) return cudaSuccess;
+  if (nb > kGjMaxBatches) return cudaErrorInvalidValue;
   const size_t gsm = gemm_smem(), asm_ = apply_smem();
   int64_t n = 0;
-  cudaError_t e = cudaMemsetAsync(a.ctl, 0, sizeof(GjCtl) * (size_t)a.nitems, s);
-  if (e != cudaSuccess) return e;
-  gj_init_kernel<<<cgrid, kThreads, 0, s>>>(a);
-  gj_start_kernel<<<ctl_blocks, 256, 0, s>>>(a);
-  gj_gemm_kernel<<<tiles, kThreads, gsm, s>>>(a, kRR1, kActive);
-  gj_gemm_kernel<<<tiles, kThreads, gsm, s>>>(a, kRR2, kActive);
-  n += 4;
-  for (int sweep = 0; sweep < a.max_sweeps; ++sweep) {
-    for (int br = 0; br < G.nG - 1; ++br) {
-      gj_table_kernel<<<dim3(G.nT, a.nitems), kTableThreads, 0, s>>>(a, br);
-      gj_apply_kernel<<<dim3(npair + G.nT * nI, a.nitems), kThreads, asm_, s>>>(a, br);
-      n += 2;
-    }
-    e = cudaMemsetAsync(a.active_count, 0, sizeof(int), s);
+  int max_rounds = 0;
+  for (int b = 0; b < nb; ++b) {
+    const GjArgs& a = batches[b];
+    Geom& m = gm[b];
+    m.G = geo_for(a.k);
+    m.nt = (a.k + kT - 1) / kT;
+    m.npair = m.G.nT * (m.G.nT - 1) / 2;
+    m.ctl_blocks = (a.nitems + 255) / 256;
+    m.tiles = dim3(m.nt * m.nt, a.nitems);
+    const int chunks = (int)std::max<int64_t>(1, std::min<int64_t>(256, (int64_t)a.k * a.k / (64 * 1024)));
+    m.cgrid = dim3(chunks, a.nitems);
+    max_rounds = std::max(max_rounds, m.G.nG - 1);
+    const cudaStream_t s = streams[b];
+    cudaError_t e = cudaMemsetAsync(a.ctl, 0, sizeof(GjCtl) * (size_t)a.nitems, s);
     if (e != cudaSuccess) return e;
-    gj_off_kernel<<<cgrid, kThreads, 0, s>>>(a);
-    gj_control_kernel<<<ctl_blocks, 256, 0, s>>>(a);
-    // restart: Newton-Schulz (E into B, V' into W, swap), then RR
-    gj_gemm_kernel<<<tiles, kThreads, gsm, s>>>(a, kNS1, kRestart);
-    gj_gemm_kernel<<<tiles, kThreads, gsm, s>>>(a, kNS2, kRestart);
-    gj_flip_kernel<<<ctl_blocks, 256, 0, s>>>(a, kRestart);
-    gj_gemm_kernel<<<tiles, kThreads, gsm, s>>>(a, kRR1, kRestart);
-    gj_gemm_kernel<<<tiles, kThreads, gsm, s>>>(a, kRR2, kRestart);
-    n += 7;
-    e = cudaMemcpyAsync(host_count, a.active_count, sizeof(int), cudaMemcpyDeviceToHost, s);
-    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
-    if (e != cudaSuccess) return e;
-    if (*host_count == 0) break;
+    gj_init_kernel<<<m.cgrid, kThreads, 0, s>>>(a);
+    gj_start_kernel<<<m.ctl_blocks, 256, 0, s>>>(a);
+    gj_gemm_kernel<<<m.tiles, kThreads, gsm, s>>>(a, kRR1, kActive);
+    gj_gemm_kernel<<<m.tiles, kThreads, gsm, s>>>(a, kRR2, kActive);
+    n += 4;
+    host_counts[b] = a.nitems;
   }
-  gj_diag_kernel<<<dim3((k + 255) / 256, a.nitems), 256, 0, s>>>(a);
-  gj_gemm_kernel<<<tiles, kThreads, gsm, s>>>(a, kNS1, kAlways);
-  gj_gemm_kernel<<<tiles, kThreads, gsm, s>>>(a, kNS2, kAlways);
-  gj_flip_kernel<<<ctl_blocks, 256, 0, s>>>(a, kAlways);
-  gj_finish_kernel<<<a.nitems, kThreads, gj_finish_smem(k), s>>>(a);
-  n += 5;
+  const int max_sweeps = batches[0].max_sweeps;
+  for (int sweep = 0; sweep < max_sweeps; ++sweep) {
+    for (int br = 0; br < max_rounds; ++br) {
+      for (int b = 0; b < nb; ++b) {
+        const GjArgs& a = batches[b];
+        const Geom& m = gm[b];
+        if (host_counts[b] == 0 || br >= m.G.nG - 1) continue;
+        gj_table_kernel<<<dim3(m.G.nT, a.nitems), kTableThreads, 0, streams[b]>>>(a, br);
+        gj_apply_kernel<<<dim3(m.npair + m.G.nT * m.nt, a.nitems), kThreads, asm_, streams[b]>>>(a, br);
+        n += 2;
+      }
+    }
+    for (int b = 0; b < nb; ++b) {
+      const GjArgs& a = batches[b];
+      const Geom& m = gm[b];
+      if (host_counts[b] == 0) continue;
+      const cudaStream_t s = streams[b];
+      cudaError_t e = cudaMemsetAsync(a.active_count, 0, sizeof(int), s);
+      if (e != cudaSuccess) return e;
+      gj_off_kernel<<<m.cgrid, kThreads, 0, s>>>(a);
+      gj_control_kernel<<<m.ctl_blocks, 256, 0, s>>>(a);
+      // restart: Newton-Schulz (E into B, V' into W, swap), then RR
+      gj_gemm_kernel<<<m.tiles, kThreads, gsm, s>>>(a, kNS1, kRestart);
+      gj_gemm_kernel<<<m.tiles, kThreads, gsm, s>>>(a, kNS2, kRestart);
+      gj_flip_kernel<<<m.ctl_blocks, 256, 0, s>>>(a, kRestart);
+      gj_gemm_kernel<<<m.tiles, kThreads, gsm, s>>>(a, kRR1, kRestart);
+      gj_gemm_kernel<<<m.tiles, kThreads, gsm, s>>>(a, kRR2, kRestart);
+      n += 7;
+      e = cudaMemcpyAsync(host_counts + b, a.active_count, sizeof(int), cudaMemcpyDeviceToHost, s);
+      if (e != cudaSuccess) return e;
+    }
+    bool any = false;
+    for (int b = 0; b < nb; ++b) {
+      cudaError_t e = cudaStreamSynchronize(streams[b]);
+      if (e != cudaSuccess) return e;
+    }
+    for (int b = 0; b < nb; ++b) any = any || host_counts[b] != 0;
+    if (!any) break;
+  }
+  for (int b = 0; b < nb; ++b) {
+    const GjArgs& a = batches[b];
+    const Geom& m = gm[b];
+    const cudaStream_t s = streams[b];
+    gj_diag_kernel<<<dim3((a.k + 255) / 256, a.nitems), 256, 0, s>>>(a);
+    gj_gemm_kernel<<<m.tiles, kThreads, gsm, s>>>(a, kNS1, kAlways);
+    gj_gemm_kernel<<<m.tiles, kThreads, gsm, s>>>(a, kNS2, kAlways);
+    gj_flip_kernel<<<m.ctl_blocks, 256, 0, s>>>(a, kAlways);
+    gj_finish_kernel<<<a.nitems, kThreads, gj_finish_smem(a.k), s>>>(a);
+    n += 5;
+  }
   if (launches) *launches += n;
   return cudaGetLastError();
 }
