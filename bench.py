@@ -439,8 +439,8 @@ def workload_name(cfg_name, cfg, n_matrices, params, layers):
             "llama3-8b": "llama3-8b"}[cfg["model"]]
     if cfg["kind"] == "stress":
         return (f"refresh stress on gpt2-xl shapes B={cfg['B']}: {n_matrices} matrices, {params} "
-                f"params, every block eigensolved every step from fresh SPD blocks "
-                f"(gap >= 1e-3, cond 1e6), bf16 W/G")
+                f"params; a step sets every block's moments to a fresh SPD block (gap >= 1e-3, "
+                f"cond 1e6) and eigensolves every block (no parameter update)")
     s = (f"{base} B={cfg['B']}: {n_matrices} matrices, {params:.4g} params, {cfg['pdt']} W/G, "
          f"fp32 M, X {cfg['N']} {cfg['adt']} tokens/matrix, refresh every {cfg['T']}")
     if layers is not None:
@@ -537,7 +537,10 @@ def run_gpu(args):
             opt.accumulate(Xsets[s])
         if ev is not None:
             ev[1].record(stream)
-        opt.step(Ws, Gsets[s % len(Gsets)], LR)
+        if stress:
+            opt.refresh()   # the stress workload: every block of every matrix, every step
+        else:
+            opt.step(Ws, Gsets[s % len(Gsets)], LR)
         if ev is not None:
             ev[2].record(stream)
 
@@ -555,7 +558,8 @@ def run_gpu(args):
             e1.record(stream)
             torch.cuda.synchronize()
             cold_ms = e0.elapsed_time(e1)
-            opt.step(Ws, Gsets[0], LR)   # its scheduled refresh runs warm from the cold result
+            if not stress:
+                opt.step(Ws, Gsets[0], LR)   # its scheduled refresh runs warm from the cold result
             continue
         one_step(opt.t)
     torch.cuda.synchronize()
@@ -598,11 +602,13 @@ def run_gpu(args):
     ref_steps = [v for v, r in zip(upd_ref_ms, is_refresh) if r]
     upd_mean = mean(upd_ms)
     refresh_ms = None
-    if ref_steps and upd_mean is not None:
+    if stress:
+        refresh_ms = mean(upd_ref_ms)    # a stress step is the refresh alone
+    elif ref_steps and upd_mean is not None:
         refresh_ms = mean(ref_steps) - upd_mean
     # the update alone when every timed step refreshes (stress), and the
     # refresh alone when the timed window held none
-    if upd_mean is None or refresh_ms is None:
+    if not stress and (upd_mean is None or refresh_ms is None):
         e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
         saved_t = opt.t
         opt.t = 1 if T != 1 else 0
@@ -634,7 +640,8 @@ def run_gpu(args):
     ffma_src = peaks["source"] + " (FFMA)" if peaks else "nominal unit count (probes skipped)"
     ffma_update = args.norm != "sign"
     phases = {
-        "update": {"ms": upd_mean, "kernel": "step_ffma_kernel" if ffma_update else "step_tc_kernel",
+        "update": None if stress else
+                  {"ms": upd_mean, "kernel": "step_ffma_kernel" if ffma_update else "step_tc_kernel",
                    "bound": "hbm", "achieved": wm["update_bytes"] / (upd_mean * 1e-3) / 1e9,
                    "peak": hbm, "peak_source": mp["source"], "unit": "GB/s",
                    "flops": wm["update_flops"], "bytes": wm["update_bytes"]},
@@ -650,12 +657,14 @@ def run_gpu(args):
                     "peak": ffma_peak, "peak_source": ffma_src, "unit": "TFLOP/s",
                     "flops": wm["refresh_flops"]},
     }
+    phases = {k: v for k, v in phases.items() if v is not None}
     for p in phases.values():
         p["frac"] = p["achieved"] / p["peak"] if p.get("achieved") else None
     # dominant kernel: most device time per refresh cycle
     per_cycle = max(T, 1)
-    share = {"update": upd_mean * per_cycle, "accumulate": mean(acc_ms) * per_cycle,
-             "refresh": refresh_ms}
+    share = {"accumulate": mean(acc_ms) * per_cycle, "refresh": refresh_ms}
+    if not stress:
+        share["update"] = upd_mean * per_cycle
     dom = max(share, key=share.get)
     d = phases[dom]
     wl = workload_name(args.config, cfg, len(all_shapes), total_params, args.layers)
@@ -664,7 +673,7 @@ def run_gpu(args):
                 "kernel": d["kernel"], "peak_source": d["peak_source"]}
     # whole-step roofline: HBM bytes at the copy rate plus the refresh flops at
     # the FFMA rate, amortised over the refresh period
-    floor_ms = (wm["update_bytes"] + wm["acc_bytes"]) / (hbm * 1e9) * 1e3 + \
+    floor_ms = ((0 if stress else wm["update_bytes"]) + wm["acc_bytes"]) / (hbm * 1e9) * 1e3 + \
         wm["refresh_flops"] / (ffma_peak * 1e12) * 1e3 / per_cycle
 
     e2e = None
@@ -680,7 +689,7 @@ def run_gpu(args):
             cpu = {"error": repr(ex)}
 
     if rank == 0:
-        amort = mean(acc_ms) + upd_mean + refresh_ms / per_cycle
+        amort = mean(acc_ms) + (0 if stress else upd_mean) + refresh_ms / per_cycle
         line = {"metric": METRIC, "value": total_params / (ms_step * 1e-3), "unit": UNIT,
                 "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": ms_step,
                 "higher_is_better": True, "scaling": "strong" if world > 1 else "weak",
