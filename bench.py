@@ -527,7 +527,12 @@ def run_gpu(args):
     stream = torch.cuda.current_stream()
     moments = opt.tensor("moments")
 
+    stress_t = [0]   # the stress workload's own step counter (it runs no optimizer step)
+
     def one_step(t, ev=None):
+        if stress:
+            t = stress_t[0]
+            stress_t[0] += 1
         s = t % cfg["pool"]
         if ev is not None:
             ev[0].record(stream)
@@ -551,6 +556,7 @@ def run_gpu(args):
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             if stress:
                 moments.copy_(Msets[0])
+                stress_t[0] += 1
             else:
                 opt.accumulate(Xsets[0])
             e0.record(stream)
