@@ -39,7 +39,7 @@ constexpr int kThreads = 256;
 #include "mma_tf32.cuh"
 static_assert(kThreads == kTileThreads, "the tile products assume 256 threads");
 
-constexpr int kTableThreads = 256;   // a table: eight warps
+constexpr int kTableThreads = 128;   // a table: one team of four warps
 
 // Scratch of item i: B, V0, V1 (the basis and the work matrix swap roles at
 // every Newton-Schulz step; ctl.vsel names the one holding the basis).
@@ -176,22 +176,22 @@ __global__ void gj_flip_kernel(const __grid_constant__ GjArgs a, int pred) {
 }
 
 // ----------------------------------------------------------------- sweeps
-// Tables of round br: one CTA of eight warps per (table, item).  The table's
+// Tables of round br: one CTA of four warps per (table, item).  The table's
 // diagonal tile S (2g x 2g) and its rotation R live in shared memory.  Each
 // inner step rotates a set of disjoint column pairs ("slots", at most 32;
 // the first round's steps inside each group have a slot with a single member
-// when g is odd), computed by the first warp (lane = slot).  The two-sided
-// update S <- J^T S J is done block by block: the 2 x 2 block of S on the
-// members of slots X and Y becomes G_X S_XY G_Y^T (G = [[c, -s], [s, c]]);
-// the threads of (X, Y) and (Y, X) compute it from the same entries in the
-// same order and each writes its own rows, so S stays exactly symmetric.
-// R <- R J updates two columns per slot (kept transposed, rows contiguous).
-// Three barriers per step (rotations ready, S read, S written).
+// when g is odd), computed by the first warp (lane = slot).  The
+// two-sided update S <- J^T S J is done block by block: for slots X <= Y the
+// 2 x 2 block of S on their members becomes G_X S_XY G_Y^T (G = [[c, -s],
+// [s, c]]) and is written to both (X, Y) and (Y, X), so every entry of S is
+// read once and written once per step and S stays exactly symmetric; R <- R J
+// updates two columns per slot (kept transposed, rows contiguous).  Two
+// barriers per step.
 constexpr int kLS = 65;             // row stride of S and R^T in shared memory
 constexpr int kMaxSlots = 32;
 
-__global__ void __launch_bounds__(kTableThreads, 4) gj_table_kernel(const __grid_constant__ GjArgs a,
-                                                                    int br) {
+__global__ void __launch_bounds__(kTableThreads) gj_table_kernel(const __grid_constant__ GjArgs a,
+                                                                 int br) {
   __shared__ float S[64 * kLS];
   __shared__ float Rt[64 * kLS];
   __shared__ int slot_p[kMaxSlots], slot_q[kMaxSlots];
@@ -260,52 +260,50 @@ __global__ void __launch_bounds__(kTableThreads, 4) gj_table_kernel(const __grid
       }
     }
     __syncthreads();
-    // S blocks: warp w takes the block rows X = w, w + 4, ..., lane Y the
-    // block (X, Y).  Both (X, Y) and (Y, X) compute the same 2 x 2 result from
-    // the same entries (the rows of min(X, Y)), G_A S_AB G_B^T, so S stays
-    // exactly symmetric; every thread then writes only the rows of its X.
-    // Reads along a row and across rows (stride 65) fall in distinct banks.
-    constexpr int kRows = (kMaxSlots + kTableThreads / 32 - 1) / (kTableThreads / 32);
-    float res[kRows][4];
-#pragma unroll
-    for (int i = 0; i < kRows; ++i) {
-      const int X = warp + i * (kTableThreads / 32), Y = lane;
-      res[i][0] = res[i][1] = res[i][2] = res[i][3] = 0.f;
-      if (X >= nslots || Y >= nslots) continue;
-      const int A = X < Y ? X : Y, Bs = X < Y ? Y : X;
-      const float sA = slot_s[A], sB = slot_s[Bs];
-      if (sA == 0.f && sB == 0.f) continue;
-      const int pA = slot_p[A], qA = slot_q[A], pB = slot_p[Bs], qB = slot_q[Bs];
-      const float cA = slot_c[A], cB = slot_c[Bs];
-      const bool hA = qA >= 0, hB = qB >= 0;
-      const float m00 = S[pA * kLS + pB];
-      const float m01 = hB ? S[pA * kLS + qB] : 0.f;
-      const float m10 = hA ? S[qA * kLS + pB] : 0.f;
-      const float m11 = (hA && hB) ? S[qA * kLS + qB] : 0.f;
-      // rows: G_A M; columns: (G_A M) G_B^T
-      const float t00 = cA * m00 - sA * m10, t01 = cA * m01 - sA * m11;
-      const float t10 = sA * m00 + cA * m10, t11 = sA * m01 + cA * m11;
-      const float n00 = cB * t00 - sB * t01, n01 = sB * t00 + cB * t01;
-      const float n10 = cB * t10 - sB * t11, n11 = sB * t10 + cB * t11;
-      // as rows of X: N itself when X = A, its transpose when X = B
-      res[i][0] = n00;
-      res[i][1] = X == A ? n01 : n10;
-      res[i][2] = X == A ? n10 : n01;
-      res[i][3] = n11;
-      if (X == Y) res[i][2] = n01;   // the diagonal block, exactly symmetric
-    }
-    __syncthreads();   // every read of S done
-#pragma unroll
-    for (int i = 0; i < kRows; ++i) {
-      const int X = warp + i * (kTableThreads / 32), Y = lane;
-      if (X >= nslots || Y >= nslots) continue;
-      if (slot_s[X] == 0.f && slot_s[Y] == 0.f) continue;
+    // S blocks (X <= Y): warp w takes the block rows X = w, w + 4, ...,
+    // lane Y the blocks (X, Y) with Y >= X; reads along the rows of slot X
+    // and mirrored writes (row stride 65) fall in distinct banks
+    for (int X = warp; X < nslots; X += kTableThreads / 32) {
+      const int Y = lane;
+      const float sX = slot_s[X];
+      if (Y < X || Y >= nslots) continue;
+      const float sY = slot_s[Y];
+      if (sX == 0.f && sY == 0.f) continue;
       const int pX = slot_p[X], qX = slot_q[X], pY = slot_p[Y], qY = slot_q[Y];
-      S[pX * kLS + pY] = res[i][0];
-      if (qY >= 0) S[pX * kLS + qY] = res[i][1];
-      if (qX >= 0) {
-        S[qX * kLS + pY] = res[i][2];
-        if (qY >= 0) S[qX * kLS + qY] = res[i][3];
+      const float cX = slot_c[X], cY = slot_c[Y];
+      const bool hX = qX >= 0, hY = qY >= 0;
+      const float m00 = S[pX * kLS + pY];
+      const float m01 = hY ? S[pX * kLS + qY] : 0.f;
+      const float m10 = hX ? S[qX * kLS + pY] : 0.f;
+      const float m11 = (hX && hY) ? S[qX * kLS + qY] : 0.f;
+      // rows: G_X M
+      const float t00 = cX * m00 - sX * m10, t01 = cX * m01 - sX * m11;
+      const float t10 = sX * m00 + cX * m10, t11 = sX * m01 + cX * m11;
+      // columns: (G_X M) G_Y^T
+      const float n00 = cY * t00 - sY * t01, n01 = sY * t00 + cY * t01;
+      const float n10 = cY * t10 - sY * t11, n11 = sY * t10 + cY * t11;
+      if (X == Y) {
+        S[pX * kLS + pX] = n00;
+        if (hX) {
+          S[qX * kLS + qX] = n11;
+          S[pX * kLS + qX] = n01;
+          S[qX * kLS + pX] = n01;
+        }
+      } else {
+        S[pX * kLS + pY] = n00;
+        S[pY * kLS + pX] = n00;
+        if (hY) {
+          S[pX * kLS + qY] = n01;
+          S[qY * kLS + pX] = n01;
+        }
+        if (hX) {
+          S[qX * kLS + pY] = n10;
+          S[pY * kLS + qX] = n10;
+        }
+        if (hX && hY) {
+          S[qX * kLS + qY] = n11;
+          S[qY * kLS + qX] = n11;
+        }
       }
     }
     // R <- R J: columns p, q of R = rows p, q of R^T; warp per slot, lanes
