@@ -156,9 +156,6 @@ step_tc_kernel(const __grid_constant__ StepArgs a, const __grid_constant__ TcArg
   unsigned char* a_buf = base;                                   // [stage][hi|lo]
   unsigned char* b_buf = base + nas * 2 * kAChunkBytes;          // [stage] t.bstage bytes
   TcSmem* sh = reinterpret_cast<TcSmem*>(b_buf + t.nbstage * t.bstage);
-  // per epilogue warp a 32 x 32 staging tile of U (row stride 33)
-  float* ep_buf = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(sh) +
-                                           ((sizeof(TcSmem) + 15) & ~size_t(15)));
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t nbs = (uint32_t)t.nbstage;  // B stages of this launch
@@ -520,13 +517,9 @@ step_tc_kernel(const __grid_constant__ StepArgs a, const __grid_constant__ TcArg
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh->s_full);
-      // drain U piece by piece.  Row-major parameters: the piece goes through
-      // a 32 x 32 staging tile so that the warp reads and writes W in row
-      // segments (8 lanes per row, four columns each); transposed parameters
-      // (output side): each lane applies its own row, the next piece's
-      // parameters loading while this one is applied.
+      // drain U piece by piece; the parameters of the next 32-column piece
+      // load while this one is applied
       bool ok = true;
-      float* us = ep_buf + (warp & 3) * 32 * 33;
       float wn[32];
       auto loadw = [&](int l0, float (&dst)[32]) {
 #pragma unroll
@@ -541,7 +534,7 @@ step_tc_kernel(const __grid_constant__ StepArgs a, const __grid_constant__ TcArg
           dst[4 * e] = t4[0]; dst[4 * e + 1] = t4[1]; dst[4 * e + 2] = t4[2]; dst[4 * e + 3] = t4[3];
         }
       };
-      if (wt) loadw(0, wn);
+      loadw(0, wn);
       for (int c0 = 0; c0 < kpN; c0 += kUCols) {
         const int nn = min(kUCols, kpN - c0);
         const int b = ucount & 1;
@@ -550,49 +543,12 @@ step_tc_kernel(const __grid_constant__ StepArgs a, const __grid_constant__ TcArg
         tc_fence_after();
         for (int q = 0; q * 32 < nn; ++q) {
           const int l0 = c0 + 32 * q;
-          float u[32];
-          if (!wt) {
-            tmem_ld32(trow + 256 + kUCols * b + 32 * q, u);
-            tmem_wait_ld(u);
-            if (rvalid) {
-#pragma unroll
-              for (int i = 0; i < 32; ++i)
-                if (l0 + i < k) u2 = fmaf(u[i], u[i], u2);
-            }
-#pragma unroll
-            for (int i = 0; i < 32; ++i) us[lane * 33 + i] = u[i];
-            __syncwarp();
-            const int cq = 4 * (lane & 7);
-            const bool cok = l0 + cq < k;   // k % 4 == 0: all four columns or none
-            float wv4[8][4];
-#pragma unroll
-            for (int it = 0; it < 8; ++it) {
-              const int64_t grow = (int64_t)tl.a + 32 * g + (lane >> 3) + 4 * it;
-              if (cok && grow < mi.m) {
-                load4(W + grow * n + (int64_t)tl.blk * k + l0 + cq, wv4[it]);
-              } else {
-                wv4[it][0] = wv4[it][1] = wv4[it][2] = wv4[it][3] = 0.f;
-              }
-            }
-#pragma unroll
-            for (int it = 0; it < 8; ++it) {
-              const int rr = (lane >> 3) + 4 * it;
-              const int64_t grow = (int64_t)tl.a + 32 * g + rr;
-              if (cok && grow < mi.m) {
-                float o[4];
-#pragma unroll
-                for (int z = 0; z < 4; ++z) o[z] = fmaf(-a.lr_s, us[rr * 33 + cq + z], wv4[it][z]);
-                store4(W + grow * n + (int64_t)tl.blk * k + l0 + cq, o);
-              }
-            }
-            __syncwarp();
-            continue;
-          }
           float wv[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) wv[i] = wn[i];
           if (l0 + 32 < kpN) loadw(l0 + 32, wn);
           const bool any = rvalid && l0 < k;
+          float u[32];
           tmem_ld32(trow + 256 + kUCols * b + 32 * q, u);
           tmem_wait_ld(u);
           if (any) {
@@ -700,8 +656,7 @@ size_t step_tc_bstage(int max_k) {
 }
 
 size_t step_tc_smem(int max_k, int nastage, int nbstage) {
-  return 1024 + (size_t)nastage * 2 * kAChunkBytes + nbstage * step_tc_bstage(max_k) +
-         ((sizeof(TcSmem) + 15) & ~size_t(15)) + 4 * 32 * 33 * sizeof(float) + 64;
+  return 1024 + (size_t)nastage * 2 * kAChunkBytes + nbstage * step_tc_bstage(max_k) + sizeof(TcSmem) + 64;
 }
 
 // Momentum stages of a launch.
