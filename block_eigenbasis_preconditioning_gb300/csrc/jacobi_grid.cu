@@ -177,25 +177,74 @@ __global__ void gj_flip_kernel(const __grid_constant__ GjArgs a, int pred) {
 
 // ----------------------------------------------------------------- sweeps
 // Tables of round br: one CTA of four warps per (table, item).  The table's
-// diagonal tile S (2g x 2g) and its rotation R live in shared memory.  Each
-// inner step rotates a set of disjoint column pairs ("slots", at most 32;
-// the first round's steps inside each group have a slot with a single member
-// when g is odd), computed by the first warp (lane = slot).  The
-// two-sided update S <- J^T S J is done block by block: for slots X <= Y the
-// 2 x 2 block of S on their members becomes G_X S_XY G_Y^T (G = [[c, -s],
-// [s, c]]) and is written to both (X, Y) and (Y, X), so every entry of S is
-// read once and written once per step and S stays exactly symmetric; R <- R J
-// updates two columns per slot (kept transposed, rows contiguous).  Two
-// barriers per step.
-constexpr int kLS = 65;             // row stride of S and R^T in shared memory
+// diagonal tile S (2g x 2g, zero-padded to 64 x 64) and its rotation R (kept
+// transposed, R^T) live in shared memory.  Each inner step rotates a set of
+// disjoint column pairs ("slots", at most 32).  In the first round's steps
+// inside each group, a slot has a single member when g is odd; that member
+// is paired with the padding row kPadRow, which holds zeros.  The first warp
+// computes the slots' rotations (lane = slot) into one 16-byte record each;
+// then every thread works through a fixed list of items:
+//  * S <- J^T S J, block by block.  For each unordered slot pair {X, Y}, the
+//    2 x 2 block of S on their members becomes G_X S_XY G_Y^T (G = [[c, -s],
+//    [s, c]]).  It is written to (X, Y) and mirrored to (Y, X), so every entry
+//    is read and written once and S stays exactly symmetric.  The pairs are
+//    dealt to the threads in circulant order (Y = X + d mod slots, d = 0, 1,
+//    ...), so all lanes are busy.  With row stride 64 the lanes of a warp
+//    (consecutive X, one d) address distinct columns, hence distinct banks,
+//    on both the block and its mirror.
+//  * R <- R J: for each (slot, column pair), rows p and q of R^T, two entries
+//    per item (float2).
+// Identity rotations (pairs past the block, single members, entries at the
+// floor) leave their entries bit-for-bit unchanged, and the padding row
+// stays zero.  Two barriers per step.
+constexpr int kLS = 64;        // row stride of S in shared memory
+constexpr int kLR = 66;        // row stride of R^T (even for float2 rows; the transposed read-out is 2-way)
 constexpr int kMaxSlots = 32;
+constexpr int kPadRow = 63;    // partner of a single-member slot (odd g: 2g <= 62)
+constexpr int kBlkPer = (32 * 33 / 2 + kTableThreads - 1) / kTableThreads;  // slot pairs per thread
+constexpr int kRotPer = (32 * 32 + kTableThreads - 1) / kTableThreads;      // R items per thread
 
-__global__ void __launch_bounds__(kTableThreads) gj_table_kernel(const __grid_constant__ GjArgs a,
-                                                                 int br) {
-  __shared__ float S[64 * kLS];
-  __shared__ float Rt[64 * kLS];
-  __shared__ int slot_p[kMaxSlots], slot_q[kMaxSlots];
-  __shared__ float slot_c[kMaxSlots], slot_s[kMaxSlots];
+struct __align__(16) SlotRec {
+  float c, s;
+  int p, q;
+};
+
+// This thread's slot pairs among ns slots, in circulant order, packed as
+// X | Y << 8 (-1 past the end): pair l is (X, X + d mod ns) with d = l / ns.
+// d = 0 .. (ns - 1) / 2 lists every unordered pair once, plus, for even ns,
+// the first ns / 2 pairs of d = ns / 2.
+__device__ __forceinline__ void deal_pairs(int ns, int (&out)[kBlkPer]) {
+  const int nb = ns * (ns + 1) / 2;
+#pragma unroll
+  for (int i = 0; i < kBlkPer; ++i) {
+    const int l = threadIdx.x + i * kTableThreads;
+    out[i] = -1;
+    if (l < nb) {
+      const int d = l / ns, X = l - d * ns;
+      const int Y = X + d < ns ? X + d : X + d - ns;
+      out[i] = X | (Y << 8);
+    }
+  }
+}
+
+// This thread's R items among ns slots x nh column pairs, packed X | jj << 8.
+__device__ __forceinline__ void deal_rot(int ns, int nh, int (&out)[kRotPer]) {
+#pragma unroll
+  for (int i = 0; i < kRotPer; ++i) {
+    const int l = threadIdx.x + i * kTableThreads;
+    out[i] = -1;
+    if (l < ns * nh) {
+      const int X = l / nh;
+      out[i] = X | ((l - X * nh) << 8);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kTableThreads, 6) gj_table_kernel(const __grid_constant__ GjArgs a,
+                                                                    int br) {
+  __shared__ __align__(16) float S[64 * kLS];
+  __shared__ __align__(16) float Rt[64 * kLR];
+  __shared__ SlotRec sl[kMaxSlots];
   const int item = blockIdx.y, tt = blockIdx.x;
   GjCtl* c = a.ctl + item;
   if (!pred_ok(*c, kActive)) return;
@@ -207,131 +256,120 @@ __global__ void __launch_bounds__(kTableThreads) gj_table_kernel(const __grid_co
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   int gI, gJ;
   rr_pair(br, tt, G.nG, gI, gJ);
-  for (int e = tid; e < nn; e += blockDim.x) {
-    const int r = e / n2, q = e - r * n2;
-    const int cr = table_col(r, gI, gJ, g, k), cq = table_col(q, gI, gJ, g, k);
-    S[r * kLS + q] = (cr < k && cq < k) ? b.B[(int64_t)cr * k + cq] : 0.f;
-    Rt[r * kLS + q] = r == q ? 1.f : 0.f;
+  // S = the table's tile of B, R^T = I; zero outside the table
+  for (int r = warp; r < 64; r += kTableThreads / 32) {
+    const int cr = r < n2 ? table_col(r, gI, gJ, g, k) : k;
+    for (int q = lane; q < 64; q += 32) {
+      const int cq = q < n2 ? table_col(q, gI, gJ, g, k) : k;
+      S[r * kLS + q] = (cr < k && cq < k) ? b.B[(int64_t)cr * k + cq] : 0.f;
+      Rt[r * kLR + q] = (r == q && r < n2) ? 1.f : 0.f;
+    }
   }
-  __syncthreads();
   const float bfloor = c->bfloor;
   const int gp = g + (g & 1);
   const int n_intra = br == 0 ? gp - 1 : 0;
+  int blk[kBlkPer], rit[kRotPer];
+  deal_pairs(n_intra ? gp : g, blk);
+  deal_rot(n_intra ? gp : g, g, rit);
+  __syncthreads();
   int rots = 0;
   for (int step = 0; step < n_intra + g; ++step) {
     const bool intra = step < n_intra;
     const int r = intra ? step : step - n_intra;
-    const int nslots = intra ? gp : g;
-    if (warp == 0) {
-      // slot `lane`: members p < q (q = -1: a single member), rotation (cs, sn)
-      int p = -1, q = -1;
-      float cs = 1.f, sn = 0.f;
-      if (lane < nslots) {
-        if (intra) {
-          const int half = gp >> 1, grp = lane / half, ii = lane - grp * half;
-          int pp, qq;
-          rr_pair(r, ii, gp, pp, qq);
-          if (pp >= g) pp = -1;
-          if (qq >= g) qq = -1;
-          if (pp < 0) { pp = qq; qq = -1; }
-          p = pp + grp * g;
-          q = qq < 0 ? -1 : qq + grp * g;
-        } else {
-          p = lane;
-          q = g + (lane + r) % g;
+    const int ns = intra ? gp : g;
+    if (step == n_intra && n_intra) {
+      deal_pairs(g, blk);
+      deal_rot(g, g, rit);
+    }
+    if (warp == 0 && lane < ns) {
+      int p, q;
+      bool single = false;
+      if (intra) {
+        // group grp's round-robin pair; player g is the odd group's dummy
+        const int half = gp >> 1, grp = lane / half, ii = lane - grp * half;
+        int pp, qq;
+        rr_pair(r, ii, gp, pp, qq);
+        if (pp >= g) {
+          pp = qq;
+          single = true;
+        } else if (qq >= g) {
+          single = true;
         }
-        if (q >= 0 && q < p) {
-          const int t = p; p = q; q = t;
+        if (!single && qq < pp) {
+          const int t = pp; pp = qq; qq = t;
         }
-        if (q >= 0 && table_col(p, gI, gJ, g, k) < k && table_col(q, gI, gJ, g, k) < k) {
-          const float bpq = S[p * kLS + q];
-          if (fabsf(bpq) > bfloor) {
-            const float ta = (S[q * kLS + q] - S[p * kLS + p]) / (2.f * bpq);
-            const float tn = ta >= 0.f ? 1.f / (ta + sqrtf(1.f + ta * ta)) : -1.f / (-ta + sqrtf(1.f + ta * ta));
-            cs = 1.f / sqrtf(1.f + tn * tn);
-            sn = tn * cs;
-            ++rots;
-          }
-        }
-        slot_p[lane] = p;
-        slot_q[lane] = q;
-        slot_c[lane] = cs;
-        slot_s[lane] = sn;
+        p = pp + grp * g;
+        q = single ? kPadRow : qq + grp * g;
+      } else {
+        p = lane;
+        q = g + (lane + r) % g;
       }
+      float cs = 1.f, sn = 0.f;
+      if (!single && table_col(p, gI, gJ, g, k) < k && table_col(q, gI, gJ, g, k) < k) {
+        const float bpq = S[p * kLS + q];
+        if (fabsf(bpq) > bfloor) {
+          const float ta = (S[q * kLS + q] - S[p * kLS + p]) / (2.f * bpq);
+          const float tn = ta >= 0.f ? 1.f / (ta + sqrtf(1.f + ta * ta)) : -1.f / (-ta + sqrtf(1.f + ta * ta));
+          cs = 1.f / sqrtf(1.f + tn * tn);
+          sn = tn * cs;
+          ++rots;
+        }
+      }
+      sl[lane] = SlotRec{cs, sn, p, q};
     }
     __syncthreads();
-    // S blocks (X <= Y): warp w takes the block rows X = w, w + 4, ...,
-    // lane Y the blocks (X, Y) with Y >= X; reads along the rows of slot X
-    // and mirrored writes (row stride 65) fall in distinct banks
-    for (int X = warp; X < nslots; X += kTableThreads / 32) {
-      const int Y = lane;
-      const float sX = slot_s[X];
-      if (Y < X || Y >= nslots) continue;
-      const float sY = slot_s[Y];
-      if (sX == 0.f && sY == 0.f) continue;
-      const int pX = slot_p[X], qX = slot_q[X], pY = slot_p[Y], qY = slot_q[Y];
-      const float cX = slot_c[X], cY = slot_c[Y];
-      const bool hX = qX >= 0, hY = qY >= 0;
-      const float m00 = S[pX * kLS + pY];
-      const float m01 = hY ? S[pX * kLS + qY] : 0.f;
-      const float m10 = hX ? S[qX * kLS + pY] : 0.f;
-      const float m11 = (hX && hY) ? S[qX * kLS + qY] : 0.f;
+    // S blocks: the thread's pairs are disjoint from every other thread's
+    // (only the zero padding entries are shared, and stay zero)
+#pragma unroll
+    for (int i = 0; i < kBlkPer; ++i) {
+      const int xy = blk[i];
+      if (xy < 0) continue;
+      const SlotRec x = sl[xy & 255], y = sl[xy >> 8];
+      const float m00 = S[x.p * kLS + y.p], m01 = S[x.p * kLS + y.q];
+      const float m10 = S[x.q * kLS + y.p], m11 = S[x.q * kLS + y.q];
       // rows: G_X M
-      const float t00 = cX * m00 - sX * m10, t01 = cX * m01 - sX * m11;
-      const float t10 = sX * m00 + cX * m10, t11 = sX * m01 + cX * m11;
-      // columns: (G_X M) G_Y^T
-      const float n00 = cY * t00 - sY * t01, n01 = sY * t00 + cY * t01;
-      const float n10 = cY * t10 - sY * t11, n11 = sY * t10 + cY * t11;
-      if (X == Y) {
-        S[pX * kLS + pX] = n00;
-        if (hX) {
-          S[qX * kLS + qX] = n11;
-          S[pX * kLS + qX] = n01;
-          S[qX * kLS + pX] = n01;
-        }
-      } else {
-        S[pX * kLS + pY] = n00;
-        S[pY * kLS + pX] = n00;
-        if (hY) {
-          S[pX * kLS + qY] = n01;
-          S[qY * kLS + pX] = n01;
-        }
-        if (hX) {
-          S[qX * kLS + pY] = n10;
-          S[pY * kLS + qX] = n10;
-        }
-        if (hX && hY) {
-          S[qX * kLS + qY] = n11;
-          S[qY * kLS + qX] = n11;
-        }
-      }
+      const float t00 = x.c * m00 - x.s * m10, t01 = x.c * m01 - x.s * m11;
+      const float t10 = x.s * m00 + x.c * m10, t11 = x.s * m01 + x.c * m11;
+      // columns: (G_X M) G_Y^T; for X = Y the mirrored writes of the
+      // off-diagonal pair both end as n10
+      const float n00 = y.c * t00 - y.s * t01, n01 = y.s * t00 + y.c * t01;
+      const float n10 = y.c * t10 - y.s * t11, n11 = y.s * t10 + y.c * t11;
+      S[x.p * kLS + y.p] = n00;
+      S[y.p * kLS + x.p] = n00;
+      S[x.p * kLS + y.q] = n01;
+      S[y.q * kLS + x.p] = n01;
+      S[x.q * kLS + y.p] = n10;
+      S[y.p * kLS + x.q] = n10;
+      S[x.q * kLS + y.q] = n11;
+      S[y.q * kLS + x.q] = n11;
     }
-    // R <- R J: columns p, q of R = rows p, q of R^T; warp per slot, lanes
-    // along the row
-    for (int X = warp; X < nslots; X += kTableThreads / 32) {
-      const float sX = slot_s[X];
-      if (sX == 0.f) continue;
-      const int pX = slot_p[X], qX = slot_q[X];
-      const float cX = slot_c[X];
-      for (int j = lane; j < n2; j += 32) {
-        const float ra = Rt[pX * kLS + j], rb = Rt[qX * kLS + j];
-        Rt[pX * kLS + j] = cX * ra - sX * rb;
-        Rt[qX * kLS + j] = sX * ra + cX * rb;
-      }
+    // R^T rows p, q of each slot, two columns per item
+#pragma unroll
+    for (int i = 0; i < kRotPer; ++i) {
+      const int xj = rit[i];
+      if (xj < 0) continue;
+      const SlotRec x = sl[xj & 255];
+      float2* ra = reinterpret_cast<float2*>(Rt + x.p * kLR) + (xj >> 8);
+      float2* rb = reinterpret_cast<float2*>(Rt + x.q * kLR) + (xj >> 8);
+      const float2 u = *ra, v = *rb;
+      *ra = make_float2(x.c * u.x - x.s * v.x, x.c * u.y - x.s * v.y);
+      *rb = make_float2(x.s * u.x + x.c * v.x, x.s * u.y + x.c * v.y);
     }
     __syncthreads();
   }
   float* Rg = a.rbuf + (int64_t)item * a.rstride + (int64_t)tt * nn;
-  for (int e = tid; e < nn; e += blockDim.x) {
-    const int r = e / n2, q = e - r * n2;
-    const int cr = table_col(r, gI, gJ, g, k), cq = table_col(q, gI, gJ, g, k);
-    if (cr < k && cq < k) b.B[(int64_t)cr * k + cq] = S[r * kLS + q];
-    Rg[e] = Rt[q * kLS + r];   // R[r][q]
+  for (int r = warp; r < n2; r += kTableThreads / 32) {
+    const int cr = table_col(r, gI, gJ, g, k);
+    for (int q = lane; q < n2; q += 32) {
+      const int cq = table_col(q, gI, gJ, g, k);
+      if (cr < k && cq < k) b.B[(int64_t)cr * k + cq] = S[r * kLS + q];
+      Rg[r * n2 + q] = Rt[q * kLR + r];   // R[r][q]
+    }
   }
   int tot = rots;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
-  if (lane == 0 && warp == 0 && tot) atomicAdd(&c->rot, tot);
+  if (tid == 0 && tot) atomicAdd(&c->rot, tot);
 }
 
 // E = R - I of table t into a zero-padded 64 x kLdM tile.
