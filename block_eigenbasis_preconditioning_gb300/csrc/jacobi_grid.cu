@@ -73,28 +73,47 @@ __device__ __forceinline__ ItemBufs bufs_of(const GjArgs& a, int item) {
 
 // ------------------------------------------------------------------- init
 // V = Q^T-layout copy of the current basis (column j of V = column j of the
-// row-major Q), ||A||_F^2 and the finiteness of A, over chunks of entries.
+// row-major Q, moved through 32 x 32 shared tiles so both sides are
+// coalesced), ||A||_F^2 and the finiteness of A over this CTA's rows
+// (per-thread fp32 partial sums of at most a few hundred terms, combined in
+// fp64).
 __global__ void __launch_bounds__(kThreads) gj_init_kernel(const __grid_constant__ GjArgs a) {
   __shared__ double red[32];
+  __shared__ float tile[32][33];
   const int item = blockIdx.y;
   const ItemBufs b = bufs_of(a, item);
   const int k = a.k;
-  const int64_t kk2 = (int64_t)k * k;
-  const int64_t per = (kk2 + gridDim.x - 1) / gridDim.x;
-  const int64_t e0 = (int64_t)blockIdx.x * per, e1 = min(kk2, e0 + per);
-  double ss = 0.0;
+  const int rows = (k + gridDim.x - 1) / gridDim.x;
+  const int r0 = min(k, (int)blockIdx.x * rows), r1 = min(k, r0 + rows);
+  float ss = 0.f;
   int bad = 0;
-  for (int64_t e = e0 + threadIdx.x; e < e1; e += blockDim.x) {
-    const float v = b.A[e];
-    bad |= !isfinite(v);
-    ss += (double)v * v;
-    const int64_t c = e / k, i = e - c * k;
-    b.V[e] = b.Q[i * k + c];
+  for (int i = r0; i < r1; ++i) {
+    const float* row = b.A + (int64_t)i * k;
+    for (int j = threadIdx.x; j < k; j += blockDim.x) {
+      const float v = row[j];
+      bad |= !isfinite(v);
+      ss = fmaf(v, v, ss);
+    }
   }
-  ss = block_sum_d(ss, red);
+  const int nt = (k + 31) / 32;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  for (int tl = blockIdx.x; tl < nt * nt; tl += gridDim.x) {
+    const int bi = tl / nt, bc = tl - bi * nt;   // Q rows 32 bi.., columns 32 bc..
+    __syncthreads();
+    for (int rr = ty; rr < 32; rr += kThreads / 32) {
+      const int i = 32 * bi + rr, c = 32 * bc + tx;
+      tile[rr][tx] = (i < k && c < k) ? b.Q[(int64_t)i * k + c] : 0.f;
+    }
+    __syncthreads();
+    for (int rr = ty; rr < 32; rr += kThreads / 32) {
+      const int c = 32 * bc + rr, i = 32 * bi + tx;
+      if (c < k && i < k) b.V[(int64_t)c * k + i] = tile[tx][rr];
+    }
+  }
+  const double tot = block_sum_d((double)ss, red);
   bad = __syncthreads_or(bad);
   if (threadIdx.x == 0) {
-    atomicAdd(&a.ctl[item].tot2, ss);
+    atomicAdd(&a.ctl[item].tot2, tot);
     if (bad) atomicOr(&a.ctl[item].skip, 1);
   }
 }
@@ -372,20 +391,27 @@ __global__ void __launch_bounds__(kTableThreads, 6) gj_table_kernel(const __grid
   if (tid == 0 && tot) atomicAdd(&c->rot, tot);
 }
 
-// E = R - I of table t into a zero-padded 64 x kLdM tile.
+// E = R - I of table t into a zero-padded 64 x kLdM tile (warp rows, lanes
+// along the row: coalesced loads, conflict-free stores).
+constexpr int kRowsPerWarp = kT / (kThreads / 32);
+
 __device__ __forceinline__ void load_corr(float* dst, const float* src, int n2) {
-  constexpr int kPer = kT * kT / kThreads;
-  float v[kPer];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  float v[kRowsPerWarp][2];
 #pragma unroll
-  for (int i = 0; i < kPer; ++i) {
-    const int e = threadIdx.x + i * kThreads;
-    const int r = e / kT, q = e - r * kT;
-    v[i] = (r < n2 && q < n2) ? src[r * n2 + q] - (r == q ? 1.f : 0.f) : 0.f;
+  for (int i = 0; i < kRowsPerWarp; ++i) {
+    const int r = warp + (kThreads / 32) * i;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int q = lane + 32 * h;
+      v[i][h] = (r < n2 && q < n2) ? src[r * n2 + q] - (r == q ? 1.f : 0.f) : 0.f;
+    }
   }
 #pragma unroll
-  for (int i = 0; i < kPer; ++i) {
-    const int e = threadIdx.x + i * kThreads;
-    dst[(e / kT) * kLdM + (e % kT)] = v[i];
+  for (int i = 0; i < kRowsPerWarp; ++i) {
+    const int r = warp + (kThreads / 32) * i;
+    dst[r * kLdM + lane] = v[i][0];
+    dst[r * kLdM + lane + 32] = v[i][1];
   }
 }
 
@@ -394,18 +420,30 @@ __device__ __forceinline__ void corr_product(const float* P, const float* Q, int
   mma_tn_64<kPasses>(P, Q, n, acc);
 }
 
-// Tile pairs and panels of round br: unit u < npair is the tile pair (s, t),
-// s < t, in row order; the rest are the panels (t, i0) of V.  The products
-// run on the warp-level tensor cores in correction form: with E = R - I,
+// Tile pairs and panels of round br.  Unit u < npair is the tile pair (s, t),
+// s < t, in row order; the rest are panel runs (t, c0): the 64-row panels
+// c0 .. c0 + kPanelRun - 1 of V's columns P_t, one after another on one
+// E_t.  The products run on the warp-level tensor cores in correction form:
+// with E = R - I,
 //   Y = X + E_s^T X,  Z = Y + Y E_t       (B[P_s, P_t] <- R_s^T X R_t)
 //   V' = V + V E_t                         (V[i0:i0+64, P_t] <- V R_t)
 // the TF32-rounded products added onto fp32 X, Y, V.  A sweep on a freshly
 // formed B (the only kind that can end the iteration) multiplies in split
 // precision (~2^-21 |E| |X|); the other sweeps, whose B is re-formed from A
 // before the iteration can stop and whose basis only seeds that re-forming,
-// in plain TF32.
-__global__ void __launch_bounds__(kThreads) gj_apply_kernel(const __grid_constant__ GjArgs a, int br) {
+// in plain TF32.  The columns of B (or V) that a table's local indices
+// stand for are looked up once per CTA.
+constexpr int kPanelRun = 4;
+
+__host__ __device__ __forceinline__ int apply_units(int k) {
+  const Geo G = geo_for(k);
+  const int nI = (k + kT - 1) / kT;
+  return G.nT * (G.nT - 1) / 2 + G.nT * ((nI + kPanelRun - 1) / kPanelRun);
+}
+
+__global__ void __launch_bounds__(kThreads, 4) gj_apply_kernel(const __grid_constant__ GjArgs a, int br) {
   extern __shared__ __align__(16) float sm[];
+  __shared__ int colS[kT], colT[kT];
   const int item = blockIdx.y;
   const GjCtl& cref = a.ctl[item];
   if (!pred_ok(cref, kActive)) return;
@@ -414,47 +452,60 @@ __global__ void __launch_bounds__(kThreads) gj_apply_kernel(const __grid_constan
   const Geo G = geo_for(k);
   if (br >= G.nG - 1) return;
   const int nI = (k + kT - 1) / kT;
+  const int nPR = (nI + kPanelRun - 1) / kPanelRun;
   const int npair = G.nT * (G.nT - 1) / 2;
   const int u = blockIdx.x;
-  if (u >= npair + G.nT * nI) return;
+  if (u >= npair + G.nT * nPR) return;
   const ItemBufs b = bufs_of(a, item);
   const int n2 = G.n2, nn = n2 * n2;
   const float* Rb = a.rbuf + (int64_t)item * a.rstride;
-  // three tiles: E_s (then Y^T and Z^T), E_t, X (then Z)
+  // three tiles: E_s (then Y^T and Z^T, or the panel output), E_t, X
   float* Es = sm;
   float* Et = sm + kT * kLdM;
   float* Xs = sm + 2 * kT * kLdM;
   float* Ys = Es;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
-  float acc[4][4];
-  if (u < npair) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const bool pair = u < npair;
+  int s = 0, t = 0, c0 = 0;
+  if (pair) {
     // (s, t) from the linear index of the strict upper triangle
-    int s = 0, rem = u;
+    int rem = u;
     while (rem >= G.nT - 1 - s) {
       rem -= G.nT - 1 - s;
       ++s;
     }
-    const int t = s + 1 + rem;
-    int sI, sJ, tI, tJ;
-    rr_pair(br, s, G.nG, sI, sJ);
-    rr_pair(br, t, G.nG, tI, tJ);
+    t = s + 1 + rem;
+  } else {
+    const int v = u - npair;
+    t = v / nPR;
+    c0 = (v - t * nPR) * kPanelRun;
+  }
+  if (tid < 2 * kT) {
+    const int r = tid & (kT - 1);
+    int gI, gJ;
+    rr_pair(br, tid < kT ? s : t, G.nG, gI, gJ);
+    (tid < kT ? colS : colT)[r] = r < n2 ? table_col(r, gI, gJ, G.g, k) : k;
+  }
+  __syncthreads();
+  float acc[4][4];
+  if (pair) {
+    const int cq0 = colT[lane], cq1 = colT[lane + 32];
     {
-      constexpr int kPer = kT * kT / kThreads;
-      float v[kPer];
+      float v[kRowsPerWarp][2];
 #pragma unroll
-      for (int i = 0; i < kPer; ++i) {
-        const int e = tid + i * kThreads;
-        const int r = e / kT, q = e - r * kT;
-        const int cr = r < n2 ? table_col(r, sI, sJ, G.g, k) : k;
-        const int cq = q < n2 ? table_col(q, tI, tJ, G.g, k) : k;
-        v[i] = (cr < k && cq < k) ? b.B[(int64_t)cr * k + cq] : 0.f;
+      for (int i = 0; i < kRowsPerWarp; ++i) {
+        const int cr = colS[warp + (kThreads / 32) * i];
+        const float* row = b.B + (int64_t)cr * k;
+        v[i][0] = (cr < k && cq0 < k) ? row[cq0] : 0.f;
+        v[i][1] = (cr < k && cq1 < k) ? row[cq1] : 0.f;
       }
       load_corr(Es, Rb + (int64_t)s * nn, n2);
       load_corr(Et, Rb + (int64_t)t * nn, n2);
 #pragma unroll
-      for (int i = 0; i < kPer; ++i) {
-        const int e = tid + i * kThreads;
-        Xs[(e / kT) * kLdM + (e % kT)] = v[i];
+      for (int i = 0; i < kRowsPerWarp; ++i) {
+        const int r = warp + (kThreads / 32) * i;
+        Xs[r * kLdM + lane] = v[i][0];
+        Xs[r * kLdM + lane + 32] = v[i][1];
       }
     }
     __syncthreads();
@@ -470,75 +521,88 @@ __global__ void __launch_bounds__(kThreads) gj_apply_kernel(const __grid_constan
     mma_store_acc<false>(Xs, acc);                    // Z
     mma_store_acc<true>(Ys, acc);                     // Z^T
     __syncthreads();
-    for (int r = warp; r < n2; r += nw) {
-      const int cr = table_col(r, sI, sJ, G.g, k), ct = table_col(r, tI, tJ, G.g, k);
-      for (int q = lane; q < n2; q += 32) {
-        const int cq = table_col(q, tI, tJ, G.g, k), cs = table_col(q, sI, sJ, G.g, k);
-        if (cr < k && cq < k) b.B[(int64_t)cr * k + cq] = Xs[r * kLdM + q];
-        if (ct < k && cs < k) b.B[(int64_t)ct * k + cs] = Ys[r * kLdM + q];
+    const int cs0 = colS[lane], cs1 = colS[lane + 32];
+#pragma unroll 2
+    for (int i = 0; i < kRowsPerWarp; ++i) {
+      const int r = warp + (kThreads / 32) * i;
+      const int crS = colS[r], crT = colT[r];
+      if (crS < k) {
+        float* row = b.B + (int64_t)crS * k;
+        if (cq0 < k) row[cq0] = Xs[r * kLdM + lane];
+        if (cq1 < k) row[cq1] = Xs[r * kLdM + lane + 32];
+      }
+      if (crT < k) {
+        float* row = b.B + (int64_t)crT * k;
+        if (cs0 < k) row[cs0] = Ys[r * kLdM + lane];
+        if (cs1 < k) row[cs1] = Ys[r * kLdM + lane + 32];
       }
     }
   } else {
-    const int v = u - npair;
-    const int t = v / nI, i0 = (v - t * nI) * kT;
-    int tI, tJ;
-    rr_pair(br, t, G.nG, tI, tJ);
-    {
-      constexpr int kPer = kT * kT / kThreads;
-      float v[kPer];
+    load_corr(Et, Rb + (int64_t)t * nn, n2);
+    const int c1 = min(nI, c0 + kPanelRun);
+    for (int c = c0; c < c1; ++c) {
+      const int i0 = c * kT;
+      const bool ok0 = i0 + lane < k, ok1 = i0 + lane + 32 < k;
+      float v[kRowsPerWarp][2];
 #pragma unroll
-      for (int ii = 0; ii < kPer; ++ii) {
-        const int e = tid + ii * kThreads;
-        const int r = e / kT, i = e - r * kT;
-        const int cr = r < n2 ? table_col(r, tI, tJ, G.g, k) : k;
-        v[ii] = (cr < k && i0 + i < k) ? b.V[(int64_t)cr * k + i0 + i] : 0.f;
+      for (int i = 0; i < kRowsPerWarp; ++i) {
+        const int cr = colT[warp + (kThreads / 32) * i];
+        const float* row = b.V + (int64_t)cr * k + i0;
+        v[i][0] = (cr < k && ok0) ? row[lane] : 0.f;
+        v[i][1] = (cr < k && ok1) ? row[lane + 32] : 0.f;
       }
-      load_corr(Et, Rb + (int64_t)t * nn, n2);
+      // Xs is free: the previous panel's product ended before the barrier
+      // that preceded its write-back
 #pragma unroll
-      for (int ii = 0; ii < kPer; ++ii) {
-        const int e = tid + ii * kThreads;
-        Xs[(e / kT) * kLdM + (e % kT)] = v[ii];
+      for (int i = 0; i < kRowsPerWarp; ++i) {
+        const int r = warp + (kThreads / 32) * i;
+        Xs[r * kLdM + lane] = v[i][0];
+        Xs[r * kLdM + lane + 32] = v[i][1];
       }
-    }
-    __syncthreads();
-    mma_load_acc<true>(Xs, acc);                      // V rows i, table columns q
-    if (precise) corr_product<3>(Xs, Et, n2, acc);    // V + V E_t
-    else corr_product<1>(Xs, Et, n2, acc);
-    mma_store_acc<true>(Ys, acc);
-    __syncthreads();
-    for (int q = warp; q < n2; q += nw) {
-      const int cq = table_col(q, tI, tJ, G.g, k);
-      if (cq >= k) continue;
-      for (int i = lane; i < kT; i += 32)
-        if (i0 + i < k) b.V[(int64_t)cq * k + i0 + i] = Ys[q * kLdM + i];
+      __syncthreads();
+      mma_load_acc<true>(Xs, acc);                      // V rows i, table columns q
+      if (precise) corr_product<3>(Xs, Et, n2, acc);    // V + V E_t
+      else corr_product<1>(Xs, Et, n2, acc);
+      mma_store_acc<true>(Ys, acc);
+      __syncthreads();
+      for (int q = warp; q < n2; q += kThreads / 32) {
+        const int cq = colT[q];
+        if (cq >= k) continue;
+        float* row = b.V + (int64_t)cq * k + i0;
+        if (ok0) row[lane] = Ys[q * kLdM + lane];
+        if (ok1) row[lane + 32] = Ys[q * kLdM + lane + 32];
+      }
     }
   }
 }
 
 // ---------------------------------------------------------------- control
-// ||off(B)||_F^2 and ||B||_F^2 over chunks of entries.
+// ||off(B)||_F^2 and ||B||_F^2 over this CTA's rows (per-thread fp32
+// partial sums, combined in fp64; the two are summed separately, so off(B)
+// keeps its relative accuracy however small it is).
 __global__ void __launch_bounds__(kThreads) gj_off_kernel(const __grid_constant__ GjArgs a) {
   __shared__ double red[32];
   const int item = blockIdx.y;
   if (!pred_ok(a.ctl[item], kActive)) return;
   const ItemBufs b = bufs_of(a, item);
   const int k = a.k;
-  const int64_t kk2 = (int64_t)k * k;
-  const int64_t per = (kk2 + gridDim.x - 1) / gridDim.x;
-  const int64_t e0 = (int64_t)blockIdx.x * per, e1 = min(kk2, e0 + per);
-  double tot = 0.0, off = 0.0;
-  for (int64_t e = e0 + threadIdx.x; e < e1; e += blockDim.x) {
-    const double v = b.B[e];
-    tot += v * v;
-    const int64_t i = e / k;
-    if (e - i * k != i) off += v * v;
+  const int rows = (k + gridDim.x - 1) / gridDim.x;
+  const int r0 = min(k, (int)blockIdx.x * rows), r1 = min(k, r0 + rows);
+  float tot = 0.f, off = 0.f;
+  for (int i = r0; i < r1; ++i) {
+    const float* row = b.B + (int64_t)i * k;
+    for (int j = threadIdx.x; j < k; j += blockDim.x) {
+      const float v = row[j];
+      tot = fmaf(v, v, tot);
+      if (j != i) off = fmaf(v, v, off);
+    }
   }
-  tot = block_sum_d(tot, red);
+  const double dt = block_sum_d((double)tot, red);
   __syncthreads();
-  off = block_sum_d(off, red);
+  const double doff = block_sum_d((double)off, red);
   if (threadIdx.x == 0) {
-    atomicAdd(&a.ctl[item].tot2, tot);
-    atomicAdd(&a.ctl[item].off2, off);
+    atomicAdd(&a.ctl[item].tot2, dt);
+    atomicAdd(&a.ctl[item].off2, doff);
   }
 }
 
@@ -636,11 +700,29 @@ __global__ void __launch_bounds__(kThreads) gj_finish_kernel(const __grid_consta
       __syncthreads();
     }
   }
-  for (int64_t e = threadIdx.x; e < (int64_t)k * k; e += blockDim.x) {
-    const int64_t i = e / k, j = e - i * k;
-    int p = perm[j];
-    if (p < 0 || p >= k) p = (int)j;  // only reachable with a NaN eigenvalue
-    b.Q[e] = b.V[(int64_t)p * k + i];
+  // Q[i][j] = V(i, perm[j]) = V[perm[j] k + i], through 32 x 32 shared tiles
+  // (placed after lamv and perm) so both sides are coalesced
+  float (*tile)[33] = reinterpret_cast<float (*)[33]>(sm + 2 * kp2);
+  const int nt = (k + 31) / 32;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  for (int tl = 0; tl < nt * nt; ++tl) {
+    const int bj = tl / nt, bi = tl - bj * nt;   // Q columns 32 bj.., rows 32 bi..
+    __syncthreads();
+    for (int jj = ty; jj < 32; jj += kThreads / 32) {
+      const int j = 32 * bj + jj, i = 32 * bi + tx;
+      float v = 0.f;
+      if (j < k && i < k) {
+        int p = perm[j];
+        if (p < 0 || p >= k) p = j;  // only reachable with a NaN eigenvalue
+        v = b.V[(int64_t)p * k + i];
+      }
+      tile[jj][tx] = v;
+    }
+    __syncthreads();
+    for (int ii = ty; ii < 32; ii += kThreads / 32) {
+      const int i = 32 * bi + ii, j = 32 * bj + tx;
+      if (i < k && j < k) b.Q[(int64_t)i * k + j] = tile[tx][ii];
+    }
   }
   for (int j = threadIdx.x; j < k; j += blockDim.x) lam[j] = lamv[j];
   if (threadIdx.x == 0) {
@@ -661,7 +743,7 @@ int64_t gj_rbuf_floats(int k) {
   return (int64_t)G.nT * G.n2 * G.n2;
 }
 
-size_t gj_finish_smem(int k) { return 2 * (size_t)pow2_ceil(k) * sizeof(float); }
+size_t gj_finish_smem(int k) { return (2 * (size_t)pow2_ceil(k) + 32 * 33) * sizeof(float); }
 
 cudaError_t configure_jacobi_grid(size_t smem_limit) {
   cudaError_t e = cudaFuncSetAttribute(gj_apply_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -719,7 +801,7 @@ cudaError_t run_jacobi_grid(const GjArgs* batches, int nb, const cudaStream_t* s
         const Geom& m = gm[b];
         if (host_counts[b] == 0 || br >= m.G.nG - 1) continue;
         gj_table_kernel<<<dim3(m.G.nT, a.nitems), kTableThreads, 0, streams[b]>>>(a, br);
-        gj_apply_kernel<<<dim3(m.npair + m.G.nT * m.nt, a.nitems), kThreads, asm_, streams[b]>>>(a, br);
+        gj_apply_kernel<<<dim3(apply_units(a.k), a.nitems), kThreads, asm_, streams[b]>>>(a, br);
         n += 2;
       }
     }
