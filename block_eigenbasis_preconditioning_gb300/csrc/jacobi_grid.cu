@@ -73,13 +73,13 @@ __device__ __forceinline__ ItemBufs bufs_of(const GjArgs& a, int item) {
 
 // ------------------------------------------------------------------- init
 // V = Q^T-layout copy of the current basis (column j of V = column j of the
-// row-major Q, moved through 32 x 32 shared tiles so both sides are
-// coalesced), ||A||_F^2 and the finiteness of A over this CTA's rows
+// row-major Q, moved through a 32 x 32 shared tile per warp so both sides
+// are coalesced), ||A||_F^2 and the finiteness of A over this CTA's rows
 // (per-thread fp32 partial sums of at most a few hundred terms, combined in
 // fp64).
 __global__ void __launch_bounds__(kThreads) gj_init_kernel(const __grid_constant__ GjArgs a) {
   __shared__ double red[32];
-  __shared__ float tile[32][33];
+  __shared__ float tile[kThreads / 32][32][33];
   const int item = blockIdx.y;
   const ItemBufs b = bufs_of(a, item);
   const int k = a.k;
@@ -95,20 +95,25 @@ __global__ void __launch_bounds__(kThreads) gj_init_kernel(const __grid_constant
       ss = fmaf(v, v, ss);
     }
   }
-  const int nt = (k + 31) / 32;
-  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
-  for (int tl = blockIdx.x; tl < nt * nt; tl += gridDim.x) {
+  // the transpose: one 32 x 32 tile per warp at a time
+  const int nt = (k + 31) / 32, lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  float (*tw)[33] = tile[w];
+  for (int tl = blockIdx.x * (kThreads / 32) + w; tl < nt * nt; tl += gridDim.x * (kThreads / 32)) {
     const int bi = tl / nt, bc = tl - bi * nt;   // Q rows 32 bi.., columns 32 bc..
-    __syncthreads();
-    for (int rr = ty; rr < 32; rr += kThreads / 32) {
-      const int i = 32 * bi + rr, c = 32 * bc + tx;
-      tile[rr][tx] = (i < k && c < k) ? b.Q[(int64_t)i * k + c] : 0.f;
+    const int c = 32 * bc + lane;
+#pragma unroll 8
+    for (int rr = 0; rr < 32; ++rr) {
+      const int i = 32 * bi + rr;
+      tw[rr][lane] = (i < k && c < k) ? b.Q[(int64_t)i * k + c] : 0.f;
     }
-    __syncthreads();
-    for (int rr = ty; rr < 32; rr += kThreads / 32) {
-      const int c = 32 * bc + rr, i = 32 * bi + tx;
-      if (c < k && i < k) b.V[(int64_t)c * k + i] = tile[tx][rr];
+    __syncwarp();
+    const int i = 32 * bi + lane;
+#pragma unroll 8
+    for (int rr = 0; rr < 32; ++rr) {
+      const int cc = 32 * bc + rr;
+      if (cc < k && i < k) b.V[(int64_t)cc * k + i] = tw[lane][rr];
     }
+    __syncwarp();
   }
   const double tot = block_sum_d((double)ss, red);
   bad = __syncthreads_or(bad);
@@ -201,8 +206,9 @@ __global__ void gj_flip_kernel(const __grid_constant__ GjArgs a, int pred) {
 // disjoint column pairs ("slots", at most 32).  In the first round's steps
 // inside each group, a slot has a single member when g is odd; that member
 // is paired with the padding row kPadRow, which holds zeros.  The first warp
-// computes the slots' rotations (lane = slot) into one 16-byte record each;
-// then every thread works through a fixed list of items:
+// computes the slots' rotations (lane = slot) into one 16-byte record each
+// (two record buffers, one per step parity); every thread then works
+// through a fixed list of items:
 //  * S <- J^T S J, block by block.  For each unordered slot pair {X, Y}, the
 //    2 x 2 block of S on their members becomes G_X S_XY G_Y^T (G = [[c, -s],
 //    [s, c]]).  It is written to (X, Y) and mirrored to (Y, X), so every entry
@@ -215,13 +221,15 @@ __global__ void gj_flip_kernel(const __grid_constant__ GjArgs a, int pred) {
 //    per item (float2).
 // Identity rotations (pairs past the block, single members, entries at the
 // floor) leave their entries bit-for-bit unchanged, and the padding row
-// stays zero.  Two barriers per step.
+// stays zero.  Two barriers per step; between them the first warp computes
+// the next step's rotations while the other warps update R.
 constexpr int kLS = 64;        // row stride of S in shared memory
 constexpr int kLR = 66;        // row stride of R^T (even for float2 rows; the transposed read-out is 2-way)
 constexpr int kMaxSlots = 32;
 constexpr int kPadRow = 63;    // partner of a single-member slot (odd g: 2g <= 62)
 constexpr int kBlkPer = (32 * 33 / 2 + kTableThreads - 1) / kTableThreads;  // slot pairs per thread
-constexpr int kRotPer = (32 * 32 + kTableThreads - 1) / kTableThreads;      // R items per thread
+constexpr int kRotThreads = kTableThreads - 32;                              // warps 1.. update R
+constexpr int kRotPer = (32 * 32 + kRotThreads - 1) / kRotThreads;          // R items per thread
 
 struct __align__(16) SlotRec {
   float c, s;
@@ -246,13 +254,14 @@ __device__ __forceinline__ void deal_pairs(int ns, int (&out)[kBlkPer]) {
   }
 }
 
-// This thread's R items among ns slots x nh column pairs, packed X | jj << 8.
-__device__ __forceinline__ void deal_rot(int ns, int nh, int (&out)[kRotPer]) {
+// R items of thread rt (0 .. kRotThreads - 1) among ns slots x nh column
+// pairs, packed X | jj << 8.
+__device__ __forceinline__ void deal_rot(int ns, int nh, int rt, int (&out)[kRotPer]) {
 #pragma unroll
   for (int i = 0; i < kRotPer; ++i) {
-    const int l = threadIdx.x + i * kTableThreads;
+    const int l = rt + i * kRotThreads;
     out[i] = -1;
-    if (l < ns * nh) {
+    if (rt >= 0 && l < ns * nh) {
       const int X = l / nh;
       out[i] = X | ((l - X * nh) << 8);
     }
@@ -263,7 +272,7 @@ __global__ void __launch_bounds__(kTableThreads, 6) gj_table_kernel(const __grid
                                                                     int br) {
   __shared__ __align__(16) float S[64 * kLS];
   __shared__ __align__(16) float Rt[64 * kLR];
-  __shared__ SlotRec sl[kMaxSlots];
+  __shared__ SlotRec sl[2][kMaxSlots];
   const int item = blockIdx.y, tt = blockIdx.x;
   GjCtl* c = a.ctl + item;
   if (!pred_ok(*c, kActive)) return;
@@ -287,63 +296,70 @@ __global__ void __launch_bounds__(kTableThreads, 6) gj_table_kernel(const __grid
   const float bfloor = c->bfloor;
   const int gp = g + (g & 1);
   const int n_intra = br == 0 ? gp - 1 : 0;
-  int blk[kBlkPer], rit[kRotPer];
-  deal_pairs(n_intra ? gp : g, blk);
-  deal_rot(n_intra ? gp : g, g, rit);
-  __syncthreads();
+  const int nsteps = n_intra + g;
   int rots = 0;
-  for (int step = 0; step < n_intra + g; ++step) {
+  // rotations of step `step` into out[lane] (warp 0)
+  auto make_slots = [&](int step, SlotRec* out) {
     const bool intra = step < n_intra;
     const int r = intra ? step : step - n_intra;
-    const int ns = intra ? gp : g;
+    if (lane >= (intra ? gp : g)) return;
+    int p, q;
+    bool single = false;
+    if (intra) {
+      // group grp's round-robin pair; player g is the odd group's dummy
+      const int half = gp >> 1, grp = lane / half, ii = lane - grp * half;
+      int pp, qq;
+      rr_pair(r, ii, gp, pp, qq);
+      if (pp >= g) {
+        pp = qq;
+        single = true;
+      } else if (qq >= g) {
+        single = true;
+      }
+      if (!single && qq < pp) {
+        const int t = pp; pp = qq; qq = t;
+      }
+      p = pp + grp * g;
+      q = single ? kPadRow : qq + grp * g;
+    } else {
+      p = lane;
+      q = g + (lane + r) % g;
+    }
+    float cs = 1.f, sn = 0.f;
+    if (!single && table_col(p, gI, gJ, g, k) < k && table_col(q, gI, gJ, g, k) < k) {
+      const float bpq = S[p * kLS + q];
+      if (fabsf(bpq) > bfloor) {
+        const float ta = (S[q * kLS + q] - S[p * kLS + p]) / (2.f * bpq);
+        const float tn = ta >= 0.f ? 1.f / (ta + sqrtf(1.f + ta * ta)) : -1.f / (-ta + sqrtf(1.f + ta * ta));
+        cs = 1.f / sqrtf(1.f + tn * tn);
+        sn = tn * cs;
+        ++rots;
+      }
+    }
+    out[lane] = SlotRec{cs, sn, p, q};
+  };
+  int blk[kBlkPer], rit[kRotPer];
+  deal_pairs(n_intra ? gp : g, blk);
+  deal_rot(n_intra ? gp : g, g, tid - 32, rit);
+  __syncthreads();   // S and R^T loaded
+  if (warp == 0) make_slots(0, sl[0]);
+  __syncthreads();
+  // per step: S update by all warps on the step's rotations; then warp 0
+  // computes the next step's rotations (into the other record buffer) while
+  // warps 1.. apply this step's to R
+  for (int step = 0; step < nsteps; ++step) {
+    const SlotRec* cur = sl[step & 1];
     if (step == n_intra && n_intra) {
       deal_pairs(g, blk);
-      deal_rot(g, g, rit);
+      deal_rot(g, g, tid - 32, rit);
     }
-    if (warp == 0 && lane < ns) {
-      int p, q;
-      bool single = false;
-      if (intra) {
-        // group grp's round-robin pair; player g is the odd group's dummy
-        const int half = gp >> 1, grp = lane / half, ii = lane - grp * half;
-        int pp, qq;
-        rr_pair(r, ii, gp, pp, qq);
-        if (pp >= g) {
-          pp = qq;
-          single = true;
-        } else if (qq >= g) {
-          single = true;
-        }
-        if (!single && qq < pp) {
-          const int t = pp; pp = qq; qq = t;
-        }
-        p = pp + grp * g;
-        q = single ? kPadRow : qq + grp * g;
-      } else {
-        p = lane;
-        q = g + (lane + r) % g;
-      }
-      float cs = 1.f, sn = 0.f;
-      if (!single && table_col(p, gI, gJ, g, k) < k && table_col(q, gI, gJ, g, k) < k) {
-        const float bpq = S[p * kLS + q];
-        if (fabsf(bpq) > bfloor) {
-          const float ta = (S[q * kLS + q] - S[p * kLS + p]) / (2.f * bpq);
-          const float tn = ta >= 0.f ? 1.f / (ta + sqrtf(1.f + ta * ta)) : -1.f / (-ta + sqrtf(1.f + ta * ta));
-          cs = 1.f / sqrtf(1.f + tn * tn);
-          sn = tn * cs;
-          ++rots;
-        }
-      }
-      sl[lane] = SlotRec{cs, sn, p, q};
-    }
-    __syncthreads();
     // S blocks: the thread's pairs are disjoint from every other thread's
     // (only the zero padding entries are shared, and stay zero)
 #pragma unroll
     for (int i = 0; i < kBlkPer; ++i) {
       const int xy = blk[i];
       if (xy < 0) continue;
-      const SlotRec x = sl[xy & 255], y = sl[xy >> 8];
+      const SlotRec x = cur[xy & 255], y = cur[xy >> 8];
       const float m00 = S[x.p * kLS + y.p], m01 = S[x.p * kLS + y.q];
       const float m10 = S[x.q * kLS + y.p], m11 = S[x.q * kLS + y.q];
       // rows: G_X M
@@ -362,17 +378,22 @@ __global__ void __launch_bounds__(kTableThreads, 6) gj_table_kernel(const __grid
       S[x.q * kLS + y.q] = n11;
       S[y.q * kLS + x.q] = n11;
     }
-    // R^T rows p, q of each slot, two columns per item
+    __syncthreads();
+    if (warp == 0) {
+      if (step + 1 < nsteps) make_slots(step + 1, sl[(step + 1) & 1]);
+    } else {
+      // R^T rows p, q of each slot, two columns per item
 #pragma unroll
-    for (int i = 0; i < kRotPer; ++i) {
-      const int xj = rit[i];
-      if (xj < 0) continue;
-      const SlotRec x = sl[xj & 255];
-      float2* ra = reinterpret_cast<float2*>(Rt + x.p * kLR) + (xj >> 8);
-      float2* rb = reinterpret_cast<float2*>(Rt + x.q * kLR) + (xj >> 8);
-      const float2 u = *ra, v = *rb;
-      *ra = make_float2(x.c * u.x - x.s * v.x, x.c * u.y - x.s * v.y);
-      *rb = make_float2(x.s * u.x + x.c * v.x, x.s * u.y + x.c * v.y);
+      for (int i = 0; i < kRotPer; ++i) {
+        const int xj = rit[i];
+        if (xj < 0) continue;
+        const SlotRec x = cur[xj & 255];
+        float2* ra = reinterpret_cast<float2*>(Rt + x.p * kLR) + (xj >> 8);
+        float2* rb = reinterpret_cast<float2*>(Rt + x.q * kLR) + (xj >> 8);
+        const float2 u = *ra, v = *rb;
+        *ra = make_float2(x.c * u.x - x.s * v.x, x.c * u.y - x.s * v.y);
+        *rb = make_float2(x.s * u.x + x.c * v.x, x.s * u.y + x.c * v.y);
+      }
     }
     __syncthreads();
   }
@@ -700,28 +721,33 @@ __global__ void __launch_bounds__(kThreads) gj_finish_kernel(const __grid_consta
       __syncthreads();
     }
   }
-  // Q[i][j] = V(i, perm[j]) = V[perm[j] k + i], through 32 x 32 shared tiles
-  // (placed after lamv and perm) so both sides are coalesced
-  float (*tile)[33] = reinterpret_cast<float (*)[33]>(sm + 2 * kp2);
-  const int nt = (k + 31) / 32;
-  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
-  for (int tl = 0; tl < nt * nt; ++tl) {
-    const int bj = tl / nt, bi = tl - bj * nt;   // Q columns 32 bj.., rows 32 bi..
-    __syncthreads();
-    for (int jj = ty; jj < 32; jj += kThreads / 32) {
-      const int j = 32 * bj + jj, i = 32 * bi + tx;
-      float v = 0.f;
-      if (j < k && i < k) {
-        int p = perm[j];
-        if (p < 0 || p >= k) p = j;  // only reachable with a NaN eigenvalue
-        v = b.V[(int64_t)p * k + i];
+  // Q[i][j] = V(i, perm[j]) = V[perm[j] k + i], through a 32 x 32 shared
+  // tile per warp (placed after lamv and perm) so both sides are coalesced
+  {
+    const int nt = (k + 31) / 32, lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    float (*tw)[33] = reinterpret_cast<float (*)[33]>(sm + 2 * kp2) + 32 * w;
+    for (int tl = w; tl < nt * nt; tl += kThreads / 32) {
+      const int bj = tl / nt, bi = tl - bj * nt;   // Q columns 32 bj.., rows 32 bi..
+      const int i = 32 * bi + lane;
+#pragma unroll 8
+      for (int jj = 0; jj < 32; ++jj) {
+        const int j = 32 * bj + jj;
+        float v = 0.f;
+        if (j < k && i < k) {
+          int p = perm[j];
+          if (p < 0 || p >= k) p = j;  // only reachable with a NaN eigenvalue
+          v = b.V[(int64_t)p * k + i];
+        }
+        tw[jj][lane] = v;
       }
-      tile[jj][tx] = v;
-    }
-    __syncthreads();
-    for (int ii = ty; ii < 32; ii += kThreads / 32) {
-      const int i = 32 * bi + ii, j = 32 * bj + tx;
-      if (i < k && j < k) b.Q[(int64_t)i * k + j] = tile[tx][ii];
+      __syncwarp();
+      const int j = 32 * bj + lane;
+#pragma unroll 8
+      for (int ii = 0; ii < 32; ++ii) {
+        const int i2 = 32 * bi + ii;
+        if (i2 < k && j < k) b.Q[(int64_t)i2 * k + j] = tw[lane][ii];
+      }
+      __syncwarp();
     }
   }
   for (int j = threadIdx.x; j < k; j += blockDim.x) lam[j] = lamv[j];
@@ -743,7 +769,7 @@ int64_t gj_rbuf_floats(int k) {
   return (int64_t)G.nT * G.n2 * G.n2;
 }
 
-size_t gj_finish_smem(int k) { return (2 * (size_t)pow2_ceil(k) + 32 * 33) * sizeof(float); }
+size_t gj_finish_smem(int k) { return (2 * (size_t)pow2_ceil(k) + (kThreads / 32) * 32 * 33) * sizeof(float); }
 
 cudaError_t configure_jacobi_grid(size_t smem_limit) {
   cudaError_t e = cudaFuncSetAttribute(gj_apply_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
