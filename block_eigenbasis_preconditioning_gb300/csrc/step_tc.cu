@@ -56,6 +56,12 @@ struct TcSmem {
   int abort;
 };
 
+// Reconstruct K steps (16 wide) that one basis stage carries: as many
+// sub-step images of sb bytes as fit the stage.
+__device__ __forceinline__ int recon_per_stage(int bstage, uint32_t sb) {
+  return max(1, bstage / (int)sb);
+}
+
 // mbarrier wait whose outcome is the same on every lane of the warp (the
 // callers run warp-collective tcgen05 instructions right after it).
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
@@ -208,8 +214,10 @@ step_tc_kernel(const __grid_constant__ StepArgs a, const __grid_constant__ TcArg
         int64_t off = 0;
         for (int c0 = 0; c0 < kpN && !aborted(sh); c0 += kUCols) {
           const int nn = min(kUCols, kpN - c0);
-          const uint32_t bytes = (uint32_t)t.rpieces * nn * 32u;
-          for (int s = 0; s < kpN / 16; ++s) {
+          const uint32_t sb = (uint32_t)t.rpieces * nn * 32u;   // one K step's images
+          const int per = recon_per_stage(t.bstage, sb), nsteps = kpN / 16;
+          for (int s = 0; s < nsteps; s += per) {
+            const uint32_t bytes = sb * (uint32_t)min(per, nsteps - s);
             if (!mbar_wait(&sh->b_empty[bs], bp ^ 1)) { raise(sh, t.err, 3); return; }
             mbar_arrive_expect_tx(&sh->b_full[bs], bytes);
             bulk_load(b_buf + bs * t.bstage, qr + off, bytes, &sh->b_full[bs]);
@@ -273,14 +281,19 @@ step_tc_kernel(const __grid_constant__ StepArgs a, const __grid_constant__ TcArg
         tc_fence_after();
         const uint32_t idr = instr_desc(1, kTM, nn);
         const uint32_t d = tmem + 256 + kUCols * b;
-        for (int s = 0; s < kpN / 16; ++s) {
+        const uint32_t sb = (uint32_t)t.rpieces * nn * 32u;
+        const int per = recon_per_stage(t.bstage, sb), nsteps = kpN / 16;
+        for (int s = 0; s < nsteps; s += per) {
+          const int cnt = min(per, nsteps - s);
           if (!warp_wait(&sh->b_full[bs], bp)) { raise(sh, t.err, 7); return false; }
           tc_fence_after();
           if (lane == 0) {
-            const uint32_t b_hi = smem_u32(b_buf + bs * t.bstage);
-            for (int p = 0; p < t.rpieces; ++p)
-              mma_f16_ts(d, tmem + cb + 8 * s, smem_desc(b_hi + p * nn * 32, 16, 256, kSw32), idr,
-                         (s == 0 && p == 0) ? 0u : 1u);
+            for (int u = 0; u < cnt; ++u) {
+              const uint32_t b_hi = smem_u32(b_buf + bs * t.bstage) + (uint32_t)u * sb;
+              for (int p = 0; p < t.rpieces; ++p)
+                mma_f16_ts(d, tmem + cb + 8 * (s + u), smem_desc(b_hi + p * nn * 32, 16, 256, kSw32), idr,
+                           (s + u == 0 && p == 0) ? 0u : 1u);
+            }
             tc_commit(&sh->b_empty[bs]);
           }
           __syncwarp();
