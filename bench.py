@@ -741,6 +741,29 @@ def _flat(torch, like, device=None, pin=False):
     return buf, views
 
 
+def _bind_to_gpu_local_cpus(torch):
+    """Run this process on the host cores attached to the current GPU, so that
+    pinned buffers allocated meanwhile land in that socket's memory (a
+    buffer on the other socket crosses the socket link on every copy).
+    Returns the previous affinity; best effort on systems that do not expose
+    the GPU's local CPUs."""
+    prev = os.sched_getaffinity(0)
+    try:
+        props = torch.cuda.get_device_properties(torch.cuda.current_device())
+        bus = "%04x:%02x:%02x.0" % (props.pci_domain_id, props.pci_bus_id, props.pci_device_id)
+        with open(f"/sys/bus/pci/devices/{bus}/local_cpulist") as f:
+            spec = f.read().strip()
+        cpus = set()
+        for part in spec.split(","):
+            lo, _, hi = part.partition("-")
+            cpus.update(range(int(lo), int(hi or lo) + 1))
+        if cpus:
+            os.sched_setaffinity(0, cpus)
+    except Exception:
+        pass
+    return prev
+
+
 def run_e2e(torch, opt, cfg, shapes, lay, sides, W, K, stream, params, world):
     """End to end through the public API with host buffers.  Every step
     copies that step's activations and gradients from pinned host memory
@@ -755,6 +778,7 @@ def run_e2e(torch, opt, cfg, shapes, lay, sides, W, K, stream, params, world):
     dev = W[0].device
     Xs2, Gs2, _ = make_train_inputs(torch, dict(cfg, pool=2), shapes, lay, dev, seed=777,
                                     pool=2, sides=sides)
+    prev_cpus = _bind_to_gpu_local_cpus(torch)
     Xh, Gh = [], []
     for s2 in range(2):
         hb, hv = _flat(torch, Xs2[s2], pin=True)
@@ -774,6 +798,18 @@ def run_e2e(torch, opt, cfg, shapes, lay, sides, W, K, stream, params, world):
         v.copy_(w)
     Wh = torch.empty_like(Wd_buf, device="cpu").pin_memory()
     link = host_link_rates(torch)
+    os.sched_setaffinity(0, prev_cpus)
+    # the rate of one copy of a step's flat activation buffer (best of 3)
+    best = 0.0
+    for _ in range(3):
+        ef0, ef1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        ef0.record(stream)
+        Xd[0][0].copy_(Xh[0], non_blocking=True)
+        ef1.record(stream)
+        torch.cuda.synchronize()
+        best = max(best, Xh[0].numel() * Xh[0].element_size() / (ef0.elapsed_time(ef1) * 1e-3) / 1e9)
+    link["h2d_flat_x_gbs"] = best
     h2d = Xh[0].numel() * Xh[0].element_size() + Gh[0].numel() * Gh[0].element_size()
     d2h = Wh.numel() * Wh.element_size()
     cx, cg, cw = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
