@@ -429,30 +429,11 @@ dobb_status do_pack(dobb_handle h, cudaStream_t s) {
   return DOBB_OK;
 }
 
-dobb_status do_refresh_orth(dobb_handle h, cudaStream_t s) {
-  for (const Chunk& ch : h->wl.chunks) {
-    if (ch.eig_n == 0) continue;
-    EigArgs a{};
-    a.info = h->dinfo();
-    a.tiles = h->dtiles() + ch.eig_off;
-    a.num_tiles = ch.eig_n;
-    a.A = h->A();
-    a.Q = h->Q();
-    a.lam = h->lam();
-    a.scratch = h->scratch();
-    a.flags = h->flags();
-    a.stats = h->stats();
-    const int g = std::max(1, std::min(ch.eig_n, h->sm_count));
-    cudaError_t e = launch_orth(a, h->orth_steps, g, s);
-    if (e != cudaSuccess) return fail(DOBB_ERR_CUDA, "orthogonal-iteration launch: %s", cudaGetErrorString(e));
-    ++h->launches;
-  }
-  return do_pack(h, s);
-}
-
-// Run grid-eigensolver batches: batch i on the caller's stream (i % 3 == 0)
-// or one of the handle's two streams, joined back into the caller's stream.
-cudaError_t run_grid_batches(dobb_handle h, const GjArgs* batches, int nb, cudaStream_t s) {
+// Run grid batches (the eigensolver, or the orthogonal iteration when
+// orth_steps > 0): batch i on the caller's stream (i % 3 == 0) or one of the
+// handle's two streams, joined back into the caller's stream.
+cudaError_t run_grid_batches(dobb_handle h, const GjArgs* batches, int nb, cudaStream_t s,
+                             int orth_steps) {
   if (nb <= 0) return cudaSuccess;
   cudaStream_t streams[kGjMaxBatches];
   const int nstreams = std::min(nb, kGjStreams + 1);
@@ -464,13 +445,106 @@ cudaError_t run_grid_batches(dobb_handle h, const GjArgs* batches, int nb, cudaS
       e = cudaStreamWaitEvent(h->gj_streams[i - 1], h->gj_events[0], 0);
     if (e != cudaSuccess) return e;
   }
-  e = run_jacobi_grid(batches, nb, streams, h->gj_host_counts, &h->launches);
+  e = orth_steps > 0 ? run_orth_grid(batches, nb, streams, orth_steps, h->sm_count, &h->launches)
+                     : run_jacobi_grid(batches, nb, streams, h->gj_host_counts, &h->launches);
   for (int i = 1; i < nstreams; ++i) {
     cudaError_t e2 = cudaEventRecord(h->gj_events[i], h->gj_streams[i - 1]);
     if (e2 == cudaSuccess) e2 = cudaStreamWaitEvent(s, h->gj_events[i], 0);
     if (e == cudaSuccess) e = e2;
   }
   return e;
+}
+
+// The blocks of chunk ch at least gj_min_k wide (the front of its list,
+// sorted by decreasing k) on the grid, with the eigensolver (orth_steps = 0)
+// or the orthogonal iteration.  Batches are runs of one width, split by the
+// byte budget, or in two when no budget is set and the width has many blocks
+// (two batches of one width interleave their latency-bound and
+// bandwidth-bound launches).  Sets *g_end to the first block left for the
+// one-CTA kernels.
+dobb_status grid_refresh(dobb_handle h, const Chunk& ch, cudaStream_t s, int orth_steps, int* g_end) {
+  const Tile* items = h->wl.tiles.data() + ch.eig_off;
+  auto kof = [&](int idx) { return (int)(h->n[items[idx].mat] / h->B); };
+  const char* what = orth_steps > 0 ? "grid orthogonal iteration" : "grid eigensolver";
+  int g0 = 0;
+  if (h->gj_min_k > 0) {
+    GjArgs batches[kGjMaxBatches];
+    int nb = 0;
+    int64_t ctl_off = 0, rbuf_off = 0;
+    while (g0 < ch.eig_n && kof(g0) >= h->gj_min_k) {
+      const int k = kof(g0);
+      int g1 = g0;
+      while (g1 < ch.eig_n && kof(g1) == k) ++g1;
+      const int count = g1 - g0;
+      int per = std::min(count, gj_batch_items(k, h->gj_batch_bytes));
+      if (h->gj_batch_bytes == 0 && count >= 64) per = (count + 1) / 2;
+      for (int b0 = g0; b0 < g1; b0 += per) {
+        const int nitems = std::min(per, g1 - b0);
+        if (nb == kGjMaxBatches) {
+          cudaError_t e = run_grid_batches(h, batches, nb, s, orth_steps);
+          if (e != cudaSuccess) return fail(DOBB_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+          nb = 0;
+          ctl_off = rbuf_off = 0;
+        }
+        if ((size_t)(ctl_off + nitems) > h->L.gj_ctl_items ||
+            (size_t)(rbuf_off + (int64_t)nitems * gj_rbuf_floats(k)) > h->L.gj_rbuf_floats)
+          return fail(DOBB_ERR_STATE, "grid eigensolver buffers too small for width %d", k);
+        GjArgs& ga = batches[nb];
+        ga = GjArgs{};
+        ga.info = h->dinfo();
+        ga.items = h->dtiles() + ch.eig_off + b0;
+        ga.nitems = nitems;
+        ga.k = k;
+        ga.A = h->A();
+        ga.Q = h->Q();
+        ga.lam = h->lam();
+        ga.scratch = h->scratch();
+        ga.rbuf = h->gj_rbuf() + rbuf_off;
+        ga.rstride = gj_rbuf_floats(k);
+        ga.ctl = h->gj_ctl() + ctl_off;
+        ga.active_count = h->gj_count() + nb;
+        ga.flags = h->flags();
+        ga.stats = h->stats();
+        ga.max_sweeps = h->max_sweeps;
+        ga.tol = h->tol;
+        ctl_off += nitems;
+        rbuf_off += (int64_t)nitems * gj_rbuf_floats(k);
+        ++nb;
+      }
+      g0 = g1;
+    }
+    cudaError_t e = run_grid_batches(h, batches, nb, s, orth_steps);
+    if (e != cudaSuccess) return fail(DOBB_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+  }
+  *g_end = g0;
+  return DOBB_OK;
+}
+
+// Orthogonal iteration: blocks at least gj_min_k wide on the grid, the rest
+// one CTA per block.
+dobb_status do_refresh_orth(dobb_handle h, cudaStream_t s) {
+  for (const Chunk& ch : h->wl.chunks) {
+    if (ch.eig_n == 0) continue;
+    int g0 = 0;
+    dobb_status st = grid_refresh(h, ch, s, h->orth_steps, &g0);
+    if (st != DOBB_OK) return st;
+    if (g0 >= ch.eig_n) continue;
+    EigArgs a{};
+    a.info = h->dinfo();
+    a.tiles = h->dtiles() + ch.eig_off + g0;
+    a.num_tiles = ch.eig_n - g0;
+    a.A = h->A();
+    a.Q = h->Q();
+    a.lam = h->lam();
+    a.scratch = h->scratch();
+    a.flags = h->flags();
+    a.stats = h->stats();
+    const int g = std::max(1, std::min(a.num_tiles, h->sm_count));
+    cudaError_t e = launch_orth(a, h->orth_steps, g, s);
+    if (e != cudaSuccess) return fail(DOBB_ERR_CUDA, "orthogonal-iteration launch: %s", cudaGetErrorString(e));
+    ++h->launches;
+  }
+  return do_pack(h, s);
 }
 
 dobb_status do_refresh(dobb_handle h, cudaStream_t s) {
@@ -483,58 +557,8 @@ dobb_status do_refresh(dobb_handle h, cudaStream_t s) {
     const Tile* items = h->wl.tiles.data() + ch.eig_off;
     auto kof = [&](int idx) { return (int)(h->n[items[idx].mat] / h->B); };
     int g0 = 0;
-    if (h->gj_min_k > 0) {
-      // batches: runs of one width, split by the byte budget, or in two when
-      // no budget is set and the width has many blocks (two batches of one
-      // width interleave their table solves and tile products)
-      GjArgs batches[kGjMaxBatches];
-      int nb = 0;
-      int64_t ctl_off = 0, rbuf_off = 0;
-      while (g0 < ch.eig_n && kof(g0) >= h->gj_min_k) {
-        const int k = kof(g0);
-        int g1 = g0;
-        while (g1 < ch.eig_n && kof(g1) == k) ++g1;
-        const int count = g1 - g0;
-        int per = std::min(count, gj_batch_items(k, h->gj_batch_bytes));
-        if (h->gj_batch_bytes == 0 && count >= 64) per = (count + 1) / 2;
-        for (int b0 = g0; b0 < g1; b0 += per) {
-          const int nitems = std::min(per, g1 - b0);
-          if (nb == kGjMaxBatches) {
-            cudaError_t e = run_grid_batches(h, batches, nb, s);
-            if (e != cudaSuccess) return fail(DOBB_ERR_CUDA, "grid eigensolver: %s", cudaGetErrorString(e));
-            nb = 0;
-            ctl_off = rbuf_off = 0;
-          }
-          if ((size_t)(ctl_off + nitems) > h->L.gj_ctl_items ||
-              (size_t)(rbuf_off + (int64_t)nitems * gj_rbuf_floats(k)) > h->L.gj_rbuf_floats)
-            return fail(DOBB_ERR_STATE, "grid eigensolver buffers too small for width %d", k);
-          GjArgs& ga = batches[nb];
-          ga = GjArgs{};
-          ga.info = h->dinfo();
-          ga.items = h->dtiles() + ch.eig_off + b0;
-          ga.nitems = nitems;
-          ga.k = k;
-          ga.A = h->A();
-          ga.Q = h->Q();
-          ga.lam = h->lam();
-          ga.scratch = h->scratch();
-          ga.rbuf = h->gj_rbuf() + rbuf_off;
-          ga.rstride = gj_rbuf_floats(k);
-          ga.ctl = h->gj_ctl() + ctl_off;
-          ga.active_count = h->gj_count() + nb;
-          ga.flags = h->flags();
-          ga.stats = h->stats();
-          ga.max_sweeps = h->max_sweeps;
-          ga.tol = h->tol;
-          ctl_off += nitems;
-          rbuf_off += (int64_t)nitems * gj_rbuf_floats(k);
-          ++nb;
-        }
-        g0 = g1;
-      }
-      cudaError_t e = run_grid_batches(h, batches, nb, s);
-      if (e != cudaSuccess) return fail(DOBB_ERR_CUDA, "grid eigensolver: %s", cudaGetErrorString(e));
-    }
+    dobb_status st = grid_refresh(h, ch, s, 0, &g0);
+    if (st != DOBB_OK) return st;
     int b = g0;
     while (b < ch.eig_n && jacobi_smem_for(kof(b), half) == 0) ++b;
     EigArgs a{};

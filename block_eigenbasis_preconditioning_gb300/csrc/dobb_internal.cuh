@@ -92,6 +92,8 @@ struct SyrkTcArgs {
   CUtensorMap maps[kMaxSyrkTcMat];
 };
 
+struct GjCtl;
+
 struct EigArgs {
   const MatInfo* info;
   const Tile* tiles;
@@ -104,6 +106,7 @@ struct EigArgs {
   uint32_t* flags;
   float* stats;
   float tol;              // relative off-diagonal norm of the last sweep's B (0 = default)
+  const GjCtl* ctl;       // orthogonal iteration: only the items a grid pass left (see orth.cu)
 };
 
 // Grid eigensolver (jacobi_grid.cu): control record of one block, 64 bytes.
@@ -112,7 +115,7 @@ struct GjCtl {
   int32_t fresh;     // B was formed by Rayleigh-Ritz before the current sweep
   int32_t restart;   // Newton-Schulz + Rayleigh-Ritz due after this sweep
   int32_t sweeps;
-  int32_t conv;
+  int32_t conv;      // Jacobi: converged; orthogonal iteration: the grid pass holds
   int32_t rot;       // rotations of the current sweep
   int32_t last_rot;
   int32_t skip;      // A non-finite: basis kept
@@ -156,6 +159,11 @@ cudaError_t configure_jacobi_grid(size_t smem_limit);
 // streams once per sweep
 cudaError_t run_jacobi_grid(const GjArgs* batches, int nb, const cudaStream_t* streams,
                             int* host_counts, int64_t* launches);
+// the orthogonal-iteration refresh of nb batches on the grid (batch b on
+// streams[b]), blocks whose Gram matrix is not numerically positive definite
+// redone by orth.cu; no host synchronisation
+cudaError_t run_orth_grid(const GjArgs* batches, int nb, const cudaStream_t* streams, int steps,
+                          int sm_count, int64_t* launches);
 
 // Coefficient normalisation of the FP32 update kernel.
 constexpr int32_t kModeSign = 0;

@@ -37,6 +37,7 @@ constexpr int kThreads = 256;
 #include "fp32_tiles.cuh"
 #include "jacobi_common.cuh"
 #include "mma_tf32.cuh"
+#include "cholqr.cuh"
 static_assert(kThreads == kTileThreads, "the tile products assume 256 threads");
 
 constexpr int kTableThreads = 128;   // a table: one team of four warps
@@ -759,6 +760,121 @@ __global__ void __launch_bounds__(kThreads) gj_finish_kernel(const __grid_consta
   }
 }
 
+// ---------------------------------------------------- orthogonal iteration
+// The grid form of the orthogonal-iteration refresh of orth.cu ("Dobb",
+// Table 15: one orthogonal-iteration step per refresh; Table 16: Cholesky
+// QR): per step T = A V, then two Cholesky QR passes (G = X^T X,
+// L = chol(G), V = X L^{-T}), then Lambda_j = v_j^T A v_j and Q = V in the
+// column order of the previous basis.  The products are 64 x 64 output tiles
+// of the whole batch (one CTA each), the Cholesky factorisation one CTA per
+// block, the triangular solve one CTA per 64-row panel.  A block whose Gram
+// matrix is not numerically positive definite drops out (ctl.conv = 0, its
+// basis untouched) and is redone from its old basis by orth.cu's shifted
+// passes.  Buffers: V (the basis) in V0, T in V1, G and L in B.
+enum OgProd : int { kOgAV = 0, kOgGramT = 1, kOgGramV = 2 };
+
+__device__ __forceinline__ bool og_ok(const GjCtl& c) { return !c.skip && c.conv; }
+
+__global__ void og_start_kernel(const __grid_constant__ GjArgs a) {
+  const int item = blockIdx.x * blockDim.x + threadIdx.x;
+  if (item >= a.nitems) return;
+  GjCtl& c = a.ctl[item];
+  if (c.skip) {
+    const Tile t = a.items[item];
+    atomicOr(a.flags + a.info[t.mat].blk0 + t.blk, (uint32_t)DOBB_FLAG_NONFINITE_A);
+  }
+  c.conv = c.skip ? 0 : 1;
+}
+
+__global__ void __launch_bounds__(kThreads) og_gemm_kernel(const __grid_constant__ GjArgs a, int prod) {
+  extern __shared__ __align__(16) float gs[];
+  const int item = blockIdx.y;
+  if (!og_ok(a.ctl[item])) return;
+  const int k = a.k;
+  const int nt = (k + kT - 1) / kT;
+  const int ti = blockIdx.x % nt, tj = blockIdx.x / nt;
+  if (prod != kOgAV && ti > tj) return;
+  const ItemBufs b = bufs_of(a, item);
+  if (prod == kOgAV)          // T (in W) = A V
+    gemm_tile<false>(b.A, b.V, b.W, nullptr, 1.f, false, false, k, ti, tj, gs);
+  else if (prod == kOgGramT)  // G (in B) = T^T T
+    gemm_tile<true>(b.W, b.W, b.B, nullptr, 1.f, false, true, k, ti, tj, gs);
+  else                        // G (in B) = V^T V
+    gemm_tile<true>(b.V, b.V, b.B, nullptr, 1.f, false, true, k, ti, tj, gs);
+}
+
+// L = chol(G) in place, one CTA per block.
+__global__ void __launch_bounds__(kThreads, 2) og_chol_kernel(const __grid_constant__ GjArgs a) {
+  extern __shared__ __align__(16) float sm[];
+  __shared__ int s_ok;
+  const int item = blockIdx.x;
+  GjCtl* c = a.ctl + item;
+  if (!og_ok(*c)) return;
+  const ItemBufs b = bufs_of(a, item);
+  if (!chol_lower(b.B, a.k, sm, &s_ok) && threadIdx.x == 0) c->conv = 0;
+}
+
+// V = X L^{-T} for the rows of this CTA's 64-row panel (X = T or V itself).
+__global__ void __launch_bounds__(kThreads, 2) og_trsm_kernel(const __grid_constant__ GjArgs a, int from_t) {
+  extern __shared__ __align__(16) float sm[];
+  const int item = blockIdx.y;
+  if (!og_ok(a.ctl[item])) return;
+  const int k = a.k, i0 = blockIdx.x * kT;
+  if (i0 >= k) return;
+  const ItemBufs b = bufs_of(a, item);
+  trsm_rows(from_t ? b.W : b.V, b.V, b.B, k, i0, sm);
+}
+
+// Lambda_j = v_j . (A v_j), a warp per column (T = A V in W).
+__global__ void og_lambda_kernel(const __grid_constant__ GjArgs a) {
+  const int item = blockIdx.y;
+  if (!og_ok(a.ctl[item])) return;
+  const int k = a.k, lane = threadIdx.x & 31;
+  const int j = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (j >= k) return;
+  const ItemBufs b = bufs_of(a, item);
+  const Tile t = a.items[item];
+  float d = 0.f;
+  for (int i = lane; i < k; i += 32) d = fmaf(b.V[(int64_t)j * k + i], b.W[(int64_t)j * k + i], d);
+  d = warp_sum(d);
+  if (lane == 0) a.lam[b.mi->lam_off + (int64_t)t.blk * k + j] = d;
+}
+
+// Q row-major from V (one 32 x 32 shared tile per warp), and the stats.
+__global__ void __launch_bounds__(kThreads) og_finish_kernel(const __grid_constant__ GjArgs a, int steps) {
+  __shared__ float tile[kThreads / 32][32][33];
+  const int item = blockIdx.y;
+  if (!og_ok(a.ctl[item])) return;
+  const ItemBufs b = bufs_of(a, item);
+  const int k = a.k, nt = (k + 31) / 32, lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  float (*tw)[33] = tile[w];
+  for (int tl = blockIdx.x * (kThreads / 32) + w; tl < nt * nt; tl += gridDim.x * (kThreads / 32)) {
+    const int bj = tl / nt, bi = tl - bj * nt;   // Q columns 32 bj.., rows 32 bi..
+    const int i = 32 * bi + lane;
+#pragma unroll 8
+    for (int jj = 0; jj < 32; ++jj) {
+      const int j = 32 * bj + jj;
+      tw[jj][lane] = (j < k && i < k) ? b.V[(int64_t)j * k + i] : 0.f;
+    }
+    __syncwarp();
+    const int j = 32 * bj + lane;
+#pragma unroll 8
+    for (int ii = 0; ii < 32; ++ii) {
+      const int i2 = 32 * bi + ii;
+      if (i2 < k && j < k) b.Q[(int64_t)i2 * k + j] = tw[lane][ii];
+    }
+    __syncwarp();
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    const Tile t = a.items[item];
+    float* st = a.stats + 4 * (int64_t)(b.mi->blk0 + t.blk);
+    st[2] = (float)steps;
+    st[3] = 0.f;   // shifted Cholesky QR passes: none on this path
+  }
+}
+
+size_t chol_smem() { return 3 * (size_t)kT * kLd * sizeof(float); }
+
 size_t apply_smem() { return 3 * (size_t)kT * kLdM * sizeof(float); }
 size_t gemm_smem() { return (size_t)kGemmFloats * sizeof(float); }
 
@@ -774,6 +890,10 @@ size_t gj_finish_smem(int k) { return (2 * (size_t)pow2_ceil(k) + (kThreads / 32
 cudaError_t configure_jacobi_grid(size_t smem_limit) {
   cudaError_t e = cudaFuncSetAttribute(gj_apply_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)apply_smem());
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(og_chol_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)chol_smem());
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(og_trsm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)chol_smem());
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(gj_finish_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)std::min<size_t>(smem_limit, gj_finish_smem(kMaxK)));
@@ -868,6 +988,59 @@ cudaError_t run_jacobi_grid(const GjArgs* batches, int nb, const cudaStream_t* s
     gj_flip_kernel<<<m.ctl_blocks, 256, 0, s>>>(a, kAlways);
     gj_finish_kernel<<<a.nitems, kThreads, gj_finish_smem(a.k), s>>>(a);
     n += 5;
+  }
+  if (launches) *launches += n;
+  return cudaGetLastError();
+}
+
+// The orthogonal-iteration refresh of nb batches (batch b on streams[b]),
+// each followed on its stream by orth.cu's one-CTA pass over the blocks the
+// grid pass left.  No host synchronisation.
+cudaError_t run_orth_grid(const GjArgs* batches, int nb, const cudaStream_t* streams, int steps,
+                          int sm_count, int64_t* launches) {
+  const size_t gsm = gemm_smem(), csm = chol_smem();
+  int64_t n = 0;
+  for (int b = 0; b < nb; ++b) {
+    const GjArgs& a = batches[b];
+    const cudaStream_t s = streams[b];
+    const int nt = (a.k + kT - 1) / kT;
+    const dim3 tiles(nt * nt, a.nitems), panels(nt, a.nitems);
+    const int chunks = (int)std::max<int64_t>(1, std::min<int64_t>(256, (int64_t)a.k * a.k / (64 * 1024)));
+    const dim3 cgrid(chunks, a.nitems);
+    const int ctl_blocks = (a.nitems + 255) / 256;
+    cudaError_t e = cudaMemsetAsync(a.ctl, 0, sizeof(GjCtl) * (size_t)a.nitems, s);
+    if (e != cudaSuccess) return e;
+    gj_init_kernel<<<cgrid, kThreads, 0, s>>>(a);
+    og_start_kernel<<<ctl_blocks, 256, 0, s>>>(a);
+    n += 2;
+    for (int st = 0; st < steps; ++st) {
+      og_gemm_kernel<<<tiles, kThreads, gsm, s>>>(a, kOgAV);
+      og_gemm_kernel<<<tiles, kThreads, gsm, s>>>(a, kOgGramT);
+      og_chol_kernel<<<a.nitems, kThreads, csm, s>>>(a);
+      og_trsm_kernel<<<panels, kThreads, csm, s>>>(a, 1);
+      og_gemm_kernel<<<tiles, kThreads, gsm, s>>>(a, kOgGramV);   // Cholesky QR2
+      og_chol_kernel<<<a.nitems, kThreads, csm, s>>>(a);
+      og_trsm_kernel<<<panels, kThreads, csm, s>>>(a, 0);
+      n += 7;
+    }
+    og_gemm_kernel<<<tiles, kThreads, gsm, s>>>(a, kOgAV);
+    og_lambda_kernel<<<dim3((a.k + 7) / 8, a.nitems), 256, 0, s>>>(a);
+    og_finish_kernel<<<cgrid, kThreads, 0, s>>>(a, steps);
+    n += 3;
+    EigArgs ea{};
+    ea.info = a.info;
+    ea.tiles = a.items;
+    ea.num_tiles = a.nitems;
+    ea.A = a.A;
+    ea.Q = a.Q;
+    ea.lam = a.lam;
+    ea.scratch = a.scratch;
+    ea.flags = a.flags;
+    ea.stats = a.stats;
+    ea.ctl = a.ctl;
+    e = launch_orth(ea, steps, std::max(1, std::min(a.nitems, sm_count)), s);
+    if (e != cudaSuccess) return e;
+    ++n;
   }
   if (launches) *launches += n;
   return cudaGetLastError();

@@ -39,118 +39,12 @@ constexpr int kThreads = 256;
 #include "fp32_tiles.cuh"
 static_assert(kThreads == kTileThreads, "the tile products assume 256 threads");
 
+#include "cholqr.cuh"
+
 constexpr float kEps = 5.9604645e-8f;  // 2^-24
-constexpr int kPW = 32;                // panel width of the Cholesky and the triangular solve
 constexpr int kMaxShifted = 8;         // shifted passes before a block gives up
 // shared memory: diagonal tile (64 x kLd) + two staging tiles / product stages
 constexpr int kOrthSmemFloats = kT * kLd + std::max(2 * kT * kLd, kGemmFloats);
-
-// In-panel forward substitution for one row held in registers:
-// w <- w L^{-T}, L = the kPW x kPW lower diagonal tile D (row stride kLd,
-// identity beyond the panel width), i.e. solve L y = w.
-__device__ __forceinline__ void row_forward_solve(float (&w)[kPW], const float* D) {
-#pragma unroll
-  for (int c = 0; c < kPW; ++c) {
-    const float y = w[c] / D[c * kLd + c];
-    w[c] = y;
-#pragma unroll
-    for (int q = c + 1; q < kPW; ++q) w[q] = fmaf(-y, D[q * kLd + c], w[q]);
-  }
-}
-
-// Load the lower triangle of the diagonal tile G[j0 : j0+jb, j0 : j0+jb]
-// (column-major lower storage) into D, identity beyond jb.
-__device__ void load_diag(float* D, const float* G, int k, int j0, int jb) {
-  for (int e = threadIdx.x; e < kPW * kPW; e += blockDim.x) {
-    const int r = e / kPW, c = e - r * kPW;
-    float v = 0.f;
-    if (r < jb && c < jb) {
-      if (c <= r) v = G[(int64_t)(j0 + c) * k + j0 + r];
-    } else if (r == c) {
-      v = 1.f;
-    }
-    D[r * kLd + c] = v;
-  }
-}
-
-// Cholesky G = L L^T in place (L lower, column-major: L(i, j) at G[j k + i]).
-// Only the lower triangle of G is read.  Returns false (uniformly) when a
-// pivot is not positive or not finite.
-__device__ bool chol_lower(float* G, int k, float* sm, int* s_ok) {
-  const int tid = threadIdx.x;
-  float* D = sm;
-  float* Pa = sm + kT * kLd;
-  float* Pb = Pa + kT * kLd;
-  if (tid == 0) *s_ok = 1;
-  for (int j0 = 0; j0 < k; j0 += kPW) {
-    const int jb = min(kPW, k - j0);
-    __syncthreads();
-    load_diag(D, G, k, j0, jb);
-    __syncthreads();
-    // (1) unblocked factor of the diagonal tile
-    for (int c = 0; c < jb; ++c) {
-      if (tid == 0) {
-        const float d = D[c * kLd + c];
-        if (!(d > 0.f) || !isfinite(d)) *s_ok = 0;
-        D[c * kLd + c] = sqrtf(fmaxf(d, 0.f));
-      }
-      __syncthreads();
-      if (!*s_ok) return false;
-      const float dc = D[c * kLd + c];
-      for (int r = c + 1 + tid; r < jb; r += blockDim.x) D[r * kLd + c] /= dc;
-      __syncthreads();
-      const int m = jb - c - 1;  // trailing size
-      for (int e = tid; e < m * m; e += blockDim.x) {
-        const int r = c + 1 + e / m, q = c + 1 + e % m;
-        if (q <= r) D[r * kLd + q] = fmaf(-D[r * kLd + c], D[q * kLd + c], D[r * kLd + q]);
-      }
-      __syncthreads();
-    }
-    for (int e = tid; e < jb * jb; e += blockDim.x) {
-      const int r = e / jb, c = e - r * jb;
-      if (c <= r) G[(int64_t)(j0 + c) * k + j0 + r] = D[r * kLd + c];
-    }
-    // (2) the panel below: row r solves x L_jj^T = g_r
-    for (int r = j0 + jb + tid; r < k; r += blockDim.x) {
-      float w[kPW];
-#pragma unroll
-      for (int c = 0; c < kPW; ++c) w[c] = c < jb ? G[(int64_t)(j0 + c) * k + r] : 0.f;
-      row_forward_solve(w, D);
-#pragma unroll
-      for (int c = 0; c < kPW; ++c)
-        if (c < jb) G[(int64_t)(j0 + c) * k + r] = w[c];
-    }
-    __syncthreads();
-    // (3) trailing lower triangle: G[r, q] -= sum_c L[r, j0 + c] L[q, j0 + c]
-    const int t0 = j0 + jb;
-    const int nt = (k - t0 + kT - 1) / kT;
-    for (int tile = 0; tile < nt * nt; ++tile) {
-      const int ti = tile % nt, tj = tile / nt;
-      if (ti < tj) continue;
-      const int i0 = t0 + ti * kT, q0 = t0 + tj * kT;
-      for (int e = tid; e < kT * kT; e += blockDim.x) {
-        const int c = e / kT, i = e - c * kT;
-        Pa[c * kLd + i] = (c < jb && i0 + i < k) ? G[(int64_t)(j0 + c) * k + i0 + i] : 0.f;
-        Pb[c * kLd + i] = (c < jb && q0 + i < k) ? G[(int64_t)(j0 + c) * k + q0 + i] : 0.f;
-      }
-      __syncthreads();
-      float acc[4][4];
-      zero_acc(acc);
-      micro_tn(Pa, Pb, kLd, jb, acc);
-      const int tx = tid & 15, ty = tid >> 4;
-#pragma unroll
-      for (int a = 0; a < 4; ++a)
-#pragma unroll
-        for (int b = 0; b < 4; ++b) {
-          const int r = i0 + 4 * ty + a, q = q0 + 4 * tx + b;
-          if (r < k && q < k && q <= r) G[(int64_t)q * k + r] -= acc[a][b];
-        }
-      __syncthreads();
-    }
-  }
-  __syncthreads();
-  return true;
-}
 
 // Y = X L^{-T} (X, Y k x k column-major; Y may alias X): row r of Y solves
 // L y_r^T = x_r^T.  L lower in G (column-major).
@@ -228,6 +122,9 @@ orth_kernel(const __grid_constant__ EigArgs a, int steps) {
   __shared__ int s_ok;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
   for (int w = blockIdx.x; w < a.num_tiles; w += gridDim.x) {
+    // after a grid pass: only the blocks whose Gram matrix was not
+    // numerically positive definite there (their basis is still the old one)
+    if (a.ctl && (a.ctl[w].skip || a.ctl[w].conv)) continue;
     const Tile t = a.tiles[w];
     const MatInfo mi = a.info[t.mat];
     const int k = mi.k;

@@ -449,6 +449,61 @@ def test_orth_refresh_shifted_pass_on_ill_conditioned_blocks():
         assert np.linalg.norm(np.tril(Q[b].T @ T, -1)) <= 1e-4 * np.linalg.norm(T)
 
 
+@pytest.mark.parametrize("k", [64, 100, 400])
+def test_orth_grid_and_one_cta_forms_agree(k):
+    """Blocks at least 64 wide run the orthogonal iteration on the grid
+    (batched tile products, a Cholesky factorisation per block, the
+    triangular solve split by 64-row panels); the one-CTA form runs the same
+    steps in one CTA per block.  Three steps from a Haar start: both match the
+    fp64 oracle to the fp32 perturbation bound, and their Rayleigh quotients
+    agree."""
+    B, cond, steps = 3, 50.0, 3
+    A, Q0 = _orth_case(k, B, cond, seed=300 + k)
+    Qr, lr = O.orthogonal_iteration(A, Q0, steps)
+    out = []
+    for grid in (True, False):
+        opt = _dobb([(4, B * k)], B, refresh_period=0, refresh="orth", orth_steps=steps)
+        if not grid:
+            opt.set_eig_grid(0)
+        _load(opt, A, Q0, k, B)
+        opt.refresh()
+        torch.cuda.synchronize()
+        assert np.all(opt.block_flags() == 0)
+        Q = to_np(opt.tensor("bases", 0))
+        lam = to_np(opt.tensor("eigvals", 0))
+        for b in range(B):
+            assert np.linalg.norm(Q[b].T @ Q[b] - np.eye(k)) <= 1e-5 * np.sqrt(k)
+            assert np.linalg.norm(Q[b] - Qr[b]) <= 20 * cond * k * 2.0 ** -24 * steps
+            assert np.abs(lam[b] - lr[b]).max() <= 1e-5 * np.abs(lr[b]).max()
+        out.append((Q, lam))
+    assert np.abs(out[0][1] - out[1][1]).max() <= 2e-5 * np.abs(out[1][1]).max()
+
+
+def test_orth_grid_hands_ill_conditioned_blocks_to_the_shifted_passes():
+    """A batch mixing well- and ill-conditioned 100-wide blocks on the grid:
+    the well-conditioned blocks finish there (no shifted pass), the others
+    (Gram matrix of T not positive definite in fp32) are redone from their
+    old basis by the one-CTA shifted passes; every block ends orthonormal with
+    Q^T T upper triangular."""
+    k, B = 100, 4
+    rng = np.random.default_rng(9)
+    conds = [50.0, 1e6, 50.0, 1e6]
+    A = np.stack([I.spd_with_gap(k, rng, cond=c)[0] for c in conds]).astype(np.float32).astype(np.float64)
+    Q0 = np.stack([I.haar_orthogonal(k, rng) for _ in range(B)]).astype(np.float32).astype(np.float64)
+    opt = _dobb([(4, B * k)], B, refresh_period=0, refresh="orth", orth_steps=1)
+    _load(opt, A, Q0, k, B)
+    opt.refresh()
+    torch.cuda.synchronize()
+    assert np.all(opt.block_flags() == 0)
+    st = opt.block_stats()
+    Q = to_np(opt.tensor("bases", 0))
+    for b in range(B):
+        T = A[b] @ Q0[b]
+        assert np.linalg.norm(Q[b].T @ Q[b] - np.eye(k)) <= 1e-5 * np.sqrt(k)
+        assert np.linalg.norm(np.tril(Q[b].T @ T, -1)) <= 1e-4 * np.linalg.norm(T)
+        assert (st[b, 3] >= 1.0) == (conds[b] > 1e3)
+
+
 @pytest.mark.parametrize("pdt", ["f32", "bf16"])
 def test_run_with_orth_refresh_matches_oracle_updates(pdt):
     """A short run refreshing by one orthogonal-iteration step every 2 steps:
