@@ -560,12 +560,13 @@ __global__ void __launch_bounds__(kThreads, 4) gj_apply_kernel(const __grid_cons
       }
     }
   } else {
-    load_corr(Et, Rb + (int64_t)t * nn, n2);
     const int c1 = min(nI, c0 + kPanelRun);
-    for (int c = c0; c < c1; ++c) {
+    // the next panel's V tile loads into registers while this one is
+    // multiplied (panels are disjoint row ranges of V)
+    float v[kRowsPerWarp][2];
+    auto load_panel = [&](int c) {
       const int i0 = c * kT;
       const bool ok0 = i0 + lane < k, ok1 = i0 + lane + 32 < k;
-      float v[kRowsPerWarp][2];
 #pragma unroll
       for (int i = 0; i < kRowsPerWarp; ++i) {
         const int cr = colT[warp + (kThreads / 32) * i];
@@ -573,6 +574,12 @@ __global__ void __launch_bounds__(kThreads, 4) gj_apply_kernel(const __grid_cons
         v[i][0] = (cr < k && ok0) ? row[lane] : 0.f;
         v[i][1] = (cr < k && ok1) ? row[lane + 32] : 0.f;
       }
+    };
+    load_panel(c0);
+    load_corr(Et, Rb + (int64_t)t * nn, n2);
+    for (int c = c0; c < c1; ++c) {
+      const int i0 = c * kT;
+      const bool ok0 = i0 + lane < k, ok1 = i0 + lane + 32 < k;
       // Xs is free: the previous panel's product ended before the barrier
       // that preceded its write-back
 #pragma unroll
@@ -581,6 +588,7 @@ __global__ void __launch_bounds__(kThreads, 4) gj_apply_kernel(const __grid_cons
         Xs[r * kLdM + lane] = v[i][0];
         Xs[r * kLdM + lane + 32] = v[i][1];
       }
+      if (c + 1 < c1) load_panel(c + 1);
       __syncthreads();
       mma_load_acc<true>(Xs, acc);                      // V rows i, table columns q
       if (precise) corr_product<3>(Xs, Et, n2, acc);    // V + V E_t
