@@ -770,11 +770,10 @@ def run_e2e(torch, opt, cfg, shapes, lay, sides, W, K, stream, params, world):
     (two independently drawn host sets, alternating) and copies the updated
     parameters back to pinned host memory; the inputs and parameters of all
     matrices sit in one flat buffer per kind (a flat parameter buffer, as a
-    training loop keeps them), so a step moves three contiguous copies.  The
-    input copies of step i+1 run on two copy streams during step i
-    (double-buffered device inputs); the parameter copy of step i runs on a
-    third stream during step i+1's accumulate, and step i+1's update waits
-    for it."""
+    training loop keeps them).  The input copies of step i+1 run during step i
+    (double-buffered device inputs): the activations in two halves on two copy
+    streams, then the gradients; the parameter copy of step i runs on a third
+    stream during step i+1's accumulate, and step i+1's update waits for it."""
     dev = W[0].device
     Xs2, Gs2, _ = make_train_inputs(torch, dict(cfg, pool=2), shapes, lay, dev, seed=777,
                                     pool=2, sides=sides)
@@ -819,15 +818,27 @@ def run_e2e(torch, opt, cfg, shapes, lay, sides, W, K, stream, params, world):
     g_used = [torch.cuda.Event() for _ in range(2)]
     w_ready, w_out = torch.cuda.Event(), torch.cuda.Event()
 
+    half_done = [torch.cuda.Event() for _ in range(2)]
+
     def issue(i):
+        # the activations in two halves on two copy streams (one large copy
+        # alone runs well below the link rate), then the gradients
         b = i % 2
-        for cs, dst, src, used, done in ((cx, Xd[b][0], Xh[b], x_used[b], x_done[b]),
-                                         (cg, Gd[b][0], Gh[b], g_used[b], g_done[b])):
-            if i >= 2:
-                cs.wait_event(used)
-            with torch.cuda.stream(cs):
-                dst.copy_(src, non_blocking=True)
-            done.record(cs)
+        if i >= 2:
+            cx.wait_event(x_used[b])
+            cx.wait_event(g_used[b])
+            cg.wait_event(x_used[b])
+        h = Xh[b].numel() // 2
+        with torch.cuda.stream(cg):
+            Xd[b][0][h:].copy_(Xh[b][h:], non_blocking=True)
+        half_done[b].record(cg)
+        with torch.cuda.stream(cx):
+            Xd[b][0][:h].copy_(Xh[b][:h], non_blocking=True)
+        cx.wait_event(half_done[b])
+        x_done[b].record(cx)
+        with torch.cuda.stream(cx):
+            Gd[b][0].copy_(Gh[b], non_blocking=True)
+        g_done[b].record(cx)
 
     torch.cuda.synchronize()
     t0 = time.perf_counter()
@@ -865,8 +876,9 @@ def run_e2e(torch, opt, cfg, shapes, lay, sides, W, K, stream, params, world):
             "wall_ms_per_step": (time.perf_counter() - t0) * 1e3 / K,
             "host_link": link,
             "copy_floor_ms": max(h2d / (link["h2d_gbs"] * 1e9), d2h / (link["d2h_gbs"] * 1e9)) * 1e3,
-            "overlap": "inputs of step i+1 copied on two streams during step i; parameters of "
-                       "step i copied back during step i+1's accumulate; one flat buffer per kind"}
+            "overlap": "inputs of step i+1 copied during step i (activations in two halves on two "
+                       "streams, then gradients); parameters of step i copied back during step i+1's "
+                       "accumulate; one flat buffer per kind"}
 
 
 def _relaunch_distributed(args):
