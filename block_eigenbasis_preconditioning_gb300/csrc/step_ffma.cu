@@ -26,13 +26,14 @@ constexpr int kCG = kThreads / kRG;
 constexpr int kNC = kCG * 4;    // output columns per pass (128)
 constexpr int kKC = 32;         // reduction chunk
 constexpr int kQS = kNC + 4;    // padded row of the Q stage
+constexpr int kMS = kTM + 4;    // padded row of the M / S chunk, stored [reduction index][row]
 constexpr int kL2MaxPass = 8;   // column passes of the l2 norm kernel
 
 __host__ __device__ __forceinline__ int pad16(int k) { return (k + 15) & ~15; }
 
 __host__ __device__ __forceinline__ size_t smem_bytes(int k) {
-  return (size_t)4 * kTM * pad16(k)                  // S (fp32)
-         + (size_t)4 * (kKC * kQS + kTM * (kKC + 1));  // Q stage + M / S chunk
+  return (size_t)4 * kTM * pad16(k)              // S (fp32)
+         + (size_t)4 * (kKC * kQS + kKC * kMS);    // Q stage + M / S chunk
 }
 
 // One basis element as the update multiplies with it (bf16 basis storage:
@@ -40,6 +41,23 @@ __host__ __device__ __forceinline__ size_t smem_bytes(int k) {
 __device__ __forceinline__ float basis_at(const float* Qb, int64_t idx, int basis_bf16) {
   const float v = Qb[idx];
   return basis_bf16 ? __bfloat162float(__float2bfloat16_rn(v)) : v;
+}
+
+// acc += A B over `len` reduction indices of one staged chunk: A = the M / S
+// chunk ([index][row], rows rg 4 .. rg 4 + 3), B = the Q stage ([index][col],
+// columns cg 4 .. cg 4 + 3): two 16-byte shared loads per 16 FMAs (the A
+// load is a broadcast: a warp is one row group).
+__device__ __forceinline__ void chunk_product(const float* Ac, const float* Bs, int len, int rg, int cg,
+                                              float (&acc)[4][4]) {
+  for (int ll = 0; ll < len; ++ll) {
+    const float4 a4 = *reinterpret_cast<const float4*>(Ac + ll * kMS + rg * 4);
+    const float4 b4 = *reinterpret_cast<const float4*>(Bs + ll * kQS + cg * 4);
+    const float av[4] = {a4.x, a4.y, a4.z, a4.w}, bv[4] = {b4.x, b4.y, b4.z, b4.w};
+#pragma unroll
+    for (int p = 0; p < 4; ++p)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) acc[p][q] = fmaf(av[p], bv[q], acc[p][q]);
+  }
 }
 
 // acc[p][q] = C(rg 4 + p, jc + cg 4 + q) = sum_l M(row0 + rg 4 + p, l) Q(l, jc + cg 4 + q)
@@ -64,21 +82,10 @@ __device__ __forceinline__ void project_pass(const float* Mg, const float* Qb, i
       const int r = e / kKC, ll = e % kKC;
       float v = 0.f;
       if (r < rows && l0 + ll < k) v = Mg[(int64_t)(row0 + r) * n + col0 + l0 + ll];
-      Mc[r * (kKC + 1) + ll] = v;
+      Mc[ll * kMS + r] = v;
     }
     __syncthreads();
-    const int lmax = min(kKC, k - l0);
-    for (int ll = 0; ll < lmax; ++ll) {
-      float av[4], bv[4];
-#pragma unroll
-      for (int p = 0; p < 4; ++p) av[p] = Mc[(rg * 4 + p) * (kKC + 1) + ll];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) bv[q] = Qs[ll * kQS + cg * 4 + q];
-#pragma unroll
-      for (int p = 0; p < 4; ++p)
-#pragma unroll
-        for (int q = 0; q < 4; ++q) acc[p][q] = fmaf(av[p], bv[q], acc[p][q]);
-    }
+    chunk_product(Mc, Qs, min(kKC, k - l0), rg, cg, acc);
     __syncthreads();
   }
 }
@@ -181,21 +188,10 @@ step_ffma_kernel(const __grid_constant__ StepArgs a) {
         }
         for (int e = tid; e < kTM * kKC; e += kThreads) {
           const int r = e / kKC, jj = e % kKC;
-          Mc[r * (kKC + 1) + jj] = (j0 + jj < k) ? Ss[r * kp + j0 + jj] : 0.f;
+          Mc[jj * kMS + r] = (j0 + jj < k) ? Ss[r * kp + j0 + jj] : 0.f;
         }
         __syncthreads();
-        const int jmax = min(kKC, k - j0);
-        for (int jj = 0; jj < jmax; ++jj) {
-          float av[4], bv[4];
-#pragma unroll
-          for (int p = 0; p < 4; ++p) av[p] = Mc[(rg * 4 + p) * (kKC + 1) + jj];
-#pragma unroll
-          for (int q = 0; q < 4; ++q) bv[q] = Qs[jj * kQS + cg * 4 + q];
-#pragma unroll
-          for (int p = 0; p < 4; ++p)
-#pragma unroll
-            for (int q = 0; q < 4; ++q) acc[p][q] = fmaf(av[p], bv[q], acc[p][q]);
-        }
+        chunk_product(Mc, Qs, min(kKC, k - j0), rg, cg, acc);
         __syncthreads();
       }
 #pragma unroll
