@@ -72,7 +72,7 @@ def _measured_peaks():
             p = json.load(f)
         return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
                 "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
-                "source": "MEASURED_PEAKS.json (driver: copy bandwidth, cuBLAS bf16)"}
+                "source": "MEASURED_PEAKS.json (copy bandwidth, cuBLAS bf16)"}
     except Exception:
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
                 "source": "fallback"}
