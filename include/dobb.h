@@ -179,7 +179,12 @@ dobb_status dobb_set_side(dobb_handle h, int matrix, int side, void* stream);
  *   T = A_b Q_b and R = chol(T^T T) (Table 16: Cholesky QR; computed as
  *   CholeskyQR2 in fp32, with a shifted first pass when T^T T is not
  *   numerically positive definite); Lambda_b holds the Rayleigh quotients
- *   diag(Q_b^T A_b Q_b).  A block whose QR fails keeps its basis and gets
+ *   diag(Q_b^T A_b Q_b).  Blocks at least as wide as dobb_set_eig_grid's
+ *   min_k run on the grid (batched products, a Cholesky factorisation per
+ *   block, the triangular solve by 64-row panels); a block whose Gram
+ *   matrix is not numerically positive definite there is redone from its
+ *   old basis with the shifted passes, one CTA per block, like the narrower
+ *   blocks.  A block whose QR fails keeps its basis and gets
  *   DOBB_FLAG_NOT_CONVERGED.
  * DOBB_ERR_INVALID_ARG for another method or steps < 1.  Takes effect at the
  * next refresh. */
@@ -204,8 +209,9 @@ dobb_status dobb_set_refresh_period(dobb_handle h, int refresh_period);
  * grid solver (every table, tile pair and panel of a sweep its own CTA, a
  * launch per phase over a batch of blocks of one width; the call then
  * synchronises `stream` once per sweep), narrower ones one CTA per block.
- * Both run the same restarted Rayleigh-Ritz two-sided Jacobi.  0 = never the
- * grid solver; otherwise min_k >= 64.  A batch holds the blocks of one width
+ * Both run the same restarted Rayleigh-Ritz two-sided Jacobi.  The same
+ * threshold and batches apply to the orthogonal-iteration refresh (no
+ * synchronisation there).  0 = never the grid solver; otherwise min_k >= 64.  A batch holds the blocks of one width
  * whose scratch (12 k^2 bytes each) fits `batch_bytes` (at least one block;
  * 0 = all blocks of that width).  Defaults: 64, 0.  DOBB_ERR_INVALID_ARG for
  * other values. */
